@@ -1,0 +1,27 @@
+"""Float64 CPU oracle of the SpecPrefill scoring path — TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import anything here. The CUDA library and its Python binding never
+do, and share no code with it. Parity of the whole oracle is pinned by the
+``-m "not gpu"`` tests (brute-force twin, closed forms, library routines and
+invariants); no function here is left unpinned.
+"""
+
+from .specprefill_oracle import (  # noqa: F401
+    attention_rows,
+    avg_pool,
+    chunk_means,
+    chunk_offsets,
+    decode_bf16,
+    finish_selection,
+    fixed_count,
+    min_max_normalize,
+    rank_order,
+    run,
+    select_fixed,
+    select_from_chunk_scores,
+    select_mass,
+    step_importance,
+    structural_boost,
+    token_importance,
+)

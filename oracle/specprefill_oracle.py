@@ -1,0 +1,320 @@
+"""Float64 CPU oracle of the SpecPrefill token-importance and chunk-selection path.
+
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+baseline leg may import this module. The product (the CUDA library and its
+binding) never calls it, and it shares no code with that product.
+
+Each function is one step of the method, in the order the pages give it, in
+plain numpy float64 (inputs are bf16 bit patterns decoded exactly):
+
+1. logits   s = scale * <q, k>, scale = 1/sqrt(d)            (PR "Speculative
+   prefill" §Approach item 2; guide "SpecPrefill — Implementation Guide"
+   §Sliding Window / The OOM Problem: the attention matrix is Q @ K^T)
+2. softmax  over the prompt's N keys                          (guide §How It
+   Works / Attention Capture: post-softmax kq_soft_max rows)
+3. max over heads, then max over layers                       (guide §How It
+   Works / Token Importance, steps 2-3; listing `compute_imp`)
+4. mean over lookahead steps                                  (same section)
+5. 1D average pool, W = 13, centred, in-range divisor         (PR §Approach
+   item 3)
+6. min-max normalisation to [0, 1]                            (guide v3.1,
+   §v3.1 Optimizations item 5)
+7. structural boost: first 64 tokens x1.5, last 128 x1.3      (guide v3,
+   §v3 Improvements item 2)
+8. chunk score = mean over a 32-token contiguous chunk        (guide §Chunk
+   Selection; listing `select_chunks`)
+9-10. rank chunks (score descending, index ascending) and keep either the
+   top k = max(1, ceil(nc * p)) or the shortest prefix whose cumulative
+   score reaches mass * total                                 (guide v3,
+   §v3 Improvements item 1; listing `select_chunks`)
+11. force BOS (token 0) and the final chunk                   (PR §Approach
+   item 4)
+12. kept-token list with original position IDs                (guide §How It
+   Works / Sparse Prefill)
+
+Readings where the pages are silent (each also listed in the design notes):
+softmax over the prompt keys only; kv head = h // G; the pool divides by the
+number of in-range tokens and never crosses a prompt boundary; normalisation
+of a constant vector gives all ones; boost factors multiply where the two
+regions overlap; ties in the ranking break by ascending chunk index and the
+fixed mode keeps exactly k chunks; a chunk's mass is its score, the crossing
+chunk is kept, forced chunks do not count, and zero total mass keeps all;
+forced chunks/tokens are added after the ranking selection.
+"""
+
+import math
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# input decoding
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> exact float64 values (bf16 is the top half of fp32)."""
+    u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def as_f32(x: float) -> float:
+    """The float64 value of a float32 parameter (p and mass are float32 inputs)."""
+    return float(np.float32(x))
+
+
+# ---------------------------------------------------------------------------
+# steps 1-4: attention rows and token importance
+
+
+def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, start: int, n: int,
+                   layer: int, kv_head: int, group: int,
+                   scale: Optional[float] = None) -> np.ndarray:
+    """Softmax rows of one (layer, KV head) for one prompt.
+
+    q_bits: [Ly, L, Hq, d] of the prompt; k_bits: [Ly, Ntot, Hk, d].
+    Returns p[l, j, t] for lookahead step l, query head h = kv_head*group + j,
+    prompt key t in [0, n). Steps 1 and 2.
+    """
+    d = q_bits.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    keys = decode_bf16(k_bits[layer, start:start + n, kv_head, :])            # [n, d]
+    heads = slice(kv_head * group, (kv_head + 1) * group)
+    queries = decode_bf16(q_bits[layer, :, heads, :])                           # [L, G, d]
+    n_steps = queries.shape[0]
+    s = (queries.reshape(-1, d) @ keys.T).reshape(n_steps, group, n) * scale    # step 1
+    s_max = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - s_max)
+    return e / e.sum(axis=-1, keepdims=True)                                     # step 2
+
+
+def step_importance(q_bits: np.ndarray, k_bits: np.ndarray, start: int, n: int,
+                    n_kv_heads: int, scale: Optional[float] = None) -> np.ndarray:
+    """A[l, t] = max over layers and query heads of p (step 3), shape [L, n]."""
+    n_layers, n_steps, n_q_heads, _ = q_bits.shape
+    group = n_q_heads // n_kv_heads
+    a = np.full((n_steps, n), -np.inf)
+    for layer in range(n_layers):
+        for g in range(n_kv_heads):
+            p = attention_rows(q_bits, k_bits, start, n, layer, g, group, scale)
+            a = np.maximum(a, p.max(axis=1))
+    return a
+
+
+def token_importance(step_max: np.ndarray) -> np.ndarray:
+    """imp[t] = mean over lookahead steps of A[l, t] (step 4)."""
+    return step_max.sum(axis=0) / step_max.shape[0]
+
+
+# ---------------------------------------------------------------------------
+# steps 5-8: smoothing, normalisation, boost, chunk scores
+
+
+def avg_pool(imp: np.ndarray, width: int) -> np.ndarray:
+    """Centred moving average of odd ``width``; the divisor counts only the
+    window positions inside [0, n) (step 5)."""
+    n = imp.shape[0]
+    half = width // 2
+    padded = np.concatenate([np.zeros(half), imp, np.zeros(half)])
+    sums = np.lib.stride_tricks.sliding_window_view(padded, width).sum(axis=1)
+    t = np.arange(n)
+    counts = np.minimum(t + half, n - 1) - np.maximum(t - half, 0) + 1
+    return sums / counts
+
+
+def min_max_normalize(x: np.ndarray) -> np.ndarray:
+    """(x - min) / (max - min); a constant vector maps to all ones (step 6)."""
+    lo, hi = x.min(), x.max()
+    if hi == lo:
+        return np.ones_like(x)
+    return (x - lo) / (hi - lo)
+
+
+def structural_boost(x: np.ndarray, first_mult: float, first_n: int,
+                     last_mult: float, last_n: int) -> np.ndarray:
+    """Multiply positions t < first_n by first_mult, then t >= n - last_n by
+    last_mult (step 7). Multipliers are float32 parameters."""
+    y = x.copy()
+    n = y.shape[0]
+    t = np.arange(n)
+    y[t < first_n] *= as_f32(first_mult)
+    y[t >= n - last_n] *= as_f32(last_mult)
+    return y
+
+
+def chunk_means(x: np.ndarray, chunk: int) -> np.ndarray:
+    """Mean score of each contiguous chunk; the last chunk may be partial (step 8)."""
+    n = x.shape[0]
+    nc = (n + chunk - 1) // chunk
+    return np.array([x[c * chunk:min((c + 1) * chunk, n)].mean() for c in range(nc)])
+
+
+# ---------------------------------------------------------------------------
+# steps 9-12: ranking, selection, forcing, kept list
+
+
+def rank_order(cs: np.ndarray) -> np.ndarray:
+    """Chunk indices sorted by score descending, then index ascending (step 9)."""
+    idx = np.arange(cs.shape[0])
+    return np.lexsort((idx, -cs))
+
+
+def fixed_count(nc: int, keep_p: float) -> int:
+    """k = max(1, ceil(nc * p)), evaluated in float64 on the float32 p."""
+    return max(1, int(math.ceil(nc * as_f32(keep_p))))
+
+
+def select_fixed(cs: np.ndarray, keep_p: float) -> np.ndarray:
+    """Boolean mask of the top-k chunks of the ranking (step 10, fixed mode)."""
+    order = rank_order(cs)
+    k = min(fixed_count(cs.shape[0], keep_p), cs.shape[0])
+    sel = np.zeros(cs.shape[0], dtype=bool)
+    sel[order[:k]] = True
+    return sel
+
+
+def select_mass(cs: np.ndarray, mass: float) -> np.ndarray:
+    """Walk the ranking, keeping chunks until the running sum of their scores
+    reaches mass * (sum of all scores); the crossing chunk is kept. Zero total
+    mass keeps every chunk (step 10, mass mode)."""
+    nc = cs.shape[0]
+    sel = np.zeros(nc, dtype=bool)
+    total = float(np.sum(cs))
+    if not total > 0.0:
+        sel[:] = True
+        return sel
+    theta = as_f32(mass) * total
+    cum = 0.0
+    for c in rank_order(cs):
+        sel[c] = True
+        cum += float(cs[c])
+        if cum >= theta:
+            break
+    return sel
+
+
+@dataclass
+class Selection:
+    chunk_keep: np.ndarray   # uint8 per chunk: bit0 ranked-selected, bit1 forced final chunk
+    kept_tokens: np.ndarray  # int64 sorted token positions within the prompt
+
+
+def finish_selection(sel: np.ndarray, n: int, chunk: int, force_bos: bool,
+                     force_last_chunk: bool) -> Selection:
+    """Add the forced final chunk and BOS token, expand chunks to tokens
+    (steps 11-12)."""
+    nc = sel.shape[0]
+    flags = sel.astype(np.uint8)
+    if force_last_chunk:
+        flags[nc - 1] |= 2
+    toks: List[int] = []
+    for c in range(nc):
+        if flags[c]:
+            toks.extend(range(c * chunk, min((c + 1) * chunk, n)))
+    if force_bos and not flags[0]:
+        toks.append(0)
+    return Selection(chunk_keep=flags, kept_tokens=np.array(sorted(toks), dtype=np.int64))
+
+
+# ---------------------------------------------------------------------------
+# whole path
+
+
+def score_prompt(imp: np.ndarray, *, pool_w: int, chunk: int, normalize: bool,
+                 boost_first_mult: float, boost_first_n: int,
+                 boost_last_mult: float, boost_last_n: int) -> Dict[str, np.ndarray]:
+    """Steps 5-8 for one prompt."""
+    x = avg_pool(imp, pool_w)
+    y = min_max_normalize(x) if normalize else x
+    y = structural_boost(y, boost_first_mult, boost_first_n, boost_last_mult, boost_last_n)
+    return {"tok_score": x, "final_score": y, "chunk_score": chunk_means(y, chunk)}
+
+
+def select_prompt(cs: np.ndarray, n: int, *, chunk: int, mode: str, keep_p: float,
+                  mass: float, force_bos: bool, force_last_chunk: bool) -> Selection:
+    """Steps 9-12 for one prompt."""
+    if mode == "fixed":
+        sel = select_fixed(cs, keep_p)
+    elif mode == "mass":
+        sel = select_mass(cs, mass)
+    else:
+        raise ValueError(mode)
+    return finish_selection(sel, n, chunk, force_bos, force_last_chunk)
+
+
+def chunk_offsets(seq_off: np.ndarray, chunk: int) -> np.ndarray:
+    lengths = np.diff(np.asarray(seq_off, dtype=np.int64))
+    out = np.zeros(len(lengths) + 1, dtype=np.int64)
+    out[1:] = np.cumsum((lengths + chunk - 1) // chunk)
+    return out
+
+
+def select_from_chunk_scores(chunk_score: np.ndarray, seq_off: np.ndarray, *, chunk: int,
+                             mode: str, keep_p: float, mass: float, force_bos: bool,
+                             force_last_chunk: bool, **_unused) -> Dict[str, np.ndarray]:
+    """Steps 9-12 over a packed batch of given chunk scores."""
+    seq_off = np.asarray(seq_off, dtype=np.int64)
+    coff = chunk_offsets(seq_off, chunk)
+    keep, idx, pos, koff = [], [], [], [0]
+    for b in range(len(seq_off) - 1):
+        n = int(seq_off[b + 1] - seq_off[b])
+        cs = np.asarray(chunk_score[coff[b]:coff[b + 1]], dtype=np.float64)
+        s = select_prompt(cs, n, chunk=chunk, mode=mode, keep_p=keep_p, mass=mass,
+                          force_bos=force_bos, force_last_chunk=force_last_chunk)
+        keep.append(s.chunk_keep)
+        idx.append(s.kept_tokens + seq_off[b])
+        pos.append(s.kept_tokens)
+        koff.append(koff[-1] + len(s.kept_tokens))
+    return {
+        "chunk_off": coff,
+        "chunk_keep": np.concatenate(keep),
+        "kept_idx": np.concatenate(idx),
+        "kept_pos": np.concatenate(pos),
+        "kept_off": np.array(koff, dtype=np.int64),
+    }
+
+
+def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
+        pool_w: int = 13, chunk: int = 32, mode: str = "fixed", keep_p: float = 0.30,
+        mass: float = 0.85, normalize: bool = True, boost_first_mult: float = 1.5,
+        boost_first_n: int = 64, boost_last_mult: float = 1.3, boost_last_n: int = 128,
+        force_bos: bool = True, force_last_chunk: bool = True,
+        scale: Optional[float] = None, keep_step_max: bool = False) -> Dict[str, np.ndarray]:
+    """The whole path over a packed batch.
+
+    q_bits: [B, Ly, L, Hq, d] bf16 bits; k_bits: [Ly, Ntot, Hk, d] bf16 bits;
+    seq_off: [B+1] prompt offsets into the token axis of k.
+    Returns float64 imp / tok_score / final_score (per token), chunk_score and
+    chunk_keep (per chunk), and the kept lists (packed index, position,
+    per-prompt offsets).
+    """
+    seq_off = np.asarray(seq_off, dtype=np.int64)
+    n_kv_heads = k_bits.shape[2]
+    imps, toks, finals, chunks, steps = [], [], [], [], []
+    for b in range(len(seq_off) - 1):
+        start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
+        a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale)
+        imp = token_importance(a)
+        sc = score_prompt(imp, pool_w=pool_w, chunk=chunk, normalize=normalize,
+                          boost_first_mult=boost_first_mult, boost_first_n=boost_first_n,
+                          boost_last_mult=boost_last_mult, boost_last_n=boost_last_n)
+        imps.append(imp)
+        toks.append(sc["tok_score"])
+        finals.append(sc["final_score"])
+        chunks.append(sc["chunk_score"])
+        if keep_step_max:
+            steps.append(a)
+    out = {
+        "imp": np.concatenate(imps),
+        "tok_score": np.concatenate(toks),
+        "final_score": np.concatenate(finals),
+        "chunk_score": np.concatenate(chunks),
+    }
+    out.update(select_from_chunk_scores(out["chunk_score"], seq_off, chunk=chunk, mode=mode,
+                                        keep_p=keep_p, mass=mass, force_bos=force_bos,
+                                        force_last_chunk=force_last_chunk))
+    if keep_step_max:
+        out["step_max"] = steps
+    return out

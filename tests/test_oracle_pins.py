@@ -1,0 +1,259 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each test checks the oracle against the brute-force twin (independent
+pure-Python loops and subset enumeration), a library routine (scipy/torch
+softmax, numpy convolution), a closed form, or an invariant the method's
+definition implies. CPU only.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from oracle import bruteforce
+from oracle import specprefill_oracle as so
+from synth import bf16_bits_from_f32, get_workload, make_inputs
+from tests._cases import random_case
+
+TINY_CASES = [
+    # lengths, Ly, Hq, Hk, d, L, params
+    dict(lengths=[40], shape=(1, 2, 1, 8, 2), q_gain=3.0,
+         params=dict(pool_w=3, chunk=4, mode="fixed", keep_p=0.3, normalize=False,
+                     boost_first_mult=1.0, boost_last_mult=1.0)),
+    dict(lengths=[37, 23], shape=(2, 4, 2, 4, 3), q_gain=2.0,
+         params=dict(pool_w=5, chunk=4, mode="mass", mass=0.6, normalize=True,
+                     boost_first_mult=1.5, boost_first_n=5, boost_last_mult=1.3, boost_last_n=7)),
+    dict(lengths=[45], shape=(2, 2, 2, 6, 1), q_gain=2.5,
+         params=dict(pool_w=13, chunk=5, mode="mass", mass=0.85, normalize=True,
+                     boost_first_mult=1.5, boost_first_n=8, boost_last_mult=1.3, boost_last_n=9)),
+    dict(lengths=[1, 2, 30], shape=(1, 2, 1, 4, 2), q_gain=2.0,
+         params=dict(pool_w=13, chunk=3, mode="fixed", keep_p=0.15, normalize=True,
+                     boost_first_mult=2.0, boost_first_n=2, boost_last_mult=1.25, boost_last_n=3)),
+    dict(lengths=[33, 19], shape=(1, 3, 3, 5, 2), q_gain=1.5,
+         params=dict(pool_w=7, chunk=4, mode="fixed", keep_p=0.5, normalize=False,
+                     boost_first_mult=1.5, boost_first_n=4, boost_last_mult=1.3, boost_last_n=4,
+                     force_bos=False, force_last_chunk=False, scale=0.37)),
+]
+
+
+def _case(i):
+    c = TINY_CASES[i]
+    ly, hq, hk, d, steps = c["shape"]
+    q, k, off = random_case(100 + i, c["lengths"], ly, hq, hk, d, steps, q_gain=c["q_gain"])
+    return q, k, off, c["params"]
+
+
+@pytest.mark.parametrize("i", range(len(TINY_CASES)))
+def test_oracle_matches_bruteforce(i):
+    q, k, off, params = _case(i)
+    got = oracle.run(q, k, off, **params)
+    want = bruteforce.run_bruteforce(q, k, off, **params)
+    for key in ("imp", "tok_score", "final_score", "chunk_score"):
+        np.testing.assert_allclose(got[key], want[key], rtol=1e-12, atol=1e-15, err_msg=key)
+    for key in ("chunk_keep", "kept_idx", "kept_pos", "kept_off"):
+        np.testing.assert_array_equal(np.asarray(got[key]), np.asarray(want[key]), err_msg=key)
+
+
+def test_single_row_is_textbook_softmax():
+    """Ly=Hq=Hk=L=1, W=1, no normalisation/boost: imp is one softmax row."""
+    q, k, off = random_case(7, [300], 1, 1, 1, 64, 1, q_gain=2.0)
+    out = oracle.run(q, k, off, pool_w=1, chunk=32, normalize=False,
+                     boost_first_mult=1.0, boost_last_mult=1.0)
+    qf = so.decode_bf16(q[0, 0, 0, 0])
+    kf = so.decode_bf16(k[0, :, 0, :])
+    logits = kf @ qf / 8.0
+    np.testing.assert_allclose(out["imp"], scipy.special.softmax(logits), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(out["tok_score"], out["imp"], rtol=0, atol=0)
+
+
+def test_softmax_rows_sum_to_one_and_importance_bounds():
+    q, k, off = random_case(8, [257], 3, 4, 2, 16, 3, q_gain=3.0)
+    for layer in range(3):
+        for g in range(2):
+            p = oracle.attention_rows(q[0], k, 0, 257, layer, g, 2)
+            assert p.shape == (3, 2, 257)
+            assert np.all(p > 0)
+            np.testing.assert_allclose(p.sum(axis=-1), 1.0, rtol=0, atol=1e-12)
+    a = oracle.step_importance(q[0], k, 0, 257, 2)
+    sums = a.sum(axis=1)
+    assert np.all(sums >= 1.0 - 1e-12) and np.all(sums <= 3 * 4 + 1e-12)
+
+
+def test_importance_permutation_invariance():
+    q, k, off = random_case(9, [200], 3, 6, 2, 8, 2, q_gain=2.0)
+    base = oracle.run(q, k, off)["imp"]
+    # permute query heads inside each group of 3
+    perm = np.array([2, 0, 1, 4, 5, 3])
+    assert np.array_equal(oracle.run(q[:, :, :, perm], k, off)["imp"], base)
+    # permute layers (queries and keys together)
+    lp = np.array([1, 2, 0])
+    assert np.array_equal(oracle.run(q[:, lp], k[lp], off)["imp"], base)
+    # swap KV heads together with their query groups
+    assert np.array_equal(oracle.run(q[:, :, :, [3, 4, 5, 0, 1, 2]], k[:, :, ::-1], off)["imp"], base)
+
+
+def test_pool_properties():
+    rng = np.random.default_rng(3)
+    v = rng.random(101)
+    # W = 1 is the identity
+    np.testing.assert_array_equal(oracle.avg_pool(v, 1), v)
+    # constant in -> same constant out, including the edges
+    np.testing.assert_allclose(oracle.avg_pool(np.full(50, 0.25), 13), 0.25, rtol=1e-15)
+    np.testing.assert_allclose(oracle.avg_pool(np.full(5, 0.5), 13), 0.5, rtol=1e-15)
+    # interior equals numpy's convolution with a box kernel
+    w = 13
+    interior = np.convolve(v, np.ones(w), mode="valid") / w
+    np.testing.assert_allclose(oracle.avg_pool(v, w)[w // 2:-(w // 2)], interior, rtol=1e-14)
+    # edges divide by the number of in-range tokens
+    x = oracle.avg_pool(v, w)
+    assert math.isclose(x[0], v[:7].mean(), rel_tol=1e-14)
+    assert math.isclose(x[3], v[:10].mean(), rel_tol=1e-14)
+    assert math.isclose(x[-1], v[-7:].mean(), rel_tol=1e-14)
+
+
+def test_normalize_closed_form():
+    np.testing.assert_allclose(oracle.min_max_normalize(np.array([2.0, 4.0, 6.0, 3.0])),
+                               [0.0, 0.5, 1.0, 0.25], rtol=0, atol=0)
+    np.testing.assert_array_equal(oracle.min_max_normalize(np.full(7, 3.5)), np.ones(7))
+    y = oracle.min_max_normalize(np.random.default_rng(1).random(99))
+    assert y.min() == 0.0 and y.max() == 1.0
+
+
+def test_boost_positions():
+    n = 300
+    y = oracle.structural_boost(np.ones(n), 1.5, 64, 1.3, 128)
+    f13 = float(np.float32(1.3))
+    assert y[0] == 1.5 and y[63] == 1.5 and y[64] == 1.0
+    assert y[n - 129] == 1.0 and y[n - 128] == f13 and y[n - 1] == f13
+    # overlap (n < 192): both factors apply
+    y = oracle.structural_boost(np.ones(100), 1.5, 64, 1.3, 128)
+    assert y[0] == 1.5 * f13 and y[63] == 1.5 * f13 and y[64] == f13
+
+
+def test_uniform_attention_gives_equal_chunks():
+    """Q = 0 makes every softmax row uniform, so imp = 1/n everywhere and every
+    chunk (partial last one included) scores 1/n. With n = 128 every step is
+    exact in binary floating point, so the chunk scores tie exactly."""
+    n = 128
+    q = np.zeros((1, 2, 3, 4, 16), dtype=np.uint16)  # bf16 +0.0
+    _, k, off = random_case(11, [n], 2, 4, 2, 16, 3)
+    out = oracle.run(q, k, off, pool_w=13, chunk=48, normalize=False,
+                     boost_first_mult=1.0, boost_last_mult=1.0, mode="fixed", keep_p=0.3)
+    assert np.all(out["imp"] == 1.0 / n)
+    assert np.all(out["tok_score"] == 1.0 / n)
+    assert np.all(out["chunk_score"] == 1.0 / n)
+    # exact ties break by ascending index: k = ceil(3 * 0.3) = 1 -> chunk 0,
+    # plus the forced final (partial) chunk
+    np.testing.assert_array_equal(out["chunk_keep"], [1, 0, 2])
+    np.testing.assert_array_equal(out["kept_idx"], list(range(48)) + list(range(96, 128)))
+    # mass mode with equal scores keeps the first ceil(mass * nc) chunks
+    out = oracle.run(q, k, off, pool_w=13, chunk=16, normalize=False,
+                     boost_first_mult=1.0, boost_last_mult=1.0, mode="mass", mass=0.5)
+    np.testing.assert_array_equal(out["chunk_keep"], [1, 1, 1, 1, 0, 0, 0, 2])
+
+
+def test_fixed_count_closed_forms():
+    assert oracle.fixed_count(16, 0.30) == 5
+    assert oracle.fixed_count(1024, 0.15) == 154
+    assert oracle.fixed_count(4096, 0.30) == 1229
+    assert oracle.fixed_count(10, 1.0) == 10
+    assert oracle.fixed_count(10, 1e-6) == 1
+    assert oracle.fixed_count(20, 0.5) == 10  # exact product
+
+
+def test_fixed_mode_ignores_normalisation_without_boost():
+    q, k, off = random_case(12, [500, 333], 2, 4, 2, 16, 2, q_gain=2.0)
+    kw = dict(pool_w=13, chunk=16, mode="fixed", keep_p=0.25, boost_first_mult=1.0,
+              boost_last_mult=1.0)
+    a = oracle.run(q, k, off, normalize=False, **kw)
+    b = oracle.run(q, k, off, normalize=True, **kw)
+    np.testing.assert_array_equal(a["chunk_keep"], b["chunk_keep"])
+
+
+def test_mass_extremes():
+    cs = np.array([0.3, 0.1, 0.5, 0.05, 0.2])
+    assert oracle.select_mass(cs, 1.0).all()
+    np.testing.assert_array_equal(oracle.select_mass(cs, 1e-6), [False, False, True, False, False])
+    # 0.5 + 0.3 = 0.8 of 1.15 total < 0.85 * 1.15, so 0.2 is added
+    np.testing.assert_array_equal(oracle.select_mass(cs, 0.85), [True, False, True, False, True])
+    assert oracle.select_mass(np.zeros(4), 0.5).all()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_selection_matches_subset_enumeration(seed):
+    rng = np.random.default_rng(seed)
+    nc = int(rng.integers(1, 13))
+    if seed % 3 == 0:
+        cs = rng.integers(0, 4, nc).astype(np.float64)  # many ties
+    else:
+        cs = rng.random(nc)
+    for p in (0.1, 0.3, 0.5, 1.0):
+        got = np.flatnonzero(oracle.select_fixed(cs, p))
+        assert got.tolist() == bruteforce._select(cs.tolist(), "fixed", p, 0.0)
+    for m in (0.2, 0.5, 0.85, 1.0):
+        got = np.flatnonzero(oracle.select_mass(cs, m))
+        assert got.tolist() == bruteforce._select(cs.tolist(), "mass", 0.0, m)
+
+
+def test_kept_list_invariants():
+    q, k, off = random_case(13, [1000, 77, 513], 2, 4, 2, 16, 2, q_gain=2.0)
+    out = oracle.run(q, k, off, chunk=32, mode="mass", mass=0.5)
+    coff = out["chunk_off"]
+    for b in range(3):
+        lo, hi = out["kept_off"][b], out["kept_off"][b + 1]
+        idx, pos = out["kept_idx"][lo:hi], out["kept_pos"][lo:hi]
+        n = off[b + 1] - off[b]
+        assert np.all(np.diff(idx) > 0)
+        np.testing.assert_array_equal(idx - off[b], pos)
+        flags = out["chunk_keep"][coff[b]:coff[b + 1]]
+        sizes = [min(32, n - 32 * c) for c in range(len(flags))]
+        expect = sum(s for s, f in zip(sizes, flags) if f) + (0 if flags[0] else 1)
+        assert hi - lo == expect
+        assert pos[0] == 0 and pos[-1] == n - 1
+        assert flags[-1] & 2
+
+
+def test_needles_are_kept_small_workload():
+    w = get_workload("tiny")
+    inp = make_inputs(w)
+    out = oracle.run(inp.q, inp.k, inp.seq_off, **w.selection_kwargs())
+    kept = set(out["kept_idx"].tolist())
+    assert len(inp.needles) == 3
+    for (b, t, h) in inp.needles:
+        assert inp.seq_off[b] + t in kept
+    # fixed p = 0.30 of 16 chunks: 5 ranked + forced final chunk
+    assert int((out["chunk_keep"] & 1).sum()) == 5
+
+
+@pytest.mark.slow
+def test_mass_selection_finds_needles_08b_workload():
+    """Mass mode keeps chunks until 85 % of the score mass: with needle keys
+    dominating every head, each ranked-selected chunk must sit within half a
+    pool window of a planted needle, and the strongest needle chunk is kept.
+    (Needles sharing a query head have identical keys and split that head's
+    attention, so the weakest may fall after the 85 % crossing.)"""
+    w = get_workload("draft08b")
+    inp = make_inputs(w)
+    out = oracle.run(inp.q, inp.k, inp.seq_off, **w.selection_kwargs())
+    half = w.pool_w // 2
+    near = np.zeros(len(out["chunk_score"]), dtype=bool)
+    for (b, t, h) in inp.needles:
+        for u in range(t - half, t + half + 1):
+            near[u // w.chunk] = True
+    ranked = np.flatnonzero(out["chunk_keep"] & 1)
+    assert len(ranked) >= 1 and near[ranked].all()
+    top = oracle.rank_order(out["chunk_score"])[0]
+    assert out["chunk_keep"][top] & 1 and near[top]
+    assert out["final_score"].min() >= 0.0
+
+
+def test_bf16_decode_exact():
+    vals = np.array([0.0, 1.0, -2.5, 3.140625, 1e-3, 65280.0], dtype=np.float32)
+    bits = bf16_bits_from_f32(vals)
+    dec = so.decode_bf16(bits)
+    # bf16 keeps 8 significant bits: these are all representable except 1e-3
+    np.testing.assert_array_equal(dec[[0, 1, 2, 3, 5]], vals[[0, 1, 2, 3, 5]].astype(np.float64))
+    assert abs(dec[4] - 1e-3) <= 1e-3 * 2.0 ** -8
