@@ -1,0 +1,327 @@
+"""Benchmark of the SpecPrefill scoring path (token importance + chunk
+selection) on the 2B-draft-like workload: N = 32768 prompt tokens, 6
+attention layers, 8 query / 2 KV heads, head_dim 256, 8 lookahead queries,
+fixed keep fraction 0.15, W = 13 pool, 32-token chunks, boost, BOS and the
+final chunk forced.
+
+One step = one call of the whole path (sp_specprefill_score) on one batch of
+seeded synthetic inputs already resident in HBM. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no cross-GPU exchange); the reported value is the tokens all
+ranks scored divided by the slowest rank's time.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "draft2b"
+METRIC = "prompt tokens scored+selected/sec at N=32K; HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+N_COPIES = 4
+FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes per launch of the logits kernel from one ncu capture
+# (profiles/logits_tc_draft2b.md), valid while the kernel source hash matches.
+TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha1():
+    p = os.path.join(ROOT, "speculative_prefill_token_gb300", "csrc", "sp_logits_tc.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [v for v in sm if mx and v >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_inputs():
+    from tests.gpu_helpers import workload_inputs
+    w, inp = workload_inputs(WORKLOAD)
+    return w, inp
+
+
+def cpu_baseline(w, inp, budget_s=20.0):
+    """The float64 oracle as it stands, on the host cores, on the full
+    workload (repeated while it fits the time budget)."""
+    import oracle
+    kw = w.selection_kwargs()
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run(inp.q, inp.k, inp.seq_off, **kw)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el + el / runs > budget_s or runs >= 3:
+            break
+    tokens = runs * inp.n_tokens_total
+    return {"value": tokens / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"full {WORKLOAD} workload (N={inp.n_tokens_total}) x{runs}, numpy float64, "
+                      f"BLAS threads = host cores, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w, inp = make_inputs()
+    kw = w.selection_kwargs()
+    # bounded sample per step: the first 4096 tokens of the prompt (same
+    # per-token work: 12 slabs x 32 rows x 256-dim dot products + softmax)
+    n = 4096
+    k = np.ascontiguousarray(inp.k[:, :n])
+    off = np.array([0, n], dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.run(inp.q, k, off, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(inp.q, k, off, **kw)
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K with planted needles)",
+            "config": {"workload": f"{WORKLOAD}: N=32768, 6 layers, 8/2 heads, d=256, L=8, "
+                                   f"fixed p=0.15 (reference sample: first {n} tokens per step)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"first {n} tokens of the {WORKLOAD} prompt per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import speculative_prefill_token_gb300 as sp
+    from speculative_prefill_token_gb300 import _build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build()
+    sp.load()
+    w, inp = make_inputs()
+    params = sp.SelectionParams(**w.selection_kwargs())
+    ntot = inp.n_tokens_total
+    q_np = np.ascontiguousarray(inp.q).view(np.int16)
+    k_np = np.ascontiguousarray(inp.k).view(np.int16)
+    qs = [torch.from_numpy(q_np).to(dev) for _ in range(N_COPIES)]
+    ks = [torch.from_numpy(k_np).to(dev) for _ in range(N_COPIES)]
+    off = torch.from_numpy(np.asarray(inp.seq_off, dtype=np.int32)).to(dev)
+    shape = sp.shape_of(qs[0], ks[0])
+    ws = sp.make_workspace(shape, params, dev)
+    out = sp.alloc_outputs(qs[0], ks[0], params, intermediates=False)
+    stream = torch.cuda.current_stream()
+    k_bytes = shape.n_layers * shape.n_kv_heads * ntot * shape.head_dim * 2
+
+    def step(i, ev=None):
+        sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, params, out=out, ws=ws,
+                             stream=stream, profile_events=ev)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert sp.device_status(ws) == 0
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    logits_ms = [a.elapsed_time(b) for a, b in evs]
+    status = sp.device_status(ws)
+    n_kept = int(out.n_kept.item())
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the call, D2H of the kept lists
+    q_host = torch.from_numpy(q_np).pin_memory()
+    k_host = torch.from_numpy(k_np).pin_memory()
+    off_host = torch.from_numpy(np.asarray(inp.seq_off, dtype=np.int32)).pin_memory()
+    res_host = [torch.empty(ntot, dtype=torch.int32).pin_memory() for _ in range(2)]
+    koff_host = torch.empty(shape.n_seqs + 1, dtype=torch.int32).pin_memory()
+    nk_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    qd, kd, od = qs[0], ks[0], off
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        qd.copy_(q_host, non_blocking=True)
+        kd.copy_(k_host, non_blocking=True)
+        od.copy_(off_host, non_blocking=True)
+        sp.specprefill_score(qd, kd, od, params, out=out, ws=ws, stream=stream)
+        res_host[0].copy_(out.kept_idx, non_blocking=True)
+        res_host[1].copy_(out.kept_pos, non_blocking=True)
+        koff_host.copy_(out.kept_off, non_blocking=True)
+        nk_host.copy_(out.n_kept, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = q_np.nbytes + k_np.nbytes + off_host.numel() * 4
+    d2h = 2 * ntot * 4 + koff_host.numel() * 4 + 4
+
+    # max over ranks of the timed region
+    times = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = float(times[0]), float(times[1])
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    value = world * ntot * args.steps / (elapsed_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    avg_logits_s = statistics.mean(logits_ms) / 1e3
+    achieved = k_bytes / avg_logits_s / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha1"] == kernel_sha1() else None
+    launches_per_step = 1 + 3 * 1 + 4  # prep, (logits, lse, reduce) x waves, pool, chunk, select, gather
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K with 64 planted needles in 8 clusters)",
+        "config": {"workload": f"{WORKLOAD}: N=32768 prompt tokens, 6 attention layers, 8 query / "
+                               "2 KV heads, head_dim 256, 8 lookahead queries, W=13, C=32, fixed "
+                               "p=0.15, normalise + boost, BOS + final chunk forced",
+                   "l2": f"inputs larger than L2: {N_COPIES} rotating copies of the 201 MB key cache",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "logits_tc_kernel (tcgen05 + TMA)",
+                     "algorithmic_bytes_per_launch": k_bytes,
+                     "avg_launch_ms": avg_logits_s * 1e3, "peak_kind": f"{peak_kind} hbm_gbs"},
+        "hbm_gbs_whole_step": k_bytes / (elapsed_ms / args.steps / 1e3) / 1e9,
+        "clocks": clk.summary(),
+        "e2e": {"value": world * ntot / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "kept_tokens": n_kept, "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * specprefill.h — C ABI of the SpecPrefill token-importance and
+ * chunk-selection path, hand-written CUDA for sm_103a (GB300).
+ *
+ * The path (pages: "SpecPrefill — Implementation Guide" of the
+ * sliding-specprefill project, versions v2 and v3.1, and the llama.cpp pull
+ * request "Speculative prefill"):
+ *
+ *   logits    s = scale * <q, k> for every lookahead query vector q of every
+ *             attention layer and query head, against the prompt's cached
+ *             keys k (GQA: query head h reads KV head h / (Hq/Hk))
+ *   softmax   over the prompt's keys                    (guide §How It Works /
+ *                                                        Attention Capture)
+ *   importance  max over heads, max over layers, mean over lookahead steps
+ *                                                       (guide §How It Works /
+ *                                                        Token Importance)
+ *   pool      centred average over W tokens (W = 13)    (PR §Approach item 3)
+ *   normalise min-max to [0, 1] (optional)              (guide v3.1 item 5)
+ *   boost     first 64 tokens x1.5, last 128 x1.3      (guide v3 item 2)
+ *   chunks    mean score of 32-token chunks             (guide §Chunk Selection)
+ *   select    top k = max(1, ceil(nc * p)) chunks, or the shortest ranked
+ *             prefix holding `mass` of the total score  (guide v3 item 1)
+ *   force     BOS and each prompt's final chunk         (PR §Approach item 4)
+ *   gather    kept token indices + original position IDs (guide §How It
+ *                                                        Works / Sparse Prefill)
+ *
+ * Conventions for every entry point
+ * - Pointers marked (device) are device memory owned by the caller; the
+ *   library never allocates, frees or retains them, and keeps no state
+ *   between calls. Pointers marked (host) are host memory read during the
+ *   call.
+ * - Work is enqueued on `stream` and runs asynchronously; no entry point
+ *   synchronises except sp_get_device_status.
+ * - Return value: SP_OK, or an sp_status code for an argument the host can
+ *   check (nothing is enqueued then) or a launch error. Faults the device
+ *   detects itself (a bounded wait that gave up) set a sticky status word in
+ *   the workspace, read with sp_get_device_status.
+ * - Ranking ties break by ascending chunk index; the fixed mode keeps
+ *   exactly k ranked chunks.
+ * - Prompts are packed along the token axis: prompt b owns global tokens
+ *   [seq_off[b], seq_off[b+1]). Chunks never cross prompts; prompt b owns
+ *   chunks [chunk_off[b], chunk_off[b+1]), chunk_off[b+1]-chunk_off[b] =
+ *   ceil(n_b / chunk).
+ */
+#ifndef SPECPREFILL_H
+#define SPECPREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t / cudaEvent_t. */
+typedef struct CUstream_st* sp_stream_t;
+typedef struct CUevent_st* sp_event_t;
+
+typedef enum sp_status {
+    SP_OK = 0,
+    SP_ERR_INVALID_ARG = 1,   /* null pointer, inconsistent shape, parameter out of range */
+    SP_ERR_UNSUPPORTED = 2,   /* head_dim not in {64,128,256}, L*G > 64, misaligned strides */
+    SP_ERR_WORKSPACE = 3,     /* workspace null, misaligned (256 B) or smaller than required */
+    SP_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    SP_ERR_TIMEOUT = 5,       /* (device status) a bounded device wait gave up */
+    SP_ERR_DEVICE = 6         /* (device status) the kernel found an inconsistent input */
+} sp_status;
+
+enum { SP_MODE_FIXED = 0, SP_MODE_MASS = 1 };
+
+/* Shapes and strides. Strides are in elements; the head_dim axis is
+ * contiguous (stride 1).
+ * K: bf16 keys of layer l, global token t, KV head g at
+ *    k[l*k_stride_layer + t*k_stride_token + g*k_stride_head + j]
+ *    (a token-major KV cache, e.g. [Ly][Ntot][Hk][d] contiguous).
+ * Q: bf16 lookahead queries of prompt b, layer l, step s, query head h at
+ *    q[b*q_stride_seq + l*q_stride_layer + s*q_stride_step + h*q_stride_head + j]
+ *    (e.g. [B][Ly][L][Hq][d] contiguous).
+ * Every stride times 2 bytes must be a multiple of 16 and both base
+ * pointers 16-byte aligned (tensor-memory-accelerator tiles). */
+typedef struct sp_shape {
+    int32_t n_seqs;          /* B >= 1 prompts */
+    int32_t n_layers;        /* Ly >= 1 attention layers */
+    int32_t n_q_heads;       /* Hq >= 1 */
+    int32_t n_kv_heads;      /* Hk >= 1, Hq % Hk == 0, G = Hq / Hk */
+    int32_t head_dim;        /* d in {64, 128, 256} */
+    int32_t n_lookahead;     /* L >= 1 query vectors per layer and head; L*G <= 64 */
+    int32_t n_tokens_total;  /* Ntot = seq_off[B] >= 1 */
+    int32_t reserved;        /* must be 0 */
+    int64_t k_stride_layer, k_stride_token, k_stride_head;
+    int64_t q_stride_seq, q_stride_layer, q_stride_step, q_stride_head;
+} sp_shape;
+
+typedef struct sp_params {
+    int32_t pool_w;            /* odd, >= 1 (13); 1 = no smoothing */
+    int32_t chunk;             /* C >= 1 (32) */
+    int32_t mode;              /* SP_MODE_FIXED or SP_MODE_MASS */
+    float keep_p;              /* fixed mode, in (0, 1] (0.30) */
+    float mass;                /* mass mode, in (0, 1] (0.85) */
+    int32_t normalize;         /* 1: min-max normalise each prompt's pooled scores */
+    float boost_first_mult;    /* > 0 (1.5); 1 = off */
+    int32_t boost_first_n;     /* >= 0 (64) */
+    float boost_last_mult;     /* > 0 (1.3); 1 = off */
+    int32_t boost_last_n;      /* >= 0 (128) */
+    int32_t force_bos;         /* 1: token 0 of every prompt is kept */
+    int32_t force_last_chunk;  /* 1: every prompt's final chunk is kept */
+    float scale;               /* logit scale; 0 selects 1/sqrt(head_dim) */
+    int32_t spin_limit;        /* polls before a device wait gives up; <= 0 selects the default */
+} sp_params;
+
+/* Optional profiling hook: when non-null, `logits_start`/`logits_stop` are
+ * recorded on `stream` immediately around the logits kernel(s). */
+typedef struct sp_profile {
+    sp_event_t logits_start;
+    sp_event_t logits_stop;
+} sp_profile;
+
+/* Upper bound on the number of chunks of a packed batch:
+ * floor(Ntot / chunk) + B. Chunk arrays must hold this many entries. */
+int sp_max_chunks(const sp_shape* shape, const sp_params* params, int64_t* n_chunks);
+
+/* Bytes of device workspace the entry points below need for this shape on
+ * the current device (writes *bytes). */
+int sp_workspace_size(const sp_shape* shape, const sp_params* params, size_t* bytes);
+
+/* Zero the workspace's status word. Call once on a new workspace (or use
+ * zero-filled memory) before the first call that uses it. */
+int sp_workspace_init(void* ws, size_t ws_bytes, sp_stream_t stream);
+
+/* Token importance (logits, softmax, max over heads and layers, mean over
+ * steps): imp[t] for every global token t (device, Ntot floats).
+ * seq_off (device, B+1 int32, non-decreasing from 0 to Ntot), q and k
+ * (device, bf16 bits) as described at sp_shape. */
+int sp_attn_importance(const sp_shape* shape, const sp_params* params,
+                       const int32_t* seq_off, const uint16_t* q, const uint16_t* k,
+                       float* imp, void* ws, size_t ws_bytes, sp_stream_t stream);
+
+/* Same contract as sp_attn_importance, but the logits come from a CUDA-core
+ * (FP32 FMA) kernel instead of the tensor-core one. It exists as an
+ * independent cross-check of the tensor-core kernel in the GPU tests. */
+int sp_attn_importance_simt(const sp_shape* shape, const sp_params* params,
+                            const int32_t* seq_off, const uint16_t* q, const uint16_t* k,
+                            float* imp, void* ws, size_t ws_bytes, sp_stream_t stream);
+
+/* Smoothing and chunk scores from imp (device, Ntot floats).
+ * tok_score (device, Ntot floats, nullable): pooled score before
+ * normalisation and boost. chunk_score (device, sp_max_chunks floats): the
+ * final chunk scores. chunk_off (device, B+1 int32): written. */
+int sp_pool_chunk(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                  const float* imp, float* tok_score, float* chunk_score, int32_t* chunk_off,
+                  void* ws, size_t ws_bytes, sp_stream_t stream);
+
+/* Chunk selection per prompt. chunk_keep (device, one byte per chunk):
+ * bit 0 = chosen by the ranking, bit 1 = forced final chunk. */
+int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+              const int32_t* chunk_off, const float* chunk_score, uint8_t* chunk_keep,
+              void* ws, size_t ws_bytes, sp_stream_t stream);
+
+/* Stream compaction of kept tokens. For prompt b, its kept tokens (those
+ * in a chunk with chunk_keep != 0, plus token 0 when force_bos) in
+ * increasing order occupy [kept_off[b], kept_off[b+1]) of kept_idx (global
+ * token index) and kept_pos (position within the prompt, i.e. the original
+ * position ID). kept_idx/kept_pos: device, capacity Ntot int32 each;
+ * kept_off: device, B+1 int32; n_kept: device, 1 int32 (= kept_off[B]). */
+int sp_gather_kept(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                   const int32_t* chunk_off, const uint8_t* chunk_keep, int32_t* kept_idx,
+                   int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
+                   size_t ws_bytes, sp_stream_t stream);
+
+/* The whole path in one call. imp, tok_score, chunk_score, chunk_off and
+ * chunk_keep are optional outputs (nullable; kept in the workspace when
+ * null); kept_idx, kept_pos, kept_off and n_kept are required. `prof` is
+ * optional (nullable). */
+int sp_specprefill_score(const sp_shape* shape, const sp_params* params,
+                         const int32_t* seq_off, const uint16_t* q, const uint16_t* k,
+                         float* imp, float* tok_score, float* chunk_score, int32_t* chunk_off,
+                         uint8_t* chunk_keep, int32_t* kept_idx, int32_t* kept_pos,
+                         int32_t* kept_off, int32_t* n_kept, void* ws, size_t ws_bytes,
+                         sp_stream_t stream, const sp_profile* prof);
+
+/* Synchronise `stream`, then read (and, when `clear` is non-zero, reset)
+ * the workspace's sticky device status word into *status_host. */
+int sp_get_device_status(void* ws, size_t ws_bytes, sp_stream_t stream, int clear,
+                         int32_t* status_host);
+
+/* Static description of a status code. */
+const char* sp_status_string(int status);
+
+/* Library build identification (architecture and kernel variant). */
+const char* sp_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECPREFILL_H */

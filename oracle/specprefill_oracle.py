@@ -39,7 +39,8 @@ of a constant vector gives all ones; boost factors multiply where the two
 regions overlap; ties in the ranking break by ascending chunk index and the
 fixed mode keeps exactly k chunks; a chunk's mass is its score, the crossing
 chunk is kept, forced chunks do not count, and zero total mass keeps all;
-forced chunks/tokens are added after the ranking selection.
+forced chunks/tokens are added after the ranking selection; an empty prompt
+(zero tokens) has no chunks and keeps nothing.
 """
 
 import math
@@ -207,6 +208,8 @@ def finish_selection(sel: np.ndarray, n: int, chunk: int, force_bos: bool,
     (steps 11-12)."""
     nc = sel.shape[0]
     flags = sel.astype(np.uint8)
+    if nc == 0:
+        return Selection(chunk_keep=flags, kept_tokens=np.zeros(0, dtype=np.int64))
     if force_last_chunk:
         flags[nc - 1] |= 2
     toks: List[int] = []
@@ -235,7 +238,9 @@ def score_prompt(imp: np.ndarray, *, pool_w: int, chunk: int, normalize: bool,
 def select_prompt(cs: np.ndarray, n: int, *, chunk: int, mode: str, keep_p: float,
                   mass: float, force_bos: bool, force_last_chunk: bool) -> Selection:
     """Steps 9-12 for one prompt."""
-    if mode == "fixed":
+    if cs.shape[0] == 0:
+        sel = np.zeros(0, dtype=bool)
+    elif mode == "fixed":
         sel = select_fixed(cs, keep_p)
     elif mode == "mass":
         sel = select_mass(cs, mass)
@@ -295,6 +300,12 @@ def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
     imps, toks, finals, chunks, steps = [], [], [], [], []
     for b in range(len(seq_off) - 1):
         start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
+        if n == 0:
+            for lst in (imps, toks, finals, chunks):
+                lst.append(np.zeros(0))
+            if keep_step_max:
+                steps.append(np.zeros((q_bits.shape[2], 0)))
+            continue
         a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale)
         imp = token_importance(a)
         sc = score_prompt(imp, pool_w=pool_w, chunk=chunk, normalize=normalize,

@@ -1,0 +1,357 @@
+"""Python binding of libspecprefill (the SpecPrefill scoring path on sm_103a).
+
+Argument marshalling only: every step of the path runs in the CUDA library
+through its C ABI (include/specprefill.h). PyTorch supplies device memory and
+streams. There is no CPU fallback: if the library is missing or fails to
+load, every call raises.
+
+Tensor conventions (bf16 data carried as torch.bfloat16 or as uint16 bits):
+  q        [B, Ly, L, Hq, d]   lookahead queries of each prompt (strided ok,
+                               head_dim contiguous)
+  k        [Ly, Ntot, Hk, d]   token-major key cache of the packed prompts
+  seq_off  [B+1] int32         prompt offsets on the token axis
+"""
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import Optional
+
+__all__ = [
+    "SelectionParams",
+    "SpecPrefillError",
+    "load",
+    "lib",
+    "workspace_size",
+    "max_chunks",
+    "make_workspace",
+    "attn_importance",
+    "attn_importance_simt",
+    "pool_chunk",
+    "select",
+    "gather_kept",
+    "specprefill_score",
+    "device_status",
+    "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecprefill.so")
+
+STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_ERR_WORKSPACE",
+          4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_DEVICE"}
+MODES = {"fixed": 0, "mass": 1}
+
+
+class SpecPrefillError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("n_seqs", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_lookahead", ctypes.c_int32),
+                ("n_tokens_total", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("k_stride_layer", ctypes.c_int64), ("k_stride_token", ctypes.c_int64),
+                ("k_stride_head", ctypes.c_int64), ("q_stride_seq", ctypes.c_int64),
+                ("q_stride_layer", ctypes.c_int64), ("q_stride_step", ctypes.c_int64),
+                ("q_stride_head", ctypes.c_int64)]
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("pool_w", ctypes.c_int32), ("chunk", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("keep_p", ctypes.c_float), ("mass", ctypes.c_float),
+                ("normalize", ctypes.c_int32), ("boost_first_mult", ctypes.c_float),
+                ("boost_first_n", ctypes.c_int32), ("boost_last_mult", ctypes.c_float),
+                ("boost_last_n", ctypes.c_int32), ("force_bos", ctypes.c_int32),
+                ("force_last_chunk", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("spin_limit", ctypes.c_int32)]
+
+
+class _Profile(ctypes.Structure):
+    _fields_ = [("logits_start", ctypes.c_void_p), ("logits_stop", ctypes.c_void_p)]
+
+
+@dataclass
+class SelectionParams:
+    """Selection settings; defaults are the pages' (W=13, C=32, mass 0.85,
+    boost x1.5 first 64 / x1.3 last 128, BOS and final chunk kept)."""
+    pool_w: int = 13
+    chunk: int = 32
+    mode: str = "mass"
+    keep_p: float = 0.30
+    mass: float = 0.85
+    normalize: bool = True
+    boost_first_mult: float = 1.5
+    boost_first_n: int = 64
+    boost_last_mult: float = 1.3
+    boost_last_n: int = 128
+    force_bos: bool = True
+    force_last_chunk: bool = True
+    scale: float = 0.0
+    spin_limit: int = 0
+
+    def _c(self) -> _Params:
+        return _Params(int(self.pool_w), int(self.chunk), MODES[self.mode], float(self.keep_p),
+                       float(self.mass), int(bool(self.normalize)), float(self.boost_first_mult),
+                       int(self.boost_first_n), float(self.boost_last_mult), int(self.boost_last_n),
+                       int(bool(self.force_bos)), int(bool(self.force_last_chunk)),
+                       float(self.scale), int(self.spin_limit))
+
+
+_lib = None
+_P = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+
+
+def load(path: Optional[str] = None):
+    """Load the shared library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libspecprefill.so not built ({path}); run __graft_entry__.build()")
+    lib_ = ctypes.CDLL(path)
+    sp = ctypes.POINTER(_Shape)
+    pp = ctypes.POINTER(_Params)
+    i32 = ctypes.c_int
+    sigs = {
+        "sp_max_chunks": [sp, pp, ctypes.POINTER(ctypes.c_int64)],
+        "sp_workspace_size": [sp, pp, ctypes.POINTER(_SZ)],
+        "sp_workspace_init": [_P, _SZ, _P],
+        "sp_attn_importance": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_attn_importance_simt": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_pool_chunk": [sp, pp, _P, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_select": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_gather_kept": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_specprefill_score": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                 _P, ctypes.POINTER(_Profile)],
+        "sp_get_device_status": [_P, _SZ, _P, i32, ctypes.POINTER(ctypes.c_int32)],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib_, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib_.sp_status_string.argtypes = [i32]
+    lib_.sp_status_string.restype = ctypes.c_char_p
+    lib_.sp_build_info.argtypes = []
+    lib_.sp_build_info.restype = ctypes.c_char_p
+    _lib = lib_
+    return _lib
+
+
+def lib():
+    return load()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise SpecPrefillError(rc, what)
+
+
+# ---------------------------------------------------------------- marshalling
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def shape_of(q, k, seq_off=None, n_seqs: Optional[int] = None) -> _Shape:
+    """C shape struct from the q [B, Ly, L, Hq, d] and k [Ly, Ntot, Hk, d] tensors."""
+    if q.dim() != 5 or k.dim() != 4:
+        raise ValueError("q must be [B, Ly, L, Hq, d] and k [Ly, Ntot, Hk, d]")
+    if q.element_size() != 2 or k.element_size() != 2:
+        raise ValueError("q and k must hold bf16 (torch.bfloat16 or uint16 bits)")
+    b, ly, steps, hq, d = q.shape
+    ly_k, ntot, hk, d_k = k.shape
+    if ly_k != ly or d_k != d:
+        raise ValueError("q and k disagree on layers or head_dim")
+    if q.stride(-1) != 1 or k.stride(-1) != 1:
+        raise ValueError("head_dim must be contiguous")
+    return _Shape(int(b), int(ly), int(hq), int(hk), int(d), int(steps), int(ntot), 0,
+                  k.stride(0), k.stride(1), k.stride(2),
+                  q.stride(0), q.stride(1), q.stride(2), q.stride(3))
+
+
+def token_shape(n_seqs: int, n_tokens_total: int, n_layers=1, n_q_heads=1, n_kv_heads=1,
+                head_dim=64, n_lookahead=1) -> _Shape:
+    """Shape struct for the stages that only need the token axis (pool,
+    select, gather); the attention dimensions are placeholders."""
+    return _Shape(int(n_seqs), n_layers, n_q_heads, n_kv_heads, head_dim, n_lookahead,
+                  int(n_tokens_total), 0, head_dim * n_tokens_total * n_kv_heads,
+                  head_dim * n_kv_heads, head_dim, head_dim, head_dim, head_dim, head_dim)
+
+
+def workspace_size(shape: _Shape, params: SelectionParams) -> int:
+    n = _SZ()
+    _check(lib().sp_workspace_size(ctypes.byref(shape), ctypes.byref(params._c()), ctypes.byref(n)),
+           "sp_workspace_size")
+    return int(n.value)
+
+
+def max_chunks(shape: _Shape, params: SelectionParams) -> int:
+    n = ctypes.c_int64()
+    _check(lib().sp_max_chunks(ctypes.byref(shape), ctypes.byref(params._c()), ctypes.byref(n)),
+           "sp_max_chunks")
+    return int(n.value)
+
+
+def make_workspace(shape: _Shape, params: SelectionParams, device=None):
+    """Allocate (torch) and initialise a workspace for this shape."""
+    import torch
+    nbytes = workspace_size(shape, params)
+    ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + nbytes]
+    _check(lib().sp_workspace_init(ws.data_ptr(), nbytes, _stream(None)), "sp_workspace_init")
+    return ws
+
+
+def _ws_args(ws):
+    return ws.data_ptr(), ws.numel()
+
+
+def attn_importance(q, k, seq_off, params: SelectionParams, imp=None, ws=None, stream=None,
+                    simt: bool = False):
+    """imp[t] for every packed token (float32, device)."""
+    import torch
+    shape = shape_of(q, k)
+    if imp is None:
+        imp = torch.empty(shape.n_tokens_total, dtype=torch.float32, device=k.device)
+    if ws is None:
+        ws = make_workspace(shape, params, k.device)
+    fn = lib().sp_attn_importance_simt if simt else lib().sp_attn_importance
+    _check(fn(ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(), q.data_ptr(),
+              k.data_ptr(), imp.data_ptr(), *_ws_args(ws), _stream(stream)),
+           "sp_attn_importance")
+    return imp
+
+
+def attn_importance_simt(q, k, seq_off, params: SelectionParams, imp=None, ws=None, stream=None):
+    return attn_importance(q, k, seq_off, params, imp, ws, stream, simt=True)
+
+
+def pool_chunk(imp, seq_off, params: SelectionParams, tok_score=None, ws=None, stream=None):
+    """(tok_score, chunk_score, chunk_off) from imp."""
+    import torch
+    n_seqs = seq_off.numel() - 1
+    shape = token_shape(n_seqs, imp.numel())
+    nch = max_chunks(shape, params)
+    chunk_score = torch.empty(nch, dtype=torch.float32, device=imp.device)
+    chunk_off = torch.empty(n_seqs + 1, dtype=torch.int32, device=imp.device)
+    if ws is None:
+        ws = make_workspace(shape, params, imp.device)
+    _check(lib().sp_pool_chunk(ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(),
+                               imp.data_ptr(), _ptr(tok_score), chunk_score.data_ptr(),
+                               chunk_off.data_ptr(), *_ws_args(ws), _stream(stream)),
+           "sp_pool_chunk")
+    return tok_score, chunk_score, chunk_off
+
+
+def select(chunk_score, chunk_off, seq_off, n_tokens_total: int, params: SelectionParams,
+           ws=None, stream=None):
+    """uint8 chunk_keep (bit 0 ranked, bit 1 forced final chunk)."""
+    import torch
+    n_seqs = seq_off.numel() - 1
+    shape = token_shape(n_seqs, n_tokens_total)
+    keep = torch.zeros(chunk_score.numel(), dtype=torch.uint8, device=chunk_score.device)
+    if ws is None:
+        ws = make_workspace(shape, params, chunk_score.device)
+    _check(lib().sp_select(ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(),
+                           chunk_off.data_ptr(), chunk_score.data_ptr(), keep.data_ptr(),
+                           *_ws_args(ws), _stream(stream)), "sp_select")
+    return keep
+
+
+def gather_kept(chunk_keep, chunk_off, seq_off, n_tokens_total: int, params: SelectionParams,
+                ws=None, stream=None):
+    """(kept_idx, kept_pos, kept_off, n_kept) device tensors; the lists hold
+    n_kept valid entries (capacity n_tokens_total)."""
+    import torch
+    n_seqs = seq_off.numel() - 1
+    shape = token_shape(n_seqs, n_tokens_total)
+    dev = chunk_keep.device
+    kept_idx = torch.empty(n_tokens_total, dtype=torch.int32, device=dev)
+    kept_pos = torch.empty(n_tokens_total, dtype=torch.int32, device=dev)
+    kept_off = torch.empty(n_seqs + 1, dtype=torch.int32, device=dev)
+    n_kept = torch.empty(1, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = make_workspace(shape, params, dev)
+    _check(lib().sp_gather_kept(ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(),
+                                chunk_off.data_ptr(), chunk_keep.data_ptr(), kept_idx.data_ptr(),
+                                kept_pos.data_ptr(), kept_off.data_ptr(), n_kept.data_ptr(),
+                                *_ws_args(ws), _stream(stream)), "sp_gather_kept")
+    return kept_idx, kept_pos, kept_off, n_kept
+
+
+@dataclass
+class ScoreOutputs:
+    kept_idx: object
+    kept_pos: object
+    kept_off: object
+    n_kept: object
+    imp: object = None
+    tok_score: object = None
+    chunk_score: object = None
+    chunk_off: object = None
+    chunk_keep: object = None
+
+
+def alloc_outputs(q, k, params: SelectionParams, intermediates: bool = True) -> ScoreOutputs:
+    import torch
+    shape = shape_of(q, k)
+    dev = k.device
+    ntot, nb = shape.n_tokens_total, shape.n_seqs
+    out = ScoreOutputs(kept_idx=torch.empty(ntot, dtype=torch.int32, device=dev),
+                       kept_pos=torch.empty(ntot, dtype=torch.int32, device=dev),
+                       kept_off=torch.empty(nb + 1, dtype=torch.int32, device=dev),
+                       n_kept=torch.empty(1, dtype=torch.int32, device=dev))
+    if intermediates:
+        nch = max_chunks(shape, params)
+        out.imp = torch.empty(ntot, dtype=torch.float32, device=dev)
+        out.tok_score = torch.empty(ntot, dtype=torch.float32, device=dev)
+        out.chunk_score = torch.empty(nch, dtype=torch.float32, device=dev)
+        out.chunk_off = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+        out.chunk_keep = torch.empty(nch, dtype=torch.uint8, device=dev)
+    return out
+
+
+def specprefill_score(q, k, seq_off, params: SelectionParams, out: Optional[ScoreOutputs] = None,
+                      ws=None, stream=None, profile_events=None) -> ScoreOutputs:
+    """The whole path: kept token indices and positions per prompt.
+
+    ``profile_events`` = (start, stop) torch.cuda.Event pair recorded around
+    the logits kernel(s).
+    """
+    shape = shape_of(q, k)
+    if out is None:
+        out = alloc_outputs(q, k, params)
+    if ws is None:
+        ws = make_workspace(shape, params, k.device)
+    prof = None
+    if profile_events is not None:
+        prof = ctypes.byref(_Profile(profile_events[0].cuda_event, profile_events[1].cuda_event))
+    _check(lib().sp_specprefill_score(
+        ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(), q.data_ptr(),
+        k.data_ptr(), _ptr(out.imp), _ptr(out.tok_score), _ptr(out.chunk_score),
+        _ptr(out.chunk_off), _ptr(out.chunk_keep), out.kept_idx.data_ptr(),
+        out.kept_pos.data_ptr(), out.kept_off.data_ptr(), out.n_kept.data_ptr(), *_ws_args(ws),
+        _stream(stream), prof), "sp_specprefill_score")
+    return out
+
+
+def device_status(ws, stream=None, clear: bool = True) -> int:
+    """Synchronise and read (and by default clear) the workspace status word."""
+    v = ctypes.c_int32()
+    _check(lib().sp_get_device_status(ws.data_ptr(), ws.numel(), _stream(stream), int(clear),
+                                      ctypes.byref(v)), "sp_get_device_status")
+    return int(v.value)

@@ -1,0 +1,331 @@
+// C ABI of the SpecPrefill scoring library: argument validation, the
+// per-shape launch plan and workspace layout, and the launch sequences of
+// the entry points declared in specprefill.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "sp_internal.h"
+#include "specprefill.h"
+
+namespace sp {
+namespace {
+
+// Scratch budget of one wave of slabs (fp32 logits): about half the L2 of
+// a GB300, so the logits written by one wave are still resident when the
+// softmax/importance kernel of the same wave reads them.
+constexpr int64_t kWaveScratchBytes = int64_t(60) << 20;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.0f; }
+
+int check_shape(const sp_shape* s) {
+    if (!s) return SP_ERR_INVALID_ARG;
+    if (s->n_seqs < 1 || s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1 ||
+        s->head_dim < 1 || s->n_lookahead < 1 || s->n_tokens_total < 1 || s->reserved != 0)
+        return SP_ERR_INVALID_ARG;
+    if (s->n_q_heads % s->n_kv_heads != 0) return SP_ERR_INVALID_ARG;
+    if (s->n_seqs > kMaxSeqs) return SP_ERR_UNSUPPORTED;
+    if (s->head_dim != 64 && s->head_dim != 128 && s->head_dim != 256) return SP_ERR_UNSUPPORTED;
+    const int G = s->n_q_heads / s->n_kv_heads;
+    if (static_cast<int64_t>(s->n_lookahead) * G > kMaxRows) return SP_ERR_UNSUPPORTED;
+    // strides: positive where the axis has more than one entry, 16-byte multiples
+    const int64_t st[7] = {s->k_stride_layer, s->k_stride_token, s->k_stride_head, s->q_stride_seq,
+                           s->q_stride_layer, s->q_stride_step, s->q_stride_head};
+    const int64_t ext[7] = {s->n_layers, s->n_tokens_total, s->n_kv_heads, s->n_seqs,
+                            s->n_layers, s->n_lookahead, s->n_q_heads};
+    for (int i = 0; i < 7; ++i) {
+        if (ext[i] <= 1) continue;
+        if (st[i] < s->head_dim) return SP_ERR_INVALID_ARG;
+        if ((st[i] * 2) % 16 != 0) return SP_ERR_UNSUPPORTED;
+    }
+    if (s->n_tokens_total > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
+    return SP_OK;
+}
+
+int check_params(const sp_params* p) {
+    if (!p) return SP_ERR_INVALID_ARG;
+    if (p->pool_w < 1 || p->pool_w % 2 == 0 || p->pool_w > kMaxPool) return SP_ERR_INVALID_ARG;
+    if (p->chunk < 1 || p->chunk > kMaxChunk) return SP_ERR_INVALID_ARG;
+    if (p->mode != SP_MODE_FIXED && p->mode != SP_MODE_MASS) return SP_ERR_INVALID_ARG;
+    if (p->mode == SP_MODE_FIXED && !(finite_pos(p->keep_p) && p->keep_p <= 1.0f)) return SP_ERR_INVALID_ARG;
+    if (p->mode == SP_MODE_MASS && !(finite_pos(p->mass) && p->mass <= 1.0f)) return SP_ERR_INVALID_ARG;
+    if (!finite_pos(p->boost_first_mult) || !finite_pos(p->boost_last_mult)) return SP_ERR_INVALID_ARG;
+    if (p->boost_first_n < 0 || p->boost_last_n < 0) return SP_ERR_INVALID_ARG;
+    if (!(std::isfinite(p->scale) && p->scale >= 0.0f)) return SP_ERR_INVALID_ARG;
+    if ((p->normalize != 0 && p->normalize != 1) || (p->force_bos != 0 && p->force_bos != 1) ||
+        (p->force_last_chunk != 0 && p->force_last_chunk != 1))
+        return SP_ERR_INVALID_ARG;
+    return SP_OK;
+}
+
+int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < pl.total)
+        return SP_ERR_WORKSPACE;
+    return SP_OK;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? SP_OK : SP_ERR_CUDA; }
+
+}  // namespace
+
+int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
+    int rc = check_shape(s);
+    if (rc != SP_OK) return rc;
+    rc = check_params(p);
+    if (rc != SP_OK) return rc;
+    Plan& P = *pl;
+    std::memset(&P, 0, sizeof(P));
+    P.B = s->n_seqs;
+    P.Ly = s->n_layers;
+    P.Hq = s->n_q_heads;
+    P.Hk = s->n_kv_heads;
+    P.G = P.Hq / P.Hk;
+    P.d = s->head_dim;
+    P.L = s->n_lookahead;
+    P.R = P.L * P.G;
+    P.Rs = (P.R + 3) & ~3;
+    P.Nmma = P.R <= 16 ? 16 : ((P.R + 15) & ~15);
+    P.Nacc = P.Nmma <= 32 ? 32 : 64;
+    P.Ntot = s->n_tokens_total;
+    P.slabs = P.Ly * P.Hk;
+    P.C = p->chunk;
+    P.W = p->pool_w;
+    P.tiles_max = P.Ntot / kTileTokens + P.B;
+    P.chunks_max = P.Ntot / P.C + P.B;
+    P.Tb = P.C <= kPostBlockTarget ? static_cast<int64_t>(P.C) * (kPostBlockTarget / P.C) : P.C;
+    P.pblk_max = P.Ntot / P.Tb + P.B;
+    int64_t maxnc = (P.Ntot + P.C - 1) / P.C;
+    if (maxnc > kMaxPromptChunks) maxnc = kMaxPromptChunks;
+    P.sort_cap = 1;
+    while (P.sort_cap < maxnc) P.sort_cap <<= 1;
+    const int64_t per_slab = P.Ntot * P.Rs * static_cast<int64_t>(sizeof(float));
+    int64_t spw = kWaveScratchBytes / per_slab;
+    if (spw < 1) spw = 1;
+    if (spw > P.slabs) spw = P.slabs;
+    P.slabs_per_wave = static_cast<int>(spw);
+    P.waves = (P.slabs + P.slabs_per_wave - 1) / P.slabs_per_wave;
+    const double scale = p->scale > 0.0f ? static_cast<double>(p->scale)
+                                          : static_cast<double>(1.0f / std::sqrt(static_cast<float>(P.d)));
+    P.scale2 = static_cast<float>(scale * 1.4426950408889634);
+    P.spin = p->spin_limit > 0 ? p->spin_limit : kDefaultSpin;
+
+    size_t off = sizeof(WsHeader);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align256(off + bytes);
+        return o;
+    };
+    const size_t B1 = static_cast<size_t>(P.B) + 1;
+    P.o_tile_base = take(B1 * 4);
+    P.o_chunk_off = take(B1 * 4);
+    P.o_pblk_base = take(B1 * 4);
+    P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.Ntot * P.Rs * 4);
+    P.o_part = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * P.Rs * 8);
+    P.o_lse = take(static_cast<size_t>(P.slabs_per_wave) * P.B * P.Rs * 4);
+    P.o_alog = take(P.waves > 1 ? static_cast<size_t>(P.L) * P.Ntot * 4 : 0);
+    P.o_imp = take(static_cast<size_t>(P.Ntot) * 4);
+    P.o_tok = take(static_cast<size_t>(P.Ntot) * 4);
+    P.o_ppart = take(static_cast<size_t>(P.pblk_max) * 8);
+    P.o_cscore = take(static_cast<size_t>(P.chunks_max) * 4);
+    P.o_ckeep = take(static_cast<size_t>(P.chunks_max));
+    P.o_ckoff = take(static_cast<size_t>(P.chunks_max) * 4);
+    P.o_pcount = take(static_cast<size_t>(P.B) * 4);
+    P.o_kept_off = take(B1 * 4);
+    P.o_nkept = take(4);
+    P.total = off;
+    return SP_OK;
+}
+
+namespace {
+
+int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, const uint16_t* q,
+                     const uint16_t* k, float* imp, void* ws, cudaStream_t st, bool simt,
+                     const sp_profile* prof) {
+    if (prof && prof->logits_start)
+        if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_start), st) != cudaSuccess)
+            return SP_ERR_CUDA;
+    for (int w = 0; w < pl.waves; ++w) {
+        const int slab0 = w * pl.slabs_per_wave;
+        const int ns = pl.slabs - slab0 < pl.slabs_per_wave ? pl.slabs - slab0 : pl.slabs_per_wave;
+        cudaError_t e = simt ? launch_logits_simt(pl, s, seq_off, q, k, ws, slab0, ns, st)
+                             : launch_logits_tc(pl, s, seq_off, q, k, ws, slab0, ns, st);
+        if (e != cudaSuccess) return SP_ERR_CUDA;
+        if (w == pl.waves - 1 && prof && prof->logits_stop)
+            if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_stop), st) != cudaSuccess)
+                return SP_ERR_CUDA;
+        if ((e = launch_lse(pl, ws, ns, st)) != cudaSuccess) return SP_ERR_CUDA;
+        if ((e = launch_reduce(pl, seq_off, ws, ns, w, imp, st)) != cudaSuccess) return SP_ERR_CUDA;
+    }
+    return SP_OK;
+}
+
+int attn_importance(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                    const uint16_t* q, const uint16_t* k, float* imp, void* ws, size_t ws_bytes,
+                    sp_stream_t stream, bool simt) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !q || !k || !imp || !aligned16(q) || !aligned16(k)) return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_prep(pl, seq_off, ws, nullptr, st) != cudaSuccess) return SP_ERR_CUDA;
+    return importance_waves(pl, shape, seq_off, q, k, imp, ws, st, simt, nullptr);
+}
+
+}  // namespace
+}  // namespace sp
+
+using namespace sp;
+
+extern "C" {
+
+int sp_max_chunks(const sp_shape* shape, const sp_params* params, int64_t* n_chunks) {
+    Plan pl;
+    const int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!n_chunks) return SP_ERR_INVALID_ARG;
+    *n_chunks = pl.chunks_max;
+    return SP_OK;
+}
+
+int sp_workspace_size(const sp_shape* shape, const sp_params* params, size_t* bytes) {
+    Plan pl;
+    const int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!bytes) return SP_ERR_INVALID_ARG;
+    *bytes = pl.total;
+    return SP_OK;
+}
+
+int sp_workspace_init(void* ws, size_t ws_bytes, sp_stream_t stream) {
+    if (!ws || ws_bytes < sizeof(WsHeader) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return SP_ERR_WORKSPACE;
+    return to_status(cudaMemsetAsync(ws, 0, sizeof(WsHeader), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sp_attn_importance(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                       const uint16_t* q, const uint16_t* k, float* imp, void* ws, size_t ws_bytes,
+                       sp_stream_t stream) {
+    return attn_importance(shape, params, seq_off, q, k, imp, ws, ws_bytes, stream, false);
+}
+
+int sp_attn_importance_simt(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                            const uint16_t* q, const uint16_t* k, float* imp, void* ws,
+                            size_t ws_bytes, sp_stream_t stream) {
+    return attn_importance(shape, params, seq_off, q, k, imp, ws, ws_bytes, stream, true);
+}
+
+int sp_pool_chunk(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                  const float* imp, float* tok_score, float* chunk_score, int32_t* chunk_off,
+                  void* ws, size_t ws_bytes, sp_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !imp || !chunk_score || !chunk_off) return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* tok = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
+    if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_pool(pl, params, seq_off, imp, tok, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    return to_status(launch_chunk(pl, params, seq_off, tok, chunk_score, ws, st));
+}
+
+int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+              const int32_t* chunk_off, const float* chunk_score, uint8_t* chunk_keep, void* ws,
+              size_t ws_bytes, sp_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !chunk_off || !chunk_score || !chunk_keep) return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_prep_check(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    return to_status(launch_select(pl, params, seq_off, ws_ptr<int32_t>(ws, pl.o_chunk_off),
+                                   chunk_score, chunk_keep, ws, false, nullptr, nullptr, st));
+}
+
+int sp_gather_kept(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                   const int32_t* chunk_off, const uint8_t* chunk_keep, int32_t* kept_idx,
+                   int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws, size_t ws_bytes,
+                   sp_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !chunk_off || !chunk_keep || !kept_idx || !kept_pos || !kept_off || !n_kept)
+        return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
+    if (launch_prep_check(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_gather_scan(pl, params, seq_off, coff, chunk_keep, ws, kept_off, n_kept, st) !=
+        cudaSuccess)
+        return SP_ERR_CUDA;
+    return to_status(launch_gather_write(pl, params, seq_off, coff, chunk_keep, kept_idx, kept_pos,
+                                         kept_off, n_kept, ws, st));
+}
+
+int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                         const uint16_t* q, const uint16_t* k, float* imp, float* tok_score,
+                         float* chunk_score, int32_t* chunk_off, uint8_t* chunk_keep,
+                         int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept,
+                         void* ws, size_t ws_bytes, sp_stream_t stream, const sp_profile* prof) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !q || !k || !kept_idx || !kept_pos || !kept_off || !n_kept || !aligned16(q) ||
+        !aligned16(k))
+        return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* imp_p = imp ? imp : ws_ptr<float>(ws, pl.o_imp);
+    float* tok_p = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
+    float* cs_p = chunk_score ? chunk_score : ws_ptr<float>(ws, pl.o_cscore);
+    uint8_t* keep_p = chunk_keep ? chunk_keep : ws_ptr<uint8_t>(ws, pl.o_ckeep);
+    const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
+    if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    if ((rc = importance_waves(pl, shape, seq_off, q, k, imp_p, ws, st, false, prof)) != SP_OK) return rc;
+    if (launch_pool(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_select(pl, params, seq_off, coff, cs_p, keep_p, ws, true, kept_off, n_kept, st) !=
+        cudaSuccess)
+        return SP_ERR_CUDA;
+    return to_status(launch_gather_write(pl, params, seq_off, coff, keep_p, kept_idx, kept_pos,
+                                         kept_off, n_kept, ws, st));
+}
+
+int sp_get_device_status(void* ws, size_t ws_bytes, sp_stream_t stream, int clear,
+                         int32_t* status_host) {
+    if (!ws || ws_bytes < sizeof(WsHeader) || !status_host) return SP_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SP_ERR_CUDA;
+    if (cudaMemcpy(status_host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SP_ERR_CUDA;
+    if (clear && cudaMemset(ws, 0, sizeof(int32_t)) != cudaSuccess) return SP_ERR_CUDA;
+    return SP_OK;
+}
+
+const char* sp_status_string(int status) {
+    switch (status) {
+        case SP_OK: return "ok";
+        case SP_ERR_INVALID_ARG: return "invalid argument";
+        case SP_ERR_UNSUPPORTED: return "unsupported shape or layout";
+        case SP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case SP_ERR_CUDA: return "CUDA runtime or launch error";
+        case SP_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case SP_ERR_DEVICE: return "device-side input check failed";
+        default: return "unknown status";
+    }
+}
+
+const char* sp_build_info(void) {
+    return "specprefill sm_103a: tcgen05/TMA logits kernel, fp32 softmax partials, "
+           "bitonic per-prompt selection";
+}
+
+}  // extern "C"

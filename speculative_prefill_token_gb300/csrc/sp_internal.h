@@ -1,0 +1,104 @@
+// Internal host/device declarations of the SpecPrefill library: the launch
+// plan derived from a shape, the workspace layout, and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "specprefill.h"
+
+namespace sp {
+
+constexpr int kTileTokens = 128;   // tokens per logits tile (tensor-core M)
+constexpr int kMaxRows = 64;       // max query rows per slab (L * G)
+constexpr int kPostBlockTarget = 1024;
+constexpr int kMaxSeqs = 65536;
+constexpr int kMaxChunk = 8192;
+constexpr int kMaxPool = 8191;
+constexpr int kMaxPromptChunks = 16384;  // per-prompt chunk count the in-CTA sort handles
+constexpr int64_t kDefaultSpin = int64_t(1) << 22;  // ~4 s of polls with a 1 us suspend hint
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    int32_t status;        // sticky device status (sp_status), written by kernels on failure
+    int32_t bad_input;     // set by the prep kernel of the current call when seq_off is invalid
+    uint32_t ticket;       // last-block-done counter of the gather scan (zeroed by prep)
+    int32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct Plan {
+    // shape
+    int B, Ly, Hq, Hk, G, d, L, R, Rs, Nmma, Nacc;
+    int64_t Ntot;
+    int slabs;
+    int64_t tiles_max;    // >= sum_b ceil(n_b / 128)
+    int64_t chunks_max;   // >= sum_b ceil(n_b / C)
+    int C, W;
+    int64_t Tb;           // tokens per post-processing block (multiple of C)
+    int64_t pblk_max;     // >= sum_b ceil(n_b / Tb)
+    int sort_cap;         // power of two >= max chunks of one prompt
+    int slabs_per_wave, waves;
+    float scale2;         // logit scale * log2(e)
+    int64_t spin;         // bounded-wait poll limit
+    // workspace offsets (bytes)
+    size_t o_tile_base, o_chunk_off, o_pblk_base, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
+        o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
+};
+
+int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
+
+// ------------------------------------------------------------ launchers
+// Each returns cudaSuccess or the launch error.
+
+cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
+                        cudaStream_t st);
+
+// Logits of the slabs [slab0, slab0 + nslab) into the workspace scratch,
+// plus per-tile softmax partials. Tensor-core (tcgen05 + TMA) kernel.
+cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
+                             const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
+                             cudaStream_t st);
+
+cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, cudaStream_t st);
+
+// Softmax, max over heads/layers of the wave; the last wave writes imp.
+cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
+                          float* imp, cudaStream_t st);
+
+cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                        const float* imp, float* tok, void* ws, cudaStream_t st);
+
+cudaError_t launch_chunk(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                         const float* tok, float* chunk_score, void* ws, cudaStream_t st);
+
+cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
+                               const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
+                               cudaStream_t st);
+
+cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
+                              const int32_t* chunk_off_check, cudaStream_t st);
+
+// Selection; when `fuse_scan` is set it also writes the per-chunk kept
+// offsets, and the last prompt to finish writes kept_off / n_kept.
+cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                          const int32_t* chunk_off, const float* chunk_score, uint8_t* keep,
+                          void* ws, bool fuse_scan, int32_t* kept_off, int32_t* n_kept,
+                          cudaStream_t st);
+
+cudaError_t launch_gather_scan(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                               const int32_t* chunk_off, const uint8_t* keep, void* ws,
+                               int32_t* kept_off, int32_t* n_kept, cudaStream_t st);
+
+cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                                const int32_t* chunk_off, const uint8_t* keep, int32_t* kept_idx,
+                                int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
+                                cudaStream_t st);
+
+template <typename T>
+inline T* ws_ptr(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace sp

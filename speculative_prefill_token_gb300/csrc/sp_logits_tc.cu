@@ -1,0 +1,489 @@
+// Logits kernel of the SpecPrefill scoring path on fifth-generation tensor
+// cores (sm_103a).
+//
+// For one (layer l, KV head g) "slab" and one prompt, the logits are
+//   s[t, r] = scale * <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>
+// for the prompt's tokens t and the R = L*G query rows r = step*G + head
+// sharing KV head g ("SpecPrefill — Implementation Guide", §How It Works /
+// Attention Capture and Token Importance: one post-softmax row per head and
+// lookahead step; the attention matrix is Q K^T, §Sliding Window / The OOM
+// Problem). Only R rows per slab are needed, so this is a tall-skinny GEMM
+// that streams every key exactly once from HBM:
+//   A = 128 keys x 64 head-dim elements (one TMA box, 128-byte swizzle),
+//   B = R query rows x 64 elements, D = 128 x N fp32 in tensor memory.
+//
+// Roles (320 threads, one CTA per SM, persistent over a contiguous range of
+// (slab, prompt, 128-token tile) work items):
+//   warp 8      TMA producer: K boxes into a ring of 16 KB stages, Q per
+//               (slab, prompt) into one of two buffers;
+//   warp 9      tcgen05.mma issuer (one thread) and TMEM owner;
+//   warps 0-7   two epilogue warpgroups; warpgroup e drains TMEM accumulator
+//               e (tiles alternate), scales to log2 units, stores the logits
+//               row of each token to the scratch and reduces per-tile
+//               softmax partials (row max, sum of exp2) for the later
+//               normaliser.
+// Every mbarrier wait is bounded; a wait that gives up records
+// SP_ERR_TIMEOUT in the workspace status word, and the CTA then drains its
+// own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "sp_internal.h"
+#include "sp_device.cuh"
+#include "sp_ptx.cuh"
+
+namespace sp {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
+constexpr int kMaxStages = 16;
+constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
+constexpr int64_t kDrainSpin = int64_t(1) << 22;
+
+struct TcArgs {
+    const int32_t* seq_off;
+    const int32_t* tile_base;
+    float* logits;   // [nslab][Ntot][Rs]
+    float2* part;    // [nslab][tiles_max][Rs]
+    int32_t* status;
+    const int32_t* bad;
+    int B, Hk, G, R, Rs, d_blocks, Nmma, Nacc, slab0, nslab, stages;
+    int64_t Ntot, tiles_max;
+    uint32_t q_block_bytes;  // Nmma * 128
+    float scale2;
+    int64_t spin;
+};
+
+struct SmemLayout {
+    uint32_t k_ring, q_buf, bars, tmem_slot, abort_flag, stats, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes) {
+    SmemLayout s;
+    uint32_t off = 0;
+    s.k_ring = off;
+    off += static_cast<uint32_t>(stages) * kKBlockBytes;
+    s.q_buf = off;
+    off += 2u * static_cast<uint32_t>(d_blocks) * q_block_bytes;
+    off = (off + 1023u) & ~1023u;
+    s.bars = off;
+    off += 8u * (2 * kMaxStages + 9);
+    s.tmem_slot = off;
+    off += 8;
+    s.abort_flag = off;
+    off += 8;
+    s.stats = off;
+    off += 2u * 4u * kMaxRows * 8u;  // [warpgroup][warp][row] float2
+    s.total = off;
+    return s;
+}
+
+struct Item {
+    int slab;   // local slab index in [0, nslab)
+    int b;      // prompt
+    int64_t tile;  // flattened tile index (for partials)
+    int64_t tok0;  // first global token of the tile
+    int nvalid;    // tokens of the tile inside the prompt
+};
+
+__device__ __forceinline__ Item decode(const TcArgs& a, int64_t w, int64_t T) {
+    Item it;
+    it.slab = static_cast<int>(w / T);
+    it.tile = w - static_cast<int64_t>(it.slab) * T;
+    int lo = 0, hi = a.B - 1;  // largest b with tile_base[b] <= tile
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (a.tile_base[mid] <= it.tile) lo = mid; else hi = mid - 1;
+    }
+    it.b = lo;
+    const int64_t i = it.tile - a.tile_base[lo];
+    const int64_t start = a.seq_off[lo];
+    const int64_t n = static_cast<int64_t>(a.seq_off[lo + 1]) - start;
+    it.tok0 = start + i * kTileTokens;
+    const int64_t rem = n - i * kTileTokens;
+    it.nvalid = static_cast<int>(rem < kTileTokens ? rem : kTileTokens);
+    return it;
+}
+
+__device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_TIMEOUT));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_q, const TcArgs a) {
+    if (*a.bad) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const SmemLayout L = smem_layout(a.stages, a.d_blocks, a.q_block_bytes);
+    const uint32_t base = smem_u32(smem);
+    const uint32_t k_ring = base + L.k_ring;
+    const uint32_t q_buf = base + L.q_buf;
+    const uint32_t bar_full = base + L.bars;
+    const uint32_t bar_empty = bar_full + 8 * kMaxStages;
+    const uint32_t bar_qfull = bar_empty + 8 * kMaxStages;   // [2]
+    const uint32_t bar_qempty = bar_qfull + 16;              // [2]
+    const uint32_t bar_tfull = bar_qempty + 16;              // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;              // [2]
+    const uint32_t bar_drain = bar_tempty + 16;              // [1]
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L.tmem_slot);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+    float2* stats = reinterpret_cast<float2*>(smem + L.stats);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t q_stage_bytes = static_cast<uint32_t>(a.d_blocks) * a.q_block_bytes;
+
+    // ---- setup: barriers, zeroed Q buffers (rows >= R stay zero), TMEM
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_qfull + 8 * i, 1);
+            mbar_init(bar_qempty + 8 * i, 1);
+            mbar_init(bar_tfull + 8 * i, 1);
+            mbar_init(bar_tempty + 8 * i, 128);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    {
+        uint4* qz = reinterpret_cast<uint4*>(smem + L.q_buf);
+        const int n16 = static_cast<int>(2 * q_stage_bytes / 16);
+        for (int i = threadIdx.x; i < n16; i += kThreads) qz[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), static_cast<uint32_t>(2 * a.Nacc));
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_q);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int64_t T = a.tile_base[a.B];
+    const int64_t W = T * a.nslab;
+    const int64_t w_begin = (W * blockIdx.x) / gridDim.x;
+    const int64_t w_end = (W * (blockIdx.x + 1)) / gridDim.x;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            int qn = 0;
+            int64_t prev_key = -1;
+            uint32_t issued_phase[kMaxStages];
+            bool issued[kMaxStages];
+            for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
+            bool ok = true;
+            for (int64_t w = w_begin; w < w_end && ok; ++w) {
+                const Item it = decode(a, w, T);
+                const int slab = a.slab0 + it.slab;
+                const int layer = slab / a.Hk, g = slab - layer * a.Hk;
+                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+                if (key != prev_key) {
+                    const int qb = qn & 1;
+                    if (!mbar_wait_bounded(bar_qempty + 8 * qb, ((qn >> 1) & 1) ^ 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_qfull + 8 * qb,
+                                          static_cast<uint32_t>(a.R) * 128u * a.d_blocks);
+                    for (int kb = 0; kb < a.d_blocks; ++kb)
+                        tma_load_5d(q_buf + qb * q_stage_bytes + kb * a.q_block_bytes, &tmap_q,
+                                    bar_qfull + 8 * qb, kb * 64, g * a.G, 0, layer, it.b);
+                    ++qn;
+                    prev_key = key;
+                }
+                for (int kb = 0; kb < a.d_blocks; ++kb) {
+                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * stage, kKBlockBytes);
+                    tma_load_4d(k_ring + stage * kKBlockBytes, &tmap_k, bar_full + 8 * stage,
+                                kb * 64, static_cast<int>(it.tok0), g, layer, pol);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // drain: every copy this thread issued must land before exit
+            for (int s = 0; s < a.stages; ++s)
+                if (issued[s]) mbar_wait_spin(bar_full + 8 * s, issued_phase[s], kDrainSpin);
+            for (int i = 0; i < 2 && i < qn; ++i) {
+                const int last = (qn - 1 - i);
+                mbar_wait_spin(bar_qfull + 8 * (last & 1), (last >> 1) & 1, kDrainSpin);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, a.Nmma);
+            int stage = 0;
+            uint32_t phase = 0;
+            int qn = 0;
+            int64_t prev_key = -1;
+            int64_t j = 0;
+            int qb = 0;
+            bool ok = true;
+            bool any_mma = false;
+            for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
+                const Item it = decode(a, w, T);
+                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+                if (key != prev_key) {
+                    if (qn > 0) tc_commit(bar_qempty + 8 * ((qn - 1) & 1));
+                    qb = qn & 1;
+                    if (!mbar_wait_bounded(bar_qfull + 8 * qb, (qn >> 1) & 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ++qn;
+                    prev_key = key;
+                }
+                const int acc = static_cast<int>(j & 1);
+                if (!mbar_wait_bounded(bar_tempty + 8 * acc, static_cast<uint32_t>(((j >> 1) & 1) ^ 1),
+                                       a.spin, abort_flag)) {
+                    record_timeout(a, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * a.Nacc);
+                for (int kb = 0; kb < a.d_blocks; ++kb) {
+                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = k_ring + stage * kKBlockBytes;
+                    const uint32_t b_addr = q_buf + qb * q_stage_bytes + kb * a.q_block_bytes;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + 32 * k4),
+                                    smem_desc_sw128(b_addr + 32 * k4), idesc, (kb | k4) != 0);
+                    }
+                    any_mma = true;
+                    tc_commit(bar_empty + 8 * stage);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar_tfull + 8 * acc);
+            }
+            // drain: all MMAs issued by this thread complete before TMEM is freed
+            if (any_mma) {
+                tc_commit(bar_drain);
+                mbar_wait_spin(bar_drain, 0, kDrainSpin);
+            }
+        }
+    } else {
+        // epilogue warpgroups
+        const int e = warp >> 2;          // warpgroup: owns accumulator e
+        const int qw = warp & 3;          // TMEM lane quarter
+        const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+        int64_t j = 0;
+        for (int64_t w = w_begin; w < w_end; ++w, ++j) {
+            if (static_cast<int>(j & 1) != e) continue;
+            const Item it = decode(a, w, T);
+            // all 128 threads of the warpgroup take the same decision, so the
+            // named barriers below never wait for a thread that left
+            const bool got = mbar_wait_bounded(bar_tfull + 8 * e, static_cast<uint32_t>((j >> 1) & 1),
+                                               a.spin, abort_flag);
+            if (!bar_sync_and(1 + e, 128, got)) {
+                record_timeout(a, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            float v[2][32];
+            const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(e * a.Nacc);
+            tmem_ld_32x32b_x32(taddr, v[0]);
+            if (a.Nmma > 32) tmem_ld_32x32b_x32(taddr + 32, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
+                if (r >= a.Nmma) v[0][r] = 0.0f;
+            tc_fence_before();
+            mbar_arrive(bar_tempty + 8 * e);
+
+            const int tl = qw * 32 + lane;
+            const bool valid = tl < it.nvalid;
+            const int halves = a.R > 32 ? 2 : 1;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh < halves) {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) v[hh][r] = valid ? v[hh][r] * a.scale2 : -INFINITY;
+                }
+            }
+            if (valid) {
+                float* dst = a.logits + (static_cast<int64_t>(it.slab) * a.Ntot + it.tok0 + tl) * a.Rs;
+                const int n4 = a.Rs >> 2;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    if (c < n4) {
+                        const float* src = &v[c >> 3][(c & 7) * 4];
+                        reinterpret_cast<float4*>(dst)[c] = make_float4(src[0], src[1], src[2], src[3]);
+                    }
+                }
+            }
+            float2* st = stats + (e * 4) * kMaxRows;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh < halves) {
+                    const float2 pr = warp_row_partials(v[hh]);
+                    st[qw * kMaxRows + hh * 32 + lane] = pr;
+                }
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + e) : "memory");
+            if (qw == 0) {
+                for (int r = lane; r < a.R; r += 32) {
+                    float2 acc2 = st[r];
+                    acc2 = merge_partial(acc2, st[kMaxRows + r]);
+                    acc2 = merge_partial(acc2, st[2 * kMaxRows + r]);
+                    acc2 = merge_partial(acc2, st[3 * kMaxRows + r]);
+                    a.part[(static_cast<int64_t>(it.slab) * a.tiles_max + it.tile) * a.Rs + r] = acc2;
+                }
+            }
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + e) : "memory");
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(2 * a.Nacc));
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
+                             const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
+                             cudaStream_t st) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int d = pl.d;
+    CUtensorMap tk, tq;
+    {
+        // K: dims (d, token, kv head, layer); unused strides get a harmless value
+        const int64_t sh = pl.Hk > 1 ? s->k_stride_head : d;
+        const int64_t sl = pl.Ly > 1 ? s->k_stride_layer : d;
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(pl.Ntot),
+                              static_cast<cuuint64_t>(pl.Hk), static_cast<cuuint64_t>(pl.Ly)};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(s->k_stride_token) * 2,
+                                 static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sl) * 2};
+        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileTokens), 1, 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(k), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // Q: dims (d, q head, step, layer, prompt); box = the G heads x L steps of one slab
+        const int64_t sh = pl.Hq > 1 ? s->q_stride_head : d;
+        const int64_t ss = pl.L > 1 ? s->q_stride_step : d;
+        const int64_t sl = pl.Ly > 1 ? s->q_stride_layer : d;
+        const int64_t sb = pl.B > 1 ? s->q_stride_seq : d;
+        cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(pl.Hq),
+                              static_cast<cuuint64_t>(pl.L), static_cast<cuuint64_t>(pl.Ly),
+                              static_cast<cuuint64_t>(pl.B)};
+        cuuint64_t strides[4] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(ss) * 2,
+                                 static_cast<cuuint64_t>(sl) * 2, static_cast<cuuint64_t>(sb) * 2};
+        cuuint32_t box[5] = {64, static_cast<cuuint32_t>(pl.G), static_cast<cuuint32_t>(pl.L), 1, 1};
+        cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<uint16_t*>(q), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    TcArgs a;
+    a.seq_off = seq_off;
+    a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
+    a.logits = ws_ptr<float>(ws, pl.o_logits);
+    a.part = ws_ptr<float2>(ws, pl.o_part);
+    a.status = &ws_ptr<WsHeader>(ws, 0)->status;
+    a.bad = &ws_ptr<WsHeader>(ws, 0)->bad_input;
+    a.B = pl.B;
+    a.Hk = pl.Hk;
+    a.G = pl.G;
+    a.R = pl.R;
+    a.Rs = pl.Rs;
+    a.d_blocks = d / 64;
+    a.Nmma = pl.Nmma;
+    a.Nacc = pl.Nacc;
+    a.slab0 = slab0;
+    a.nslab = nslab;
+    a.Ntot = pl.Ntot;
+    a.tiles_max = pl.tiles_max;
+    a.q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
+    a.scale2 = pl.scale2;
+    a.spin = pl.spin;
+
+    const uint32_t q_bytes = 2u * a.d_blocks * a.q_block_bytes;
+    const uint32_t fixed = smem_layout(0, a.d_blocks, a.q_block_bytes).total + 1024;
+    int stages = static_cast<int>((kSmemLimit - fixed) / kKBlockBytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2 || q_bytes > kSmemLimit) return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    const uint32_t smem = smem_layout(stages, a.d_blocks, a.q_block_bytes).total + 1024;
+
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t err = cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const int64_t work = pl.tiles_max * nslab;
+    const int grid = static_cast<int>(work < sms ? work : sms);
+    logits_tc_kernel<<<grid, kThreads, smem, st>>>(tk, tq, a);
+    return cudaGetLastError();
+}
+
+}  // namespace sp

@@ -1,0 +1,706 @@
+// Stage kernels of the SpecPrefill scoring path after (and around) the
+// logits: per-call offsets, softmax normalisers, token importance, pooling,
+// chunk scores, selection and the kept-token gather.
+//
+// Method steps (pages: "SpecPrefill — Implementation Guide" v2/v3.1 of the
+// sliding-specprefill project; llama.cpp PR "Speculative prefill"):
+//   normaliser + importance  guide §How It Works / Token Importance
+//   pool (W = 13)            PR §Approach item 3
+//   normalise                guide v3.1 §v3.1 Optimizations item 5
+//   boost                    guide v3 §v3 Improvements item 2
+//   chunk mean, ranking      guide §Chunk Selection
+//   cumulative mass          guide v3 §v3 Improvements item 1
+//   forced BOS / last chunk  PR §Approach item 4
+//   kept list + positions    guide §How It Works / Sparse Prefill
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+
+namespace sp {
+namespace {
+
+__device__ __forceinline__ void set_status(WsHeader* h, int code) { atomicCAS(&h->status, 0, code); }
+
+// ------------------------------------------------------------------ prep
+// One CTA: validates seq_off (0 = first, non-decreasing, last = Ntot) and
+// writes the per-prompt bases of logits tiles, chunks and post blocks.
+// A user-provided chunk_off (standalone select/gather) must match.
+constexpr int kPrepThreads = 1024;
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_off, int B,
+                                                            int64_t Ntot, int C, int64_t Tb,
+                                                            int32_t* tile_base, int32_t* chunk_off,
+                                                            int32_t* pblk_base, int32_t* chunk_off_out,
+                                                            const int32_t* chunk_off_check,
+                                                            WsHeader* hdr) {
+    __shared__ int bad;
+    __shared__ int64_t warp_sums[3][32];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        bad = (seq_off[0] != 0 || static_cast<int64_t>(seq_off[B]) != Ntot) ? 1 : 0;
+        hdr->ticket = 0u;
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += kPrepThreads)
+        if (seq_off[b + 1] < seq_off[b]) bad = 1;
+    __syncthreads();
+    const int per = (B + kPrepThreads - 1) / kPrepThreads;
+    const int lo = min(B, tid * per), hi = min(B, lo + per);
+    int64_t sums[3] = {0, 0, 0};
+    if (!bad) {
+        for (int b = lo; b < hi; ++b) {
+            const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
+            sums[0] += (n + kTileTokens - 1) / kTileTokens;
+            sums[1] += (n + C - 1) / C;
+            sums[2] += (n + Tb - 1) / Tb;
+        }
+    }
+    // block exclusive scan of the three per-thread totals
+    const int lane = tid & 31, warp = tid >> 5;
+    int64_t incl[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        int64_t v = sums[k];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        incl[k] = v;
+        if (lane == 31) warp_sums[k][warp] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            int64_t v = warp_sums[k][lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            warp_sums[k][lane] = v;  // inclusive over warps
+        }
+    }
+    __syncthreads();
+    int64_t run[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) run[k] = incl[k] - sums[k] + (warp > 0 ? warp_sums[k][warp - 1] : 0);
+    for (int b = lo; b < hi; ++b) {
+        const int64_t n = bad ? 0 : static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
+        tile_base[b] = static_cast<int32_t>(run[0]);
+        chunk_off[b] = static_cast<int32_t>(run[1]);
+        pblk_base[b] = static_cast<int32_t>(run[2]);
+        if (chunk_off_out) chunk_off_out[b] = static_cast<int32_t>(run[1]);
+        if (chunk_off_check && chunk_off_check[b] != static_cast<int32_t>(run[1])) bad = 1;
+        run[0] += (n + kTileTokens - 1) / kTileTokens;
+        run[1] += (n + C - 1) / C;
+        run[2] += (n + Tb - 1) / Tb;
+    }
+    if (hi == B && lo < hi) {
+        tile_base[B] = static_cast<int32_t>(run[0]);
+        chunk_off[B] = static_cast<int32_t>(run[1]);
+        pblk_base[B] = static_cast<int32_t>(run[2]);
+        if (chunk_off_out) chunk_off_out[B] = static_cast<int32_t>(run[1]);
+        if (chunk_off_check && chunk_off_check[B] != static_cast<int32_t>(run[1])) bad = 1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        hdr->bad_input = bad;
+        if (bad) set_status(hdr, SP_ERR_DEVICE);
+    }
+}
+
+// ------------------------------------------------------------ normaliser
+// lse2[slab][b][r] = log2 sum_t exp2(s2[t, r]) over prompt b's keys, merged
+// from the per-tile partials (max, sum exp2(x - max)).
+__global__ void __launch_bounds__(256) lse_kernel(const float2* part, const int32_t* tile_base,
+                                                  float* lse2, int B, int R, int Rs,
+                                                  int64_t tiles_max, const int32_t* bad) {
+    if (*bad) return;
+    __shared__ float2 acc_s[8][kMaxRows];
+    const int slab = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = tile_base[b], t1 = tile_base[b + 1];
+    for (int r = lane; r < kMaxRows; r += 32) {
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        if (r < R)
+            for (int64_t t = t0 + warp; t < t1; t += 8)
+                acc = merge_partial(acc, part[(static_cast<int64_t>(slab) * tiles_max + t) * Rs + r]);
+        acc_s[warp][r] = acc;
+    }
+    __syncthreads();
+    const int r = threadIdx.x;
+    if (r < R) {
+        float2 acc = acc_s[0][r];
+        for (int w = 1; w < 8; ++w) acc = merge_partial(acc, acc_s[w][r]);
+        lse2[(static_cast<int64_t>(slab) * B + b) * Rs + r] = acc.y > 0.0f ? acc.x + log2f(acc.y) : INFINITY;
+    }
+}
+
+// --------------------------------------------------------------- reduce
+// Token importance: for every token t of a tile and lookahead step l,
+// a_l = max over the wave's slabs and the G heads of (s2 - lse2) (log2 of
+// the softmax probability), combined with earlier waves by max; the last
+// wave writes imp[t] = (1/L) sum_l exp2(a_l).
+__global__ void __launch_bounds__(kTileTokens) reduce_kernel(const float* logits, const float* lse2,
+                                                             const int32_t* seq_off,
+                                                             const int32_t* tile_base, float* alog,
+                                                             float* imp, int B, int G, int L, int R,
+                                                             int Rs, int nslab, int64_t Ntot,
+                                                             int first_wave, int last_wave,
+                                                             const int32_t* bad) {
+    if (*bad) return;
+    const int64_t tile = blockIdx.x;
+    if (tile >= tile_base[B]) return;
+    extern __shared__ float sm[];
+    float* rows = sm;                                // [128][Rs + 1]
+    float* lse_s = rows + kTileTokens * (Rs + 1);    // [nslab][Rs]
+    float* amax = lse_s + nslab * Rs;                // [L][128]
+    const int b = search_base(tile_base, B, tile);
+    const int64_t i = tile - tile_base[b];
+    const int64_t start = seq_off[b];
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    const int64_t tok0 = start + i * kTileTokens;
+    const int nvalid = static_cast<int>(min64(kTileTokens, n - i * kTileTokens));
+    const int t = threadIdx.x;
+    for (int idx = t; idx < nslab * Rs; idx += kTileTokens) {
+        const int s = idx / Rs, r = idx - s * Rs;
+        lse_s[idx] = r < R ? lse2[(static_cast<int64_t>(s) * B + b) * Rs + r] : 0.0f;
+    }
+    for (int l = 0; l < L; ++l) amax[l * kTileTokens + t] = -INFINITY;
+    for (int s = 0; s < nslab; ++s) {
+        __syncthreads();
+        const float* src = logits + (static_cast<int64_t>(s) * Ntot + tok0) * Rs;
+        const int nflt = nvalid * Rs;
+        for (int idx = t; idx < nflt; idx += kTileTokens) {
+            const int tt = idx / Rs, r = idx - tt * Rs;
+            rows[tt * (Rs + 1) + r] = src[idx];
+        }
+        __syncthreads();
+        if (t < nvalid) {
+            const float* row = rows + t * (Rs + 1);
+            const float* ls = lse_s + s * Rs;
+            for (int l = 0; l < L; ++l) {
+                float m = amax[l * kTileTokens + t];
+                for (int j = 0; j < G; ++j) m = fmaxf(m, row[l * G + j] - ls[l * G + j]);
+                amax[l * kTileTokens + t] = m;
+            }
+        }
+    }
+    if (t < nvalid) {
+        const int64_t tok = tok0 + t;
+        float total = 0.0f;
+        for (int l = 0; l < L; ++l) {
+            float m = amax[l * kTileTokens + t];
+            if (!first_wave) m = fmaxf(m, alog[l * Ntot + tok]);
+            if (last_wave) total += exp2f(m);
+            else alog[l * Ntot + tok] = m;
+        }
+        if (last_wave) imp[tok] = total / static_cast<float>(L);
+    }
+}
+
+// ----------------------------------------------------------------- pool
+// x[t] = mean of imp over [t - W/2, t + W/2] clipped to the prompt; per
+// block min/max of x for the normalisation.
+__global__ void __launch_bounds__(256) pool_kernel(const float* imp, float* tok, float2* ppart,
+                                                   const int32_t* seq_off, const int32_t* pblk_base,
+                                                   int B, int W, int64_t Tb, const int32_t* bad) {
+    if (*bad) return;
+    const int64_t blk = blockIdx.x;
+    if (blk >= pblk_base[B]) return;
+    extern __shared__ float win[];
+    __shared__ float red_min[8], red_max[8];
+    const int b = search_base(pblk_base, B, blk);
+    const int64_t i = blk - pblk_base[b];
+    const int64_t start = seq_off[b];
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    const int64_t t0 = i * Tb, t1 = min64(n, t0 + Tb);
+    const int h = W / 2;
+    const int64_t lo = max64(0, t0 - h), hi = min64(n, t1 + h);
+    for (int64_t u = lo + threadIdx.x; u < hi; u += blockDim.x) win[u - lo] = imp[start + u];
+    __syncthreads();
+    float mn = INFINITY, mx = -INFINITY;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+        const int64_t u0 = max64(0, t - h), u1 = min64(n - 1, t + h);
+        float s = 0.0f;
+        for (int64_t u = u0; u <= u1; ++u) s += win[u - lo];
+        const float x = s / static_cast<float>(u1 - u0 + 1);
+        tok[start + t] = x;
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        red_min[warp] = mn;
+        red_max[warp] = mx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+            mn = fminf(mn, red_min[w]);
+            mx = fmaxf(mx, red_max[w]);
+        }
+        ppart[blk] = make_float2(mn, mx);
+    }
+}
+
+// ---------------------------------------------------------------- chunk
+// y = normalise(x) (optional) then boost, and the mean of y over each
+// chunk of the block.
+__global__ void __launch_bounds__(256) chunk_kernel(const float* tok, const float2* ppart,
+                                                    float* chunk_score, const int32_t* seq_off,
+                                                    const int32_t* pblk_base, const int32_t* chunk_off,
+                                                    int B, int C, int64_t Tb, int normalize,
+                                                    float bf_mult, int bf_n, float bl_mult, int bl_n,
+                                                    const int32_t* bad) {
+    if (*bad) return;
+    const int64_t blk = blockIdx.x;
+    if (blk >= pblk_base[B]) return;
+    extern __shared__ float ys[];
+    __shared__ float red_min[8], red_max[8];
+    __shared__ float s_mn, s_mx;
+    const int b = search_base(pblk_base, B, blk);
+    const int64_t i = blk - pblk_base[b];
+    const int64_t start = seq_off[b];
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    const int64_t t0 = i * Tb, t1 = min64(n, t0 + Tb);
+    if (normalize) {
+        float mn = INFINITY, mx = -INFINITY;
+        for (int64_t p = pblk_base[b] + threadIdx.x; p < pblk_base[b + 1]; p += blockDim.x) {
+            const float2 v = ppart[p];
+            mn = fminf(mn, v.x);
+            mx = fmaxf(mx, v.y);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (lane == 0) {
+            red_min[warp] = mn;
+            red_max[warp] = mx;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+                mn = fminf(mn, red_min[w]);
+                mx = fmaxf(mx, red_max[w]);
+            }
+            s_mn = mn;
+            s_mx = mx;
+        }
+        __syncthreads();
+    }
+    const float mn = normalize ? s_mn : 0.0f, mx = normalize ? s_mx : 0.0f;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+        float y = tok[start + t];
+        if (normalize) y = (mx == mn) ? 1.0f : (y - mn) / (mx - mn);
+        if (t < bf_n) y *= bf_mult;
+        if (t >= n - bl_n) y *= bl_mult;
+        ys[t - t0] = y;
+    }
+    __syncthreads();
+    const int64_t c0 = t0 / C, c1 = (t1 + C - 1) / C;
+    for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+        const int64_t a0 = c * C, a1 = min64(t1, a0 + C);
+        float s = 0.0f;
+        for (int64_t t = a0; t < a1; ++t) s += ys[t - t0];
+        chunk_score[chunk_off[b] + c] = s / static_cast<float>(a1 - a0);
+    }
+}
+
+// --------------------------------------------------------------- select
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ uint32_t desc_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending order key
+    return ~ord;                                                       // descending
+}
+
+// Block-wide inclusive scan of one int64 per thread.
+__device__ __forceinline__ int64_t block_scan_i64(int64_t v, int64_t* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int64_t r = v + (warp > 0 ? warp_tot[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ double block_scan_f64(double v, double* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        double w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const double r = v + (warp > 0 ? warp_tot[warp - 1] : 0.0);
+    __syncthreads();
+    return r;
+}
+
+// Per-prompt kept-token counts of each chunk, their exclusive scan, the
+// prompt's total; the last prompt to finish (ticket) writes kept_off and
+// n_kept for the whole batch. `flags` is the prompt's chunk_keep in shared
+// or global memory.
+__device__ void scan_kept(const uint8_t* flags, int64_t nc, int64_t n, int C, int force_bos, int b,
+                          int B, int32_t* ckoff, int32_t* pcount, int32_t* kept_off,
+                          int32_t* n_kept, WsHeader* hdr, int64_t* scratch) {
+    __shared__ int64_t carry;
+    __shared__ bool last;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < nc; base += blockDim.x) {
+        const int64_t c = base + threadIdx.x;
+        int64_t cnt = 0;
+        if (c < nc) {
+            const int64_t size = min64(C, n - c * C);
+            cnt = flags[c] ? size : ((c == 0 && force_bos && n > 0) ? 1 : 0);
+        }
+        const int64_t incl = block_scan_i64(cnt, scratch);
+        if (c < nc) ckoff[c] = static_cast<int32_t>(carry + incl - cnt);
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry += incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        pcount[b] = static_cast<int32_t>(carry);
+        __threadfence();
+        const unsigned prev = atomicAdd(&hdr->ticket, 1u);
+        last = (prev == static_cast<unsigned>(B - 1));
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += blockDim.x) {
+        const int bb = base + threadIdx.x;
+        const int64_t v = bb < B ? static_cast<int64_t>(__ldcg(pcount + bb)) : 0;
+        const int64_t incl = block_scan_i64(v, scratch);
+        if (bb < B) kept_off[bb] = static_cast<int32_t>(carry + incl - v);
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry += incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        kept_off[B] = static_cast<int32_t>(carry);
+        *n_kept = static_cast<int32_t>(carry);
+        hdr->ticket = 0u;
+    }
+}
+
+struct SelectArgs {
+    const int32_t* seq_off;
+    const int32_t* chunk_off;
+    const float* chunk_score;
+    uint8_t* keep;
+    int32_t* ckoff;
+    int32_t* pcount;
+    int32_t* kept_off;
+    int32_t* n_kept;
+    WsHeader* hdr;
+    int B, C, mode, force_bos, force_last, sort_cap, fuse_scan;
+    float keep_p, mass;
+};
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
+    if (a.hdr->bad_input) return;
+    extern __shared__ uint64_t keys[];  // [sort_cap], then flags bytes
+    uint8_t* flags = reinterpret_cast<uint8_t*>(keys + a.sort_cap);
+    __shared__ int64_t scan_i[32];
+    __shared__ double scan_d[32];
+    __shared__ int k_sel;
+    const int b = blockIdx.x;
+    const int64_t c0 = a.chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - c0;
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - a.seq_off[b];
+    const int tid = threadIdx.x;
+    const bool too_many = nc > a.sort_cap;
+    if (too_many && tid == 0) atomicCAS(&a.hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
+    int64_t P = 1;
+    while (P < nc) P <<= 1;
+    if (!too_many && nc > 0) {
+        for (int64_t i = tid; i < P; i += kSelThreads)
+            keys[i] = i < nc ? (static_cast<uint64_t>(desc_key(a.chunk_score[c0 + i])) << 32) |
+                                   static_cast<uint64_t>(i)
+                             : ~0ull;
+        for (int64_t i = tid; i < nc; i += kSelThreads) flags[i] = 0;
+        __syncthreads();
+        // bitonic sort, ascending: score descending, then chunk index ascending
+        for (int64_t k = 2; k <= P; k <<= 1) {
+            for (int64_t j = k >> 1; j > 0; j >>= 1) {
+                for (int64_t i = tid; i < P; i += kSelThreads) {
+                    const int64_t ixj = i ^ j;
+                    if (ixj > i) {
+                        const uint64_t x = keys[i], y = keys[ixj];
+                        const bool up = (i & k) == 0;
+                        if ((x > y) == up) {
+                            keys[i] = y;
+                            keys[ixj] = x;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        if (a.mode == SP_MODE_FIXED) {
+            if (tid == 0) {
+                const double kk = ceil(static_cast<double>(nc) * static_cast<double>(a.keep_p));
+                int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
+                k_sel = static_cast<int>(k > nc ? nc : k);
+            }
+        } else {
+            // cumulative mass over the ranking, fp64 running sums
+            const int64_t per = (P + kSelThreads - 1) / kSelThreads;
+            const int64_t lo = min64(nc, tid * per), hi = min64(nc, lo + per);
+            double local = 0.0;
+            for (int64_t i = lo; i < hi; ++i)
+                local += static_cast<double>(a.chunk_score[c0 + static_cast<int64_t>(keys[i] & 0xffffffffu)]);
+            const double incl = block_scan_f64(local, scan_d);
+            __shared__ double total_s;
+            if (tid == kSelThreads - 1) total_s = incl;
+            if (tid == 0) k_sel = static_cast<int>(nc);
+            __syncthreads();
+            const double total = total_s;
+            if (total > 0.0) {
+                const double theta = static_cast<double>(a.mass) * total;
+                double cum = incl - local;
+                for (int64_t i = lo; i < hi; ++i) {
+                    const double before = cum;
+                    cum += static_cast<double>(a.chunk_score[c0 + static_cast<int64_t>(keys[i] & 0xffffffffu)]);
+                    if (cum >= theta && before < theta) k_sel = static_cast<int>(i + 1);
+                }
+            }
+        }
+        __syncthreads();
+        const int ks = k_sel;
+        for (int64_t i = tid; i < ks; i += kSelThreads) flags[keys[i] & 0xffffffffu] = 1;
+        __syncthreads();
+        if (a.force_last && tid == 0) flags[nc - 1] |= 2;
+        __syncthreads();
+        for (int64_t i = tid; i < nc; i += kSelThreads) a.keep[c0 + i] = flags[i];
+        __syncthreads();
+    }
+    if (a.fuse_scan) {
+        const int64_t ncs = too_many ? 0 : nc;
+        scan_kept(flags, ncs, n, a.C, a.force_bos, b, a.B, a.ckoff + c0, a.pcount, a.kept_off,
+                  a.n_kept, a.hdr, scan_i);
+    }
+}
+
+__global__ void __launch_bounds__(kSelThreads) gather_scan_kernel(
+    const int32_t* seq_off, const int32_t* chunk_off, const uint8_t* keep, int32_t* ckoff,
+    int32_t* pcount, int32_t* kept_off, int32_t* n_kept, WsHeader* hdr, int B, int C,
+    int force_bos) {
+    if (hdr->bad_input) return;
+    __shared__ int64_t scan_i[32];
+    const int b = blockIdx.x;
+    const int64_t c0 = chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(chunk_off[b + 1]) - c0;
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
+    scan_kept(keep + c0, nc, n, C, force_bos, b, B, ckoff + c0, pcount, kept_off, n_kept, hdr,
+              scan_i);
+}
+
+// --------------------------------------------------------------- gather
+// One warp per chunk writes its kept tokens (global index, position).
+__global__ void __launch_bounds__(256) gather_write_kernel(
+    const int32_t* seq_off, const int32_t* chunk_off, const uint8_t* keep, const int32_t* ckoff,
+    const int32_t* kept_off, int32_t* kept_idx, int32_t* kept_pos, int B, int C, int force_bos,
+    const int32_t* bad) {
+    if (*bad) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t cg = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+    if (cg >= chunk_off[B]) return;
+    const int b = search_base(chunk_off, B, cg);
+    const int64_t c = cg - chunk_off[b];
+    const int64_t start = seq_off[b];
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    const int64_t base = static_cast<int64_t>(kept_off[b]) + ckoff[cg];
+    if (keep[cg]) {
+        const int64_t a0 = c * C, a1 = min64(n, a0 + C);
+        for (int64_t t = a0 + lane; t < a1; t += 32) {
+            kept_idx[base + (t - a0)] = static_cast<int32_t>(start + t);
+            kept_pos[base + (t - a0)] = static_cast<int32_t>(t);
+        }
+    } else if (c == 0 && force_bos && n > 0 && lane == 0) {
+        kept_idx[base] = static_cast<int32_t>(start);
+        kept_pos[base] = 0;
+    }
+}
+
+}  // namespace
+
+// ================================================================ launchers
+
+cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
+                        cudaStream_t st) {
+    prep_kernel<<<1, kPrepThreads, 0, st>>>(seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
+                                            ws_ptr<int32_t>(ws, pl.o_tile_base),
+                                            ws_ptr<int32_t>(ws, pl.o_chunk_off),
+                                            ws_ptr<int32_t>(ws, pl.o_pblk_base), chunk_off_out,
+                                            nullptr, ws_ptr<WsHeader>(ws, 0));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
+                              const int32_t* chunk_off_check, cudaStream_t st) {
+    prep_kernel<<<1, kPrepThreads, 0, st>>>(seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
+                                            ws_ptr<int32_t>(ws, pl.o_tile_base),
+                                            ws_ptr<int32_t>(ws, pl.o_chunk_off),
+                                            ws_ptr<int32_t>(ws, pl.o_pblk_base), nullptr,
+                                            chunk_off_check, ws_ptr<WsHeader>(ws, 0));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, cudaStream_t st) {
+    dim3 grid(static_cast<unsigned>(nslab), static_cast<unsigned>(pl.B));
+    lse_kernel<<<grid, 256, 0, st>>>(ws_ptr<float2>(ws, pl.o_part), ws_ptr<int32_t>(ws, pl.o_tile_base),
+                                     ws_ptr<float>(ws, pl.o_lse), pl.B, pl.R, pl.Rs, pl.tiles_max,
+                                     &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
+                          float* imp, cudaStream_t st) {
+    const size_t smem = sizeof(float) * (static_cast<size_t>(kTileTokens) * (pl.Rs + 1) +
+                                         static_cast<size_t>(nslab) * pl.Rs +
+                                         static_cast<size_t>(pl.L) * kTileTokens);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    reduce_kernel<<<static_cast<unsigned>(pl.tiles_max), kTileTokens, smem, st>>>(
+        ws_ptr<float>(ws, pl.o_logits), ws_ptr<float>(ws, pl.o_lse), seq_off,
+        ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
+        pl.R, pl.Rs, nslab, pl.Ntot, wave == 0 ? 1 : 0, wave == pl.waves - 1 ? 1 : 0,
+        &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                        const float* imp, float* tok, void* ws, cudaStream_t st) {
+    const size_t smem = sizeof(float) * static_cast<size_t>(pl.Tb + 2 * (p->pool_w / 2));
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(pool_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    pool_kernel<<<static_cast<unsigned>(pl.pblk_max), 256, smem, st>>>(
+        imp, tok, ws_ptr<float2>(ws, pl.o_ppart), seq_off, ws_ptr<int32_t>(ws, pl.o_pblk_base),
+        pl.B, p->pool_w, pl.Tb, &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                         const float* tok, float* chunk_score, void* ws, cudaStream_t st) {
+    const size_t smem = sizeof(float) * static_cast<size_t>(pl.Tb);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    chunk_kernel<<<static_cast<unsigned>(pl.pblk_max), 256, smem, st>>>(
+        tok, ws_ptr<float2>(ws, pl.o_ppart), chunk_score, seq_off,
+        ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_chunk_off), pl.B, pl.C, pl.Tb,
+        p->normalize, p->boost_first_mult, p->boost_first_n, p->boost_last_mult, p->boost_last_n,
+        &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                          const int32_t* chunk_off, const float* chunk_score, uint8_t* keep,
+                          void* ws, bool fuse_scan, int32_t* kept_off, int32_t* n_kept,
+                          cudaStream_t st) {
+    SelectArgs a;
+    a.seq_off = seq_off;
+    a.chunk_off = chunk_off;
+    a.chunk_score = chunk_score;
+    a.keep = keep;
+    a.ckoff = ws_ptr<int32_t>(ws, pl.o_ckoff);
+    a.pcount = ws_ptr<int32_t>(ws, pl.o_pcount);
+    a.kept_off = kept_off;
+    a.n_kept = n_kept;
+    a.hdr = ws_ptr<WsHeader>(ws, 0);
+    a.B = pl.B;
+    a.C = pl.C;
+    a.mode = p->mode;
+    a.force_bos = p->force_bos;
+    a.force_last = p->force_last_chunk;
+    a.sort_cap = pl.sort_cap;
+    a.fuse_scan = fuse_scan ? 1 : 0;
+    a.keep_p = p->keep_p;
+    a.mass = p->mass;
+    const size_t smem = static_cast<size_t>(pl.sort_cap) * 9;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    select_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_scan(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                               const int32_t* chunk_off, const uint8_t* keep, void* ws,
+                               int32_t* kept_off, int32_t* n_kept, cudaStream_t st) {
+    gather_scan_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, 0, st>>>(
+        seq_off, chunk_off, keep, ws_ptr<int32_t>(ws, pl.o_ckoff), ws_ptr<int32_t>(ws, pl.o_pcount),
+        kept_off, n_kept, ws_ptr<WsHeader>(ws, 0), pl.B, pl.C, p->force_bos);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                                const int32_t* chunk_off, const uint8_t* keep, int32_t* kept_idx,
+                                int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
+                                cudaStream_t st) {
+    (void)n_kept;
+    const unsigned grid = static_cast<unsigned>((pl.chunks_max + 7) / 8);
+    gather_write_kernel<<<grid, 256, 0, st>>>(seq_off, chunk_off, keep, ws_ptr<int32_t>(ws, pl.o_ckoff),
+                                              kept_off, kept_idx, kept_pos, pl.B, pl.C, p->force_bos,
+                                              &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+}  // namespace sp

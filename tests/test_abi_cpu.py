@@ -1,0 +1,120 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every symbol declared in include/*.h, and rejects bad arguments on the host
+(these calls enqueue nothing, so no GPU is needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_prefill_token_gb300 as sp
+from speculative_prefill_token_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sp.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(sp_[a-z_0-9]+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("sp_attn_importance", "sp_pool_chunk", "sp_select", "sp_gather_kept",
+                     "sp_specprefill_score", "sp_workspace_size", "sp_get_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} is declared but not exported"
+
+
+def test_build_info_and_status_strings(lib):
+    assert b"sm_103a" in lib.sp_build_info()
+    assert lib.sp_status_string(0) == b"ok"
+    assert lib.sp_status_string(5) == b"a bounded device wait gave up"
+    assert lib.sp_status_string(99) == b"unknown status"
+
+
+def _shape(**kw):
+    base = dict(n_seqs=1, n_layers=6, n_q_heads=8, n_kv_heads=2, head_dim=256, n_lookahead=8,
+                n_tokens_total=32768)
+    base.update(kw)
+    d, ntot, hk = base["head_dim"], base["n_tokens_total"], base["n_kv_heads"]
+    hq, steps, ly = base["n_q_heads"], base["n_lookahead"], base["n_layers"]
+    return sp._Shape(base["n_seqs"], ly, hq, hk, d, steps, ntot, 0,
+                     ntot * hk * d, hk * d, d, ly * steps * hq * d, steps * hq * d, hq * d, d)
+
+
+def _ws(shape, params):
+    n = ctypes.c_size_t()
+    rc = sp.lib().sp_workspace_size(ctypes.byref(shape), ctypes.byref(params._c()), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_size_valid(lib):
+    rc, n = _ws(_shape(), sp.SelectionParams(mode="fixed", keep_p=0.15))
+    assert rc == 0
+    # logits scratch of all 12 slabs (32 rows fp32) is the dominant term
+    assert n >= 12 * 32768 * 32 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), 2),          # unsupported head_dim
+    (dict(n_q_heads=6, n_kv_heads=4), 1),  # Hq not a multiple of Hk
+    (dict(n_lookahead=17), 2),       # L*G = 68 > 64 rows
+    (dict(n_tokens_total=0), 1),
+    (dict(n_seqs=0), 1),
+])
+def test_bad_shapes_rejected(lib, kw, code):
+    rc, _ = _ws(_shape(**kw), sp.SelectionParams())
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw", [
+    dict(pool_w=12), dict(pool_w=0), dict(chunk=0), dict(mode="fixed", keep_p=0.0),
+    dict(mode="fixed", keep_p=1.5), dict(mode="mass", mass=0.0), dict(boost_first_mult=0.0),
+    dict(boost_last_n=-1), dict(scale=-1.0),
+])
+def test_bad_params_rejected(lib, kw):
+    rc, _ = _ws(_shape(), sp.SelectionParams(**kw))
+    assert rc == 1
+
+
+def test_misaligned_stride_rejected(lib):
+    s = _shape()
+    s.k_stride_token = 2 * 256 + 4   # 1032 bytes: not a multiple of 16
+    rc, _ = _ws(s, sp.SelectionParams())
+    assert rc == 2
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    s, p = _shape(), sp.SelectionParams()
+    rc = lib.sp_attn_importance(ctypes.byref(s), ctypes.byref(p._c()), None, None, None, None,
+                                None, 0, None)
+    assert rc == 1
+    rc = lib.sp_get_device_status(None, 0, None, 0, None)
+    assert rc == 1
+
+
+def test_workspace_checks(lib):
+    s, p = _shape(n_tokens_total=512), sp.SelectionParams()
+    buf = (ctypes.c_uint8 * 1024)()
+    rc = lib.sp_workspace_init(None, 0, None)
+    assert rc == 3
+    rc = lib.sp_workspace_init(ctypes.addressof(buf) | 1, 512, None)
+    assert rc == 3

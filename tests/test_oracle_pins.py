@@ -250,6 +250,20 @@ def test_mass_selection_finds_needles_08b_workload():
     assert out["final_score"].min() >= 0.0
 
 
+def test_empty_prompt_changes_nothing_else():
+    """An empty prompt owns no chunks and keeps nothing; removing it leaves
+    every other prompt's results unchanged."""
+    q, k, off = random_case(14, [90, 0, 40], 2, 4, 2, 8, 2, q_gain=2.0)
+    out = oracle.run(q, k, off, chunk=8, mode="fixed", keep_p=0.3)
+    q2 = q[[0, 2]]
+    off2 = np.array([0, 90, 130])
+    ref = oracle.run(q2, k, off2, chunk=8, mode="fixed", keep_p=0.3)
+    for key in ("imp", "chunk_score", "chunk_keep", "kept_idx", "kept_pos"):
+        np.testing.assert_array_equal(out[key], ref[key], err_msg=key)
+    np.testing.assert_array_equal(out["kept_off"], [ref["kept_off"][0], ref["kept_off"][1],
+                                                    ref["kept_off"][1], ref["kept_off"][2]])
+
+
 def test_bf16_decode_exact():
     vals = np.array([0.0, 1.0, -2.5, 3.140625, 1e-3, 65280.0], dtype=np.float32)
     bits = bf16_bits_from_f32(vals)
