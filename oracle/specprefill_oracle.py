@@ -114,15 +114,17 @@ def token_importance(step_max: np.ndarray) -> np.ndarray:
 
 
 def avg_pool(imp: np.ndarray, width: int) -> np.ndarray:
-    """Centred moving average of odd ``width``; the divisor counts only the
-    window positions inside [0, n) (step 5)."""
+    """Centred moving average of odd ``width``: the mean of the window
+    positions inside [0, n) (step 5). Each window sum is exact (math.fsum),
+    so windows holding the same tokens give identical means."""
     n = imp.shape[0]
     half = width // 2
-    padded = np.concatenate([np.zeros(half), imp, np.zeros(half)])
-    sums = np.lib.stride_tricks.sliding_window_view(padded, width).sum(axis=1)
-    t = np.arange(n)
-    counts = np.minimum(t + half, n - 1) - np.maximum(t - half, 0) + 1
-    return sums / counts
+    vals = imp.tolist()
+    out = np.empty(n)
+    for t in range(n):
+        lo, hi = max(0, t - half), min(n, t + half + 1)
+        out[t] = math.fsum(vals[lo:hi]) / (hi - lo)
+    return out
 
 
 def min_max_normalize(x: np.ndarray) -> np.ndarray:

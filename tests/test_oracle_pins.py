@@ -114,6 +114,18 @@ def test_pool_properties():
     assert math.isclose(x[-1], v[-7:].mean(), rel_tol=1e-14)
 
 
+def test_pool_of_prompt_within_one_window_is_exactly_constant():
+    """When every window covers the whole prompt (n <= W//2 + 1) all pooled
+    values are the same mean, exactly; normalisation then gives all ones."""
+    rng = np.random.default_rng(5)
+    for n in range(1, 8):
+        v = rng.random(n) * 1e-3
+        x = oracle.avg_pool(v, 13)
+        assert np.all(x == x[0])
+        assert math.isclose(x[0], math.fsum(v) / n, rel_tol=1e-15)
+        np.testing.assert_array_equal(oracle.min_max_normalize(x), np.ones(n))
+
+
 def test_normalize_closed_form():
     np.testing.assert_allclose(oracle.min_max_normalize(np.array([2.0, 4.0, 6.0, 3.0])),
                                [0.0, 0.5, 1.0, 0.25], rtol=0, atol=0)

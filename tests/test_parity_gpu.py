@@ -80,6 +80,10 @@ def _run(cuda_lib, q_np, k_np, off_np, kw):
     return gh.out_to_numpy(out), (q, k, off)
 
 
+BASE = dict(pool_w=13, chunk=32, mode="mass", keep_p=0.3, mass=0.85, normalize=True,
+            boost_first_mult=1.5, boost_first_n=64, boost_last_mult=1.3, boost_last_n=128,
+            force_bos=True, force_last_chunk=True)
+
 SMALL = [
     # lengths, Ly, Hq, Hk, d, L, params
     ([512], 1, 4, 2, 64, 2, dict(mode="fixed", keep_p=0.3, normalize=False,
@@ -97,8 +101,7 @@ SMALL = [
 def test_small_cases_match_oracle(cuda_lib, case):
     lengths, ly, hq, hk, d, steps, kw = SMALL[case]
     q, k, off = random_case(500 + case, lengths, ly, hq, hk, d, steps, q_gain=2.0)
-    full = dict(pool_w=13, chunk=32, normalize=True, boost_first_mult=1.5, boost_first_n=64,
-                boost_last_mult=1.3, boost_last_n=128, force_bos=True, force_last_chunk=True)
+    full = dict(BASE)
     full.update(kw)
     got, _ = _run(cuda_lib, q, k, off, full)
     ref = oracle.run(q, k, off, **full)
@@ -198,8 +201,7 @@ def test_two_runs_are_bitwise_identical(cuda_lib):
 ])
 def test_selection_extremes(cuda_lib, kw):
     q, k, off = random_case(900, [777, 64, 3], 2, 4, 2, 64, 2, q_gain=2.0)
-    full = dict(pool_w=13, chunk=32, normalize=True, boost_first_mult=1.5, boost_first_n=64,
-                boost_last_mult=1.3, boost_last_n=128, force_bos=True, force_last_chunk=True)
+    full = dict(BASE)
     full.update(kw)
     got, _ = _run(cuda_lib, q, k, off, full)
     ref = oracle.run(q, k, off, **full)
@@ -211,9 +213,7 @@ def test_selection_extremes(cuda_lib, kw):
 
 def test_ragged_batch_with_empty_and_tiny_prompts(cuda_lib):
     q, k, off = random_case(901, [300, 0, 1, 12, 0, 200], 2, 4, 2, 128, 3, q_gain=2.0)
-    kw = dict(pool_w=13, chunk=32, mode="fixed", keep_p=0.3, normalize=True,
-              boost_first_mult=1.5, boost_first_n=64, boost_last_mult=1.3, boost_last_n=128,
-              force_bos=True, force_last_chunk=True)
+    kw = dict(BASE, mode="fixed", keep_p=0.3)
     got, _ = _run(cuda_lib, q, k, off, kw)
     ref = oracle.run(q, k, off, **kw)
     _check_scores(got, ref)
