@@ -72,6 +72,53 @@ def kernel_sha1():
         return hashlib.sha1(f.read()).hexdigest()
 
 
+class RawEvents:
+    """CUDA events created through the process's CUDA runtime, so that the
+    library can record them on its launch stream and we can read the elapsed
+    time (torch's Event only times events that torch itself recorded)."""
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.rt = None
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                self.rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if self.rt is None:
+            raise RuntimeError("CUDA runtime library not found")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+        self.made = []
+
+    def pair(self):
+        a, b = self.ct.c_void_p(), self.ct.c_void_p()
+        assert self.rt.cudaEventCreate(self.ct.byref(a)) == 0
+        assert self.rt.cudaEventCreate(self.ct.byref(b)) == 0
+        self.made += [a, b]
+        return _Ev(a.value), _Ev(b.value)
+
+    def elapsed_ms(self, a, b):
+        ms = self.ct.c_float()
+        rc = self.rt.cudaEventElapsedTime(self.ct.byref(ms), a.cuda_event, b.cuda_event)
+        assert rc == 0, f"cudaEventElapsedTime failed ({rc})"
+        return float(ms.value)
+
+    def close(self):
+        for e in self.made:
+            self.rt.cudaEventDestroy(e)
+        self.made = []
+
+
+class _Ev:
+    def __init__(self, handle):
+        self.cuda_event = handle
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -217,8 +264,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     assert sp.device_status(ws) == 0
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    raw = RawEvents()
+    evs = [raw.pair() for _ in range(args.steps)]
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -232,7 +279,8 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_stop)
-    logits_ms = [a.elapsed_time(b) for a, b in evs]
+    logits_ms = [raw.elapsed_ms(a, b) for a, b in evs]
+    raw.close()
     status = sp.device_status(ws)
     n_kept = int(out.n_kept.item())
 
