@@ -150,6 +150,32 @@ int sp_pool_chunk(const sp_shape* shape, const sp_params* params, const int32_t*
                   const float* imp, float* tok_score, float* chunk_score, int32_t* chunk_off,
                   void* ws, size_t ws_bytes, sp_stream_t stream);
 
+/* Allocation-free variant of sp_pool_chunk (the pages have no counterpart;
+ * this entry point exists for callers that cannot allocate device memory:
+ * code running under a memory pool that owns all device memory and forbids
+ * allocations after start-up, plugins whose host runtime gives them no
+ * allocator, or loops that must not risk the device synchronisation a
+ * cudaMalloc/cudaFree can cause). Same results as sp_pool_chunk, without a
+ * workspace: its scratch lives in a fixed 1 MiB array inside the library on
+ * every GPU that loads it, kept until the process exits. It calls no
+ * allocation routine.
+ * - tok_score, chunk_score (sp_max_chunks floats) and chunk_off (B+1) are
+ *   required device outputs.
+ * - status_out (device, one int32, nullable) receives this call's device
+ *   status in stream order: SP_OK, or SP_ERR_DEVICE when seq_off is invalid.
+ * - Batches whose scratch does not fit return SP_ERR_UNSUPPORTED. The
+ *   scratch is about 12*(B+1) bytes of offsets plus 8 bytes per 1024-token
+ *   block (chunk 32), i.e. up to roughly 4096 prompts of 16M tokens total.
+ * - The first call on each GPU looks up the array's device address once;
+ *   make that first call before any stream capture.
+ * - All calls on one GPU share the array and each leaves its contents
+ *   behind: calls that overlap on the GPU (unordered streams or threads)
+ *   race, so order them on one stream. */
+int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* params,
+                          const int32_t* seq_off, const float* imp, float* tok_score,
+                          float* chunk_score, int32_t* chunk_off, int32_t* status_out,
+                          sp_stream_t stream);
+
 /* Chunk selection per prompt. chunk_keep (device, one byte per chunk):
  * bit 0 = chosen by the ranking, bit 1 = forced final chunk. */
 int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,

@@ -28,6 +28,7 @@ __all__ = [
     "attn_importance",
     "attn_importance_simt",
     "pool_chunk",
+    "pool_chunk_noalloc",
     "select",
     "gather_kept",
     "specprefill_score",
@@ -125,6 +126,7 @@ def load(path: Optional[str] = None):
         "sp_attn_importance": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
         "sp_attn_importance_simt": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
         "sp_pool_chunk": [sp, pp, _P, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_pool_chunk_noalloc": [sp, pp, _P, _P, _P, _P, _P, _P, _P],
         "sp_select": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
         "sp_gather_kept": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
         "sp_specprefill_score": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -255,6 +257,18 @@ def pool_chunk(imp, seq_off, params: SelectionParams, tok_score=None, ws=None, s
                                chunk_off.data_ptr(), *_ws_args(ws), _stream(stream)),
            "sp_pool_chunk")
     return tok_score, chunk_score, chunk_off
+
+
+def pool_chunk_noalloc(imp, seq_off, params: SelectionParams, tok_score, chunk_score, chunk_off,
+                       status=None, stream=None):
+    """sp_pool_chunk without a workspace (fixed scratch inside the library);
+    all outputs are caller-provided. For callers that cannot allocate device
+    memory at call time."""
+    shape = token_shape(seq_off.numel() - 1, imp.numel())
+    _check(lib().sp_pool_chunk_noalloc(ctypes.byref(shape), ctypes.byref(params._c()),
+                                       seq_off.data_ptr(), imp.data_ptr(), tok_score.data_ptr(),
+                                       chunk_score.data_ptr(), chunk_off.data_ptr(), _ptr(status),
+                                       _stream(stream)), "sp_pool_chunk_noalloc")
 
 
 def select(chunk_score, chunk_off, seq_off, n_tokens_total: int, params: SelectionParams,
