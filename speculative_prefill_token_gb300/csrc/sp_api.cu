@@ -89,7 +89,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.d = s->head_dim;
     P.L = s->n_lookahead;
     P.R = P.L * P.G;
-    P.Rs = (P.R + 3) & ~3;
+    P.Rs = P.R <= 32 ? 32 : 64;
     P.Nmma = P.R <= 16 ? 16 : ((P.R + 15) & ~15);
     P.Nacc = P.Nmma <= 32 ? 32 : 64;
     P.Ntot = s->n_tokens_total;
@@ -104,12 +104,15 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     if (maxnc > kMaxPromptChunks) maxnc = kMaxPromptChunks;
     P.sort_cap = 1;
     while (P.sort_cap < maxnc) P.sort_cap <<= 1;
-    const int64_t per_slab = P.Ntot * P.Rs * static_cast<int64_t>(sizeof(float));
+    const int64_t per_slab = (P.tiles_max * kTileTokens) * P.Rs * static_cast<int64_t>(sizeof(float));
     int64_t spw = kWaveScratchBytes / per_slab;
     if (spw < 1) spw = 1;
     if (spw > P.slabs) spw = P.slabs;
+    if (spw > 64) spw = 64;
     P.slabs_per_wave = static_cast<int>(spw);
     P.waves = (P.slabs + P.slabs_per_wave - 1) / P.slabs_per_wave;
+    // the CUDA-core cross-check runs one item per CTA: up to tiles_max * slabs CTAs
+    P.rec_slots = (P.tiles_max * P.slabs_per_wave + static_cast<int64_t>(P.slabs_per_wave) * P.B) * 2;
     const double scale = p->scale > 0.0f ? static_cast<double>(p->scale)
                                           : static_cast<double>(1.0f / std::sqrt(static_cast<float>(P.d)));
     P.scale2 = static_cast<float>(scale * 1.4426950408889634);
@@ -125,8 +128,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_tile_base = take(B1 * 4);
     P.o_chunk_off = take(B1 * 4);
     P.o_pblk_base = take(B1 * 4);
-    P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.Ntot * P.Rs * 4);
-    P.o_part = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * P.Rs * 8);
+    P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 4);
+    P.o_part = take(static_cast<size_t>(P.rec_slots) * P.Rs * 8);
     P.o_lse = take(static_cast<size_t>(P.slabs_per_wave) * P.B * P.Rs * 4);
     P.o_alog = take(P.waves > 1 ? static_cast<size_t>(P.L) * P.Ntot * 4 : 0);
     P.o_imp = take(static_cast<size_t>(P.Ntot) * 4);
@@ -153,13 +156,19 @@ int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, 
     for (int w = 0; w < pl.waves; ++w) {
         const int slab0 = w * pl.slabs_per_wave;
         const int ns = pl.slabs - slab0 < pl.slabs_per_wave ? pl.slabs - slab0 : pl.slabs_per_wave;
-        cudaError_t e = simt ? launch_logits_simt(pl, s, seq_off, q, k, ws, slab0, ns, st)
-                             : launch_logits_tc(pl, s, seq_off, q, k, ws, slab0, ns, st);
+        int grid = 0;
+        cudaError_t e;
+        if (simt) {
+            e = launch_logits_simt(pl, s, seq_off, q, k, ws, slab0, ns, &grid, st);
+        } else {
+            grid = logits_tc_grid(pl, ns);
+            e = launch_logits_tc(pl, s, seq_off, q, k, ws, slab0, ns, grid, st);
+        }
         if (e != cudaSuccess) return SP_ERR_CUDA;
         if (w == pl.waves - 1 && prof && prof->logits_stop)
             if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_stop), st) != cudaSuccess)
                 return SP_ERR_CUDA;
-        if ((e = launch_lse(pl, ws, ns, st)) != cudaSuccess) return SP_ERR_CUDA;
+        if ((e = launch_lse(pl, ws, ns, grid, st)) != cudaSuccess) return SP_ERR_CUDA;
         if ((e = launch_reduce(pl, seq_off, ws, ns, w, imp, st)) != cudaSuccess) return SP_ERR_CUDA;
     }
     return SP_OK;

@@ -30,10 +30,11 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct Plan {
     // shape
-    int B, Ly, Hq, Hk, G, d, L, R, Rs, Nmma, Nacc;
+    int B, Ly, Hq, Hk, G, d, L, R, Rs, Nmma, Nacc;  // Rs = 32 or 64 (row stride of the scratch)
     int64_t Ntot;
     int slabs;
     int64_t tiles_max;    // >= sum_b ceil(n_b / 128)
+    int64_t rec_slots;    // softmax records: (max CTAs + segments per wave) * 2 warpgroups
     int64_t chunks_max;   // >= sum_b ceil(n_b / C)
     int C, W;
     int64_t Tb;           // tokens per post-processing block (multiple of C)
@@ -55,13 +56,17 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
                         cudaStream_t st);
 
-// Logits of the slabs [slab0, slab0 + nslab) into the workspace scratch,
-// plus per-tile softmax partials. Tensor-core (tcgen05 + TMA) kernel.
+// Logits of the slabs [slab0, slab0 + nslab) into the workspace scratch
+// (one 128-row slot per tile), plus softmax records per (CTA, segment,
+// warpgroup). Tensor-core (tcgen05 + TMA) kernel on `grid` CTAs.
+int logits_tc_grid(const Plan& pl, int nslab);
 cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                              const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                             cudaStream_t st);
+                             int grid, cudaStream_t st);
 
-cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, cudaStream_t st);
+// Softmax normalisers of every (slab, prompt) from the records written by a
+// logits launch of `grid` CTAs.
+cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, int grid, cudaStream_t st);
 
 // Softmax, max over heads/layers of the wave; the last wave writes imp.
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
@@ -73,9 +78,11 @@ cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_o
 cudaError_t launch_chunk(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                          const float* tok, float* chunk_score, void* ws, cudaStream_t st);
 
+// CUDA-core cross-check of the logits kernel, same outputs; returns its
+// grid (one work item per CTA) through *grid.
 cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                                const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                               cudaStream_t st);
+                               int* grid, cudaStream_t st);
 
 cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
                               const int32_t* chunk_off_check, cudaStream_t st);

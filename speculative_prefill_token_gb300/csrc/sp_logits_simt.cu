@@ -20,11 +20,11 @@ struct SimtArgs {
     const int32_t* tile_base;
     const uint16_t* q;
     const uint16_t* k;
-    float* logits;
-    float2* part;
+    float* logits;   // [nslab][tiles_max * 128][Rs], raw dot products
+    float2* rec;     // softmax records [(cta + segment) * 2 + warpgroup][Rs]
     const int32_t* bad;
-    int B, Hk, G, L, R, Rs, d, slab0;
-    int64_t Ntot, tiles_max;
+    int B, Hk, G, L, R, Rs, d, slab0, nslab;
+    int64_t rows_per_slab;
     int64_t ks_layer, ks_token, ks_head, qs_seq, qs_layer, qs_step, qs_head;
     float scale2;
 };
@@ -33,20 +33,26 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-template <int RMAX>
+// One work item (tile of one slab) per CTA; CTAs past the last item exit.
+template <int NH>
 __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
     if (*a.bad) return;
-    const int64_t tile = blockIdx.x;
-    if (tile >= a.tile_base[a.B]) return;
+    constexpr int RMAX = 32 * NH;
+    const int64_t T = a.tile_base[a.B];
+    const int64_t W = T * a.nslab;
+    const int64_t w0 = split_start(W, gridDim.x, blockIdx.x);
+    const int64_t w1 = split_start(W, gridDim.x, blockIdx.x + 1);
+    if (w0 >= w1) return;
     extern __shared__ float qs[];  // [RMAX][d]
-    __shared__ float2 stats[4][RMAX];
+    __shared__ float2 stats[4 * 64];
+    const int slab_local = static_cast<int>(w0 / T);
+    const int64_t tile = w0 - static_cast<int64_t>(slab_local) * T;
     const int b = search_base(a.tile_base, a.B, tile);
     const int64_t i = tile - a.tile_base[b];
     const int64_t start = a.seq_off[b];
     const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
     const int64_t tok0 = start + i * kTileTokens;
     const int nvalid = static_cast<int>(min64(kTileTokens, n - i * kTileTokens));
-    const int slab_local = blockIdx.y;
     const int slab = a.slab0 + slab_local;
     const int layer = slab / a.Hk, g = slab - layer * a.Hk;
 
@@ -63,9 +69,11 @@ __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
 
     const int t = threadIdx.x;
     const bool valid = t < nvalid;
-    float acc[RMAX];
+    float v[NH][32];
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc[r] = 0.0f;
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[h][r] = 0.0f;
     if (valid) {
         const uint16_t* krow = a.k + layer * a.ks_layer + (tok0 + t) * a.ks_token + g * a.ks_head;
         for (int x0 = 0; x0 < a.d; x0 += 8) {
@@ -78,51 +86,42 @@ __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
                 kf[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
             }
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                const float* qr = qs + r * a.d + x0;
+            for (int h = 0; h < NH; ++h)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[r] = fmaf(kf[e], qr[e], acc[r]);
-            }
+                for (int r = 0; r < 32; ++r) {
+                    const float* qr = qs + (h * 32 + r) * a.d + x0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[h][r] = fmaf(kf[e], qr[e], v[h][r]);
+                }
         }
-    }
-    float v[RMAX > 32 ? 2 : 1][32];
+        float* dst = a.logits + (static_cast<int64_t>(slab_local) * a.rows_per_slab +
+                                 tile * kTileTokens + t) * a.Rs;
 #pragma unroll
-    for (int r = 0; r < (RMAX > 32 ? 64 : 32); ++r) {
-        float x = (r < RMAX) ? acc[r < RMAX ? r : 0] : 0.0f;
-        v[r >> 5][r & 31] = valid ? x * a.scale2 : -INFINITY;
-    }
-    if (valid) {
-        float* dst = a.logits + (static_cast<int64_t>(slab_local) * a.Ntot + tok0 + t) * a.Rs;
-        for (int r = 0; r < a.Rs; ++r) dst[r] = v[r >> 5][r & 31];
-    }
-    const int warp = t >> 5, lane = t & 31;
+        for (int h = 0; h < NH; ++h)
 #pragma unroll
-    for (int hh = 0; hh < (RMAX > 32 ? 2 : 1); ++hh) {
-        const float2 pr = warp_row_partials(v[hh]);
-        if (hh * 32 + lane < RMAX) stats[warp][hh * 32 + lane] = pr;
+            for (int r = 0; r < 32; ++r) dst[h * 32 + r] = v[h][r];
     }
-    __syncthreads();
-    if (t < a.R) {
-        float2 acc2 = stats[0][t];
-        acc2 = merge_partial(acc2, stats[1][t]);
-        acc2 = merge_partial(acc2, stats[2][t]);
-        acc2 = merge_partial(acc2, stats[3][t]);
-        a.part[(static_cast<int64_t>(slab_local) * a.tiles_max + tile) * a.Rs + t] = acc2;
-    }
+    RowStats<NH> rs;
+    stats_reset(rs);
+    if (valid) stats_add<NH>(rs, v, a.scale2);
+    const int64_t seg = static_cast<int64_t>(slab_local) * a.B + b;
+    float2* out = a.rec + ((blockIdx.x + seg) * 2) * a.Rs;
+    stats_flush<NH>(rs, stats, t >> 5, 1, out, a.R);
+    if (t < a.R) out[a.Rs + t] = make_float2(-INFINITY, 0.0f);  // no second warpgroup here
 }
 
 }  // namespace
 
 cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                                const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                               cudaStream_t st) {
+                               int* grid_out, cudaStream_t st) {
     SimtArgs a;
     a.seq_off = seq_off;
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
     a.q = q;
     a.k = k;
     a.logits = ws_ptr<float>(ws, pl.o_logits);
-    a.part = ws_ptr<float2>(ws, pl.o_part);
+    a.rec = ws_ptr<float2>(ws, pl.o_part);
     a.bad = &ws_ptr<WsHeader>(ws, 0)->bad_input;
     a.B = pl.B;
     a.Hk = pl.Hk;
@@ -132,8 +131,8 @@ cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t*
     a.Rs = pl.Rs;
     a.d = pl.d;
     a.slab0 = slab0;
-    a.Ntot = pl.Ntot;
-    a.tiles_max = pl.tiles_max;
+    a.nslab = nslab;
+    a.rows_per_slab = pl.tiles_max * kTileTokens;
     a.ks_layer = s->k_stride_layer;
     a.ks_token = s->k_stride_token;
     a.ks_head = s->k_stride_head;
@@ -142,17 +141,15 @@ cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t*
     a.qs_step = s->q_stride_step;
     a.qs_head = s->q_stride_head;
     a.scale2 = pl.scale2;
-    dim3 grid(static_cast<unsigned>(pl.tiles_max), static_cast<unsigned>(nslab));
-    if (pl.R <= 8) {
-        logits_simt_kernel<8><<<grid, 128, 8 * pl.d * sizeof(float), st>>>(a);
-    } else if (pl.R <= 32) {
-        logits_simt_kernel<32><<<grid, 128, 32 * pl.d * sizeof(float), st>>>(a);
-    } else {
-        const size_t sm = 64 * pl.d * sizeof(float);
-        cudaFuncSetAttribute(logits_simt_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sm));
-        logits_simt_kernel<64><<<grid, 128, sm, st>>>(a);
-    }
+    const int grid = static_cast<int>(pl.tiles_max * nslab);
+    *grid_out = grid;
+    const int nh = pl.Rs > 32 ? 2 : 1;
+    const size_t sm = static_cast<size_t>(32 * nh) * pl.d * sizeof(float);
+    auto kern = nh == 2 ? logits_simt_kernel<2> : logits_simt_kernel<1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 128, sm, st>>>(a);
     return cudaGetLastError();
 }
 

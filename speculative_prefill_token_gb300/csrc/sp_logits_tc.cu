@@ -2,7 +2,7 @@
 // cores (sm_103a).
 //
 // For one (layer l, KV head g) "slab" and one prompt, the logits are
-//   s[t, r] = scale * <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>
+//   s[t, r] = <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>   (unscaled)
 // for the prompt's tokens t and the R = L*G query rows r = step*G + head
 // sharing KV head g ("SpecPrefill — Implementation Guide", §How It Works /
 // Attention Capture and Token Importance: one post-softmax row per head and
@@ -18,13 +18,14 @@
 //               (slab, prompt) into one of two buffers;
 //   warp 9      tcgen05.mma issuer (one thread) and TMEM owner;
 //   warps 0-7   two epilogue warpgroups; warpgroup e drains TMEM accumulator
-//               e (tiles alternate), scales to log2 units, stores the logits
-//               row of each token to the scratch and reduces per-tile
-//               softmax partials (row max, sum of exp2) for the later
-//               normaliser.
+//               e (tiles alternate), stages the tile's logits in swizzled
+//               shared memory for one TMA store into the scratch (one
+//               128-token slot per tile), and keeps per-thread running
+//               softmax statistics (row max reference, sum of exp2) that it
+//               reduces across threads once per (slab, prompt) segment.
 // Every mbarrier wait is bounded; a wait that gives up records
 // SP_ERR_TIMEOUT in the workspace status word, and the CTA then drains its
-// own copies and MMAs in flight, frees TMEM and returns.
+// own copies, stores and MMAs in flight, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -32,8 +33,8 @@
 #include <cstdint>
 #include <cstring>
 
-#include "sp_internal.h"
 #include "sp_device.cuh"
+#include "sp_internal.h"
 #include "sp_ptx.cuh"
 
 namespace sp {
@@ -43,6 +44,7 @@ constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
+constexpr int kStageOutBytes = kTileTokens * 128;  // 128 tokens x 32 fp32
 constexpr int kMaxStages = 16;
 constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
 constexpr int64_t kDrainSpin = int64_t(1) << 22;
@@ -50,22 +52,21 @@ constexpr int64_t kDrainSpin = int64_t(1) << 22;
 struct TcArgs {
     const int32_t* seq_off;
     const int32_t* tile_base;
-    float* logits;   // [nslab][Ntot][Rs]
-    float2* part;    // [nslab][tiles_max][Rs]
+    float2* rec;     // per (CTA, segment, warpgroup) softmax records [.. * 2 + wg][Rs]
     int32_t* status;
     const int32_t* bad;
     int B, Hk, G, R, Rs, d_blocks, Nmma, Nacc, slab0, nslab, stages;
-    int64_t Ntot, tiles_max;
     uint32_t q_block_bytes;  // Nmma * 128
     float scale2;
     int64_t spin;
 };
 
 struct SmemLayout {
-    uint32_t k_ring, q_buf, bars, tmem_slot, abort_flag, stats, total;
+    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, stats, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes) {
+__host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes,
+                                                  int nh) {
     SmemLayout s;
     uint32_t off = 0;
     s.k_ring = off;
@@ -73,6 +74,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
     s.q_buf = off;
     off += 2u * static_cast<uint32_t>(d_blocks) * q_block_bytes;
     off = (off + 1023u) & ~1023u;
+    s.out_buf = off;                                   // [warpgroup][half] 16 KB, swizzled
+    off += 2u * static_cast<uint32_t>(nh) * kStageOutBytes;
     s.bars = off;
     off += 8u * (2 * kMaxStages + 9);
     s.tmem_slot = off;
@@ -80,15 +83,15 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
     s.abort_flag = off;
     off += 8;
     s.stats = off;
-    off += 2u * 4u * kMaxRows * 8u;  // [warpgroup][warp][row] float2
+    off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
     s.total = off;
     return s;
 }
 
 struct Item {
-    int slab;   // local slab index in [0, nslab)
-    int b;      // prompt
-    int64_t tile;  // flattened tile index (for partials)
+    int slab;      // local slab index in [0, nslab)
+    int b;         // prompt
+    int64_t tile;  // flattened tile index of the slab (scratch slot)
     int64_t tok0;  // first global token of the tile
     int nvalid;    // tokens of the tile inside the prompt
 };
@@ -97,15 +100,10 @@ __device__ __forceinline__ Item decode(const TcArgs& a, int64_t w, int64_t T) {
     Item it;
     it.slab = static_cast<int>(w / T);
     it.tile = w - static_cast<int64_t>(it.slab) * T;
-    int lo = 0, hi = a.B - 1;  // largest b with tile_base[b] <= tile
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (a.tile_base[mid] <= it.tile) lo = mid; else hi = mid - 1;
-    }
-    it.b = lo;
-    const int64_t i = it.tile - a.tile_base[lo];
-    const int64_t start = a.seq_off[lo];
-    const int64_t n = static_cast<int64_t>(a.seq_off[lo + 1]) - start;
+    it.b = search_base(a.tile_base, a.B, it.tile);
+    const int64_t i = it.tile - a.tile_base[it.b];
+    const int64_t start = a.seq_off[it.b];
+    const int64_t n = static_cast<int64_t>(a.seq_off[it.b + 1]) - start;
     it.tok0 = start + i * kTileTokens;
     const int64_t rem = n - i * kTileTokens;
     it.nvalid = static_cast<int>(rem < kTileTokens ? rem : kTileTokens);
@@ -117,14 +115,16 @@ __device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* ab
     atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_TIMEOUT));
 }
 
+template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_q, const TcArgs a) {
+                     const __grid_constant__ CUtensorMap tmap_q,
+                     const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
     if (*a.bad) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    const SmemLayout L = smem_layout(a.stages, a.d_blocks, a.q_block_bytes);
+    const SmemLayout L = smem_layout(a.stages, a.d_blocks, a.q_block_bytes, NH);
     const uint32_t base = smem_u32(smem);
     const uint32_t k_ring = base + L.k_ring;
     const uint32_t q_buf = base + L.q_buf;
@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_s);
     }
     tc_fence_before();
     __syncthreads();
@@ -180,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int64_t T = a.tile_base[a.B];
     const int64_t W = T * a.nslab;
-    const int64_t w_begin = (W * blockIdx.x) / gridDim.x;
-    const int64_t w_end = (W * (blockIdx.x + 1)) / gridDim.x;
+    const int64_t C = gridDim.x;
+    const int64_t w_begin = split_start(W, C, blockIdx.x);
+    const int64_t w_end = split_start(W, C, blockIdx.x + 1);
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -307,72 +309,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue warpgroups
         const int e = warp >> 2;          // warpgroup: owns accumulator e
         const int qw = warp & 3;          // TMEM lane quarter
+        const int bar_id = 1 + e;
         const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+        uint8_t* out_buf = smem + L.out_buf + e * NH * kStageOutBytes;
+        const uint32_t out_addr = smem_u32(out_buf);
+        float2* st_sm = stats + e * 4 * 64;
+        const int tl = qw * 32 + lane;   // token row of the tile
+        RowStats<NH> rs;
+        stats_reset(rs);
+        int64_t cur_key = -1;
+        bool stores = false;
+        bool ok = true;
         int64_t j = 0;
         for (int64_t w = w_begin; w < w_end; ++w, ++j) {
-            if (static_cast<int>(j & 1) != e) continue;
             const Item it = decode(a, w, T);
+            const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+            if (key != cur_key) {
+                if (cur_key >= 0)
+                    stats_flush<NH>(rs, st_sm, qw, bar_id,
+                                    a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs, a.R);
+                cur_key = key;
+            }
+            if (static_cast<int>(j & 1) != e) continue;
             // all 128 threads of the warpgroup take the same decision, so the
             // named barriers below never wait for a thread that left
             const bool got = mbar_wait_bounded(bar_tfull + 8 * e, static_cast<uint32_t>((j >> 1) & 1),
                                                a.spin, abort_flag);
-            if (!bar_sync_and(1 + e, 128, got)) {
+            if (!bar_sync_and(bar_id, 128, got)) {
                 record_timeout(a, abort_flag);
+                ok = false;
                 break;
             }
             tc_fence_after();
-            float v[2][32];
+            float v[NH][32];
             const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(e * a.Nacc);
             tmem_ld_32x32b_x32(taddr, v[0]);
-            if (a.Nmma > 32) tmem_ld_32x32b_x32(taddr + 32, v[1]);
+            if (NH > 1) tmem_ld_32x32b_x32(taddr + 32, v[NH - 1]);
             tmem_ld_wait();
-#pragma unroll
-            for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
-                if (r >= a.Nmma) v[0][r] = 0.0f;
             tc_fence_before();
             mbar_arrive(bar_tempty + 8 * e);
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+                for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
+                    if (hh * 32 + r >= a.Nmma) v[hh][r] = 0.0f;
 
-            const int tl = qw * 32 + lane;
-            const bool valid = tl < it.nvalid;
-            const int halves = a.R > 32 ? 2 : 1;
+            // stage the raw logits (128-byte swizzle) and store the tile with TMA
+            if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                if (hh < halves) {
+            for (int hh = 0; hh < NH; ++hh) {
+                uint8_t* row = out_buf + hh * kStageOutBytes + tl * 128;
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) v[hh][r] = valid ? v[hh][r] * a.scale2 : -INFINITY;
-                }
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(row + ((c ^ (tl & 7)) << 4)) =
+                        make_float4(v[hh][4 * c], v[hh][4 * c + 1], v[hh][4 * c + 2], v[hh][4 * c + 3]);
             }
-            if (valid) {
-                float* dst = a.logits + (static_cast<int64_t>(it.slab) * a.Ntot + it.tok0 + tl) * a.Rs;
-                const int n4 = a.Rs >> 2;
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+            if (qw == 0 && lane == 0) {
+                const int y = static_cast<int>(it.tile * kTileTokens);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    if (c < n4) {
-                        const float* src = &v[c >> 3][(c & 7) * 4];
-                        reinterpret_cast<float4*>(dst)[c] = make_float4(src[0], src[1], src[2], src[3]);
-                    }
-                }
+                for (int hh = 0; hh < NH; ++hh)
+                    tma_store_3d(&tmap_s, out_addr + hh * kStageOutBytes, hh * 32, y, it.slab);
+                bulk_commit();
+                stores = true;
             }
-            float2* st = stats + (e * 4) * kMaxRows;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                if (hh < halves) {
-                    const float2 pr = warp_row_partials(v[hh]);
-                    st[qw * kMaxRows + hh * 32 + lane] = pr;
-                }
-            }
-            asm volatile("bar.sync %0, 128;" ::"r"(1 + e) : "memory");
-            if (qw == 0) {
-                for (int r = lane; r < a.R; r += 32) {
-                    float2 acc2 = st[r];
-                    acc2 = merge_partial(acc2, st[kMaxRows + r]);
-                    acc2 = merge_partial(acc2, st[2 * kMaxRows + r]);
-                    acc2 = merge_partial(acc2, st[3 * kMaxRows + r]);
-                    a.part[(static_cast<int64_t>(it.slab) * a.tiles_max + it.tile) * a.Rs + r] = acc2;
-                }
-            }
-            asm volatile("bar.sync %0, 128;" ::"r"(1 + e) : "memory");
+            if (tl < it.nvalid) stats_add<NH>(rs, v, a.scale2);
         }
+        if (ok && cur_key >= 0)
+            stats_flush<NH>(rs, st_sm, qw, bar_id, a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs,
+                            a.R);
+        if (qw == 0 && lane == 0 && stores) bulk_wait0();
     }
 
     tc_fence_before();
@@ -403,13 +411,21 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+int logits_tc_grid(const Plan& pl, int nslab) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t work = pl.tiles_max * nslab;
+    return static_cast<int>(work < sms ? work : sms);
+}
+
 cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                              const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                             cudaStream_t st) {
+                             int grid, cudaStream_t st) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int d = pl.d;
-    CUtensorMap tk, tq;
+    CUtensorMap tk, tq, ts;
     {
         // K: dims (d, token, kv head, layer); unused strides get a harmless value
         const int64_t sh = pl.Hk > 1 ? s->k_stride_head : d;
@@ -443,11 +459,23 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    {
+        // logits scratch: dims (row value, tile slot row, slab); box = 32 values x 128 rows
+        const uint64_t rows = static_cast<uint64_t>(pl.tiles_max) * kTileTokens;
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(pl.Rs), rows, static_cast<cuuint64_t>(nslab)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(pl.Rs) * 4,
+                                 static_cast<cuuint64_t>(rows * pl.Rs * 4)};
+        cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTileTokens), 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws_ptr<float>(ws, pl.o_logits), dims,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     TcArgs a;
     a.seq_off = seq_off;
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
-    a.logits = ws_ptr<float>(ws, pl.o_logits);
-    a.part = ws_ptr<float2>(ws, pl.o_part);
+    a.rec = ws_ptr<float2>(ws, pl.o_part);
     a.status = &ws_ptr<WsHeader>(ws, 0)->status;
     a.bad = &ws_ptr<WsHeader>(ws, 0)->bad_input;
     a.B = pl.B;
@@ -460,29 +488,22 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
     a.Nacc = pl.Nacc;
     a.slab0 = slab0;
     a.nslab = nslab;
-    a.Ntot = pl.Ntot;
-    a.tiles_max = pl.tiles_max;
     a.q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
     a.scale2 = pl.scale2;
     a.spin = pl.spin;
 
-    const uint32_t q_bytes = 2u * a.d_blocks * a.q_block_bytes;
-    const uint32_t fixed = smem_layout(0, a.d_blocks, a.q_block_bytes).total + 1024;
-    int stages = static_cast<int>((kSmemLimit - fixed) / kKBlockBytes);
+    const int nh = pl.Rs > 32 ? 2 : 1;
+    const uint32_t fixed = smem_layout(0, a.d_blocks, a.q_block_bytes, nh).total + 1024;
+    int stages = static_cast<int>((kSmemLimit - static_cast<int>(fixed)) / kKBlockBytes);
     if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2 || q_bytes > kSmemLimit) return cudaErrorInvalidConfiguration;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
     a.stages = stages;
-    const uint32_t smem = smem_layout(stages, a.d_blocks, a.q_block_bytes).total + 1024;
-
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t err = cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const uint32_t smem = smem_layout(stages, a.d_blocks, a.q_block_bytes, nh).total + 1024;
+    auto kern = nh == 2 ? logits_tc_kernel<2> : logits_tc_kernel<1>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const int64_t work = pl.tiles_max * nslab;
-    const int grid = static_cast<int>(work < sms ? work : sms);
-    logits_tc_kernel<<<grid, kThreads, smem, st>>>(tk, tq, a);
+    kern<<<grid, kThreads, smem, st>>>(tk, tq, ts, a);
     return cudaGetLastError();
 }
 

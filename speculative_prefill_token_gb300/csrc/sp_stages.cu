@@ -117,90 +117,101 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 }
 
 // ------------------------------------------------------------ normaliser
-// lse2[slab][b][r] = log2 sum_t exp2(s2[t, r]) over prompt b's keys, merged
-// from the per-tile partials (max, sum exp2(x - max)).
-__global__ void __launch_bounds__(256) lse_kernel(const float2* part, const int32_t* tile_base,
-                                                  float* lse2, int B, int R, int Rs,
-                                                  int64_t tiles_max, const int32_t* bad) {
+// lse2[slab][b][r] = log2 sum_t exp2(scale2 * s[t, r]) over prompt b's keys,
+// merged from the records the logits kernel wrote per (CTA, segment,
+// warpgroup): only the CTAs whose item range meets the segment are read.
+__global__ void __launch_bounds__(64) lse_kernel(const float2* rec, const int32_t* tile_base,
+                                                 float* lse2, int B, int R, int Rs, int64_t C,
+                                                 int nslab, const int32_t* bad) {
     if (*bad) return;
-    __shared__ float2 acc_s[8][kMaxRows];
-    const int slab = blockIdx.x, b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = tile_base[b], t1 = tile_base[b + 1];
-    for (int r = lane; r < kMaxRows; r += 32) {
-        float2 acc = make_float2(-INFINITY, 0.0f);
-        if (r < R)
-            for (int64_t t = t0 + warp; t < t1; t += 8)
-                acc = merge_partial(acc, part[(static_cast<int64_t>(slab) * tiles_max + t) * Rs + r]);
-        acc_s[warp][r] = acc;
-    }
-    __syncthreads();
+    const int seg = blockIdx.x;  // slab_local * B + b
+    const int slab = seg / B, b = seg - slab * B;
     const int r = threadIdx.x;
-    if (r < R) {
-        float2 acc = acc_s[0][r];
-        for (int w = 1; w < 8; ++w) acc = merge_partial(acc, acc_s[w][r]);
-        lse2[(static_cast<int64_t>(slab) * B + b) * Rs + r] = acc.y > 0.0f ? acc.x + log2f(acc.y) : INFINITY;
+    if (r >= R) return;
+    const int64_t T = tile_base[B];
+    const int64_t W = T * nslab;
+    const int64_t i0 = static_cast<int64_t>(slab) * T + tile_base[b];
+    const int64_t i1 = static_cast<int64_t>(slab) * T + tile_base[b + 1];
+    float out = INFINITY;
+    if (i1 > i0) {
+        const int64_t c0 = split_owner(W, C, i0), c1 = split_owner(W, C, i1 - 1);
+        float2 acc = make_float2(-INFINITY, 0.0f);
+        for (int64_t c = c0; c <= c1; ++c) {
+            acc = merge_partial(acc, rec[((c + seg) * 2 + 0) * Rs + r]);
+            acc = merge_partial(acc, rec[((c + seg) * 2 + 1) * Rs + r]);
+        }
+        out = acc.y > 0.0f ? acc.x + log2f(acc.y) : INFINITY;
     }
+    lse2[static_cast<int64_t>(seg) * Rs + r] = out;
 }
 
 // --------------------------------------------------------------- reduce
-// Token importance: for every token t of a tile and lookahead step l,
-// a_l = max over the wave's slabs and the G heads of (s2 - lse2) (log2 of
-// the softmax probability), combined with earlier waves by max; the last
-// wave writes imp[t] = (1/L) sum_l exp2(a_l).
-__global__ void __launch_bounds__(kTileTokens) reduce_kernel(const float* logits, const float* lse2,
-                                                             const int32_t* seq_off,
-                                                             const int32_t* tile_base, float* alog,
-                                                             float* imp, int B, int G, int L, int R,
-                                                             int Rs, int nslab, int64_t Ntot,
-                                                             int first_wave, int last_wave,
-                                                             const int32_t* bad) {
+// Token importance. One CTA covers TOK tokens of one tile; thread (token,
+// quad) reads the quad's four raw logits of every slab of the wave with one
+// coalesced 16-byte load each, and keeps the running max over slabs of
+// scale2 * s - lse2 (the log2 softmax probability). One thread per token
+// then takes the max over the G heads of each lookahead step, combines it
+// with earlier waves, and (last wave) writes
+// imp[t] = (1/L) sum_l exp2(max over layers, heads).
+constexpr int kReduceThreads = 256;
+
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
+    const float* logits, const float* lse2, const int32_t* seq_off, const int32_t* tile_base,
+    float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab, int64_t Ntot,
+    int64_t rows_per_slab, float scale2, int first_wave, int last_wave, const int32_t* bad) {
     if (*bad) return;
-    const int64_t tile = blockIdx.x;
+    const int Q4 = Rs / 4;
+    const int TOK = kReduceThreads / Q4;
+    const int subs = kTileTokens / TOK;
+    const int64_t tile = blockIdx.x / subs;
+    const int sub = blockIdx.x - static_cast<int>(tile) * subs;
     if (tile >= tile_base[B]) return;
     extern __shared__ float sm[];
-    float* rows = sm;                                // [128][Rs + 1]
-    float* lse_s = rows + kTileTokens * (Rs + 1);    // [nslab][Rs]
-    float* amax = lse_s + nslab * Rs;                // [L][128]
+    float* lse_s = sm;                  // [nslab][Rs]
+    float* ms = lse_s + nslab * Rs;     // [TOK][Rs + 1]
     const int b = search_base(tile_base, B, tile);
     const int64_t i = tile - tile_base[b];
     const int64_t start = seq_off[b];
     const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
-    const int64_t tok0 = start + i * kTileTokens;
-    const int nvalid = static_cast<int>(min64(kTileTokens, n - i * kTileTokens));
-    const int t = threadIdx.x;
-    for (int idx = t; idx < nslab * Rs; idx += kTileTokens) {
+    const int64_t first = i * kTileTokens + static_cast<int64_t>(sub) * TOK;  // within the prompt
+    const int nvalid = static_cast<int>(min64(TOK, n - first));
+    if (nvalid <= 0) return;
+    for (int idx = threadIdx.x; idx < nslab * Rs; idx += kReduceThreads) {
         const int s = idx / Rs, r = idx - s * Rs;
-        lse_s[idx] = r < R ? lse2[(static_cast<int64_t>(s) * B + b) * Rs + r] : 0.0f;
+        lse_s[idx] = lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
     }
-    for (int l = 0; l < L; ++l) amax[l * kTileTokens + t] = -INFINITY;
-    for (int s = 0; s < nslab; ++s) {
-        __syncthreads();
-        const float* src = logits + (static_cast<int64_t>(s) * Ntot + tok0) * Rs;
-        const int nflt = nvalid * Rs;
-        for (int idx = t; idx < nflt; idx += kTileTokens) {
-            const int tt = idx / Rs, r = idx - tt * Rs;
-            rows[tt * (Rs + 1) + r] = src[idx];
+    __syncthreads();
+    const int tq = threadIdx.x / Q4, c = threadIdx.x - tq * Q4;
+    if (tq < nvalid) {
+        const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+        for (int s = 0; s < nslab; ++s) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(
+                logits + (static_cast<int64_t>(s) * rows_per_slab + row) * Rs + 4 * c));
+            const float* ls = lse_s + s * Rs + 4 * c;
+            m0 = fmaxf(m0, fmaf(v.x, scale2, -ls[0]));
+            m1 = fmaxf(m1, fmaf(v.y, scale2, -ls[1]));
+            m2 = fmaxf(m2, fmaf(v.z, scale2, -ls[2]));
+            m3 = fmaxf(m3, fmaf(v.w, scale2, -ls[3]));
         }
-        __syncthreads();
-        if (t < nvalid) {
-            const float* row = rows + t * (Rs + 1);
-            const float* ls = lse_s + s * Rs;
-            for (int l = 0; l < L; ++l) {
-                float m = amax[l * kTileTokens + t];
-                for (int j = 0; j < G; ++j) m = fmaxf(m, row[l * G + j] - ls[l * G + j]);
-                amax[l * kTileTokens + t] = m;
-            }
-        }
+        float* mrow = ms + tq * (Rs + 1) + 4 * c;
+        mrow[0] = m0;
+        mrow[1] = m1;
+        mrow[2] = m2;
+        mrow[3] = m3;
     }
+    __syncthreads();
+    const int t = threadIdx.x;
     if (t < nvalid) {
-        const int64_t tok = tok0 + t;
+        const int64_t tok = start + first + t;
+        const float* mrow = ms + t * (Rs + 1);
         float total = 0.0f;
         for (int l = 0; l < L; ++l) {
-            float m = amax[l * kTileTokens + t];
-            if (!first_wave) m = fmaxf(m, alog[l * Ntot + tok]);
-            if (last_wave) total += exp2f(m);
-            else alog[l * Ntot + tok] = m;
+            float a = -INFINITY;
+            for (int j = 0; j < G; ++j) a = fmaxf(a, mrow[l * G + j]);
+            if (!first_wave) a = fmaxf(a, alog[l * Ntot + tok]);
+            if (last_wave) total += exp2f(a);
+            else alog[l * Ntot + tok] = a;
         }
         if (last_wave) imp[tok] = total / static_cast<float>(L);
     }
@@ -593,29 +604,24 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
     return cudaGetLastError();
 }
 
-cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, cudaStream_t st) {
-    dim3 grid(static_cast<unsigned>(nslab), static_cast<unsigned>(pl.B));
-    lse_kernel<<<grid, 256, 0, st>>>(ws_ptr<float2>(ws, pl.o_part), ws_ptr<int32_t>(ws, pl.o_tile_base),
-                                     ws_ptr<float>(ws, pl.o_lse), pl.B, pl.R, pl.Rs, pl.tiles_max,
-                                     &ws_ptr<WsHeader>(ws, 0)->bad_input);
+cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, int grid, cudaStream_t st) {
+    lse_kernel<<<static_cast<unsigned>(nslab * pl.B), 64, 0, st>>>(
+        ws_ptr<float2>(ws, pl.o_part), ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_lse),
+        pl.B, pl.R, pl.Rs, grid, nslab, &ws_ptr<WsHeader>(ws, 0)->bad_input);
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
                           float* imp, cudaStream_t st) {
-    const size_t smem = sizeof(float) * (static_cast<size_t>(kTileTokens) * (pl.Rs + 1) +
-                                         static_cast<size_t>(nslab) * pl.Rs +
-                                         static_cast<size_t>(pl.L) * kTileTokens);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    reduce_kernel<<<static_cast<unsigned>(pl.tiles_max), kTileTokens, smem, st>>>(
+    const int tok = kReduceThreads / (pl.Rs / 4);
+    const size_t smem = sizeof(float) * (static_cast<size_t>(nslab) * pl.Rs +
+                                         static_cast<size_t>(tok) * (pl.Rs + 1));
+    const unsigned grid = static_cast<unsigned>(pl.tiles_max * (kTileTokens / tok));
+    reduce_kernel<<<grid, kReduceThreads, smem, st>>>(
         ws_ptr<float>(ws, pl.o_logits), ws_ptr<float>(ws, pl.o_lse), seq_off,
         ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
-        pl.R, pl.Rs, nslab, pl.Ntot, wave == 0 ? 1 : 0, wave == pl.waves - 1 ? 1 : 0,
-        &ws_ptr<WsHeader>(ws, 0)->bad_input);
+        pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.scale2, wave == 0 ? 1 : 0,
+        wave == pl.waves - 1 ? 1 : 0, &ws_ptr<WsHeader>(ws, 0)->bad_input);
     return cudaGetLastError();
 }
 
