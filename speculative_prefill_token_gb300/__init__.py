@@ -207,13 +207,16 @@ def max_chunks(shape: _Shape, params: SelectionParams) -> int:
     return int(n.value)
 
 
-def make_workspace(shape: _Shape, params: SelectionParams, device=None):
-    """Allocate (torch) and initialise a workspace for this shape."""
+def make_workspace(shape: _Shape, params: SelectionParams, device=None, poison: bool = False):
+    """Allocate (torch) and initialise a workspace for this shape. With
+    ``poison`` every byte except the header starts as 0xFF (NaN as float)."""
     import torch
     nbytes = workspace_size(shape, params)
     ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
     off = (-ws.data_ptr()) % 256
     ws = ws[off:off + nbytes]
+    if poison:
+        ws.fill_(0xFF)
     _check(lib().sp_workspace_init(ws.data_ptr(), nbytes, _stream(None)), "sp_workspace_init")
     return ws
 

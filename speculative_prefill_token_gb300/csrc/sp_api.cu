@@ -128,6 +128,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_tile_base = take(B1 * 4);
     P.o_chunk_off = take(B1 * 4);
     P.o_pblk_base = take(B1 * 4);
+    P.o_segcnt = take(static_cast<size_t>(P.slabs_per_wave) * P.B * 4);
     P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 4);
     P.o_part = take(static_cast<size_t>(P.rec_slots) * P.Rs * 8);
     P.o_lse = take(static_cast<size_t>(P.slabs_per_wave) * P.B * P.Rs * 4);
@@ -168,7 +169,6 @@ int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, 
         if (w == pl.waves - 1 && prof && prof->logits_stop)
             if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_stop), st) != cudaSuccess)
                 return SP_ERR_CUDA;
-        if ((e = launch_lse(pl, ws, ns, grid, st)) != cudaSuccess) return SP_ERR_CUDA;
         if ((e = launch_reduce(pl, seq_off, ws, ns, w, imp, st)) != cudaSuccess) return SP_ERR_CUDA;
     }
     return SP_OK;
@@ -299,11 +299,10 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
     const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
     if ((rc = importance_waves(pl, shape, seq_off, q, k, imp_p, ws, st, false, prof)) != SP_OK) return rc;
-    if (launch_pool(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-    if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-    if (launch_select(pl, params, seq_off, coff, cs_p, keep_p, ws, true, kept_off, n_kept, st) !=
-        cudaSuccess)
+    if (launch_post(pl, params, seq_off, imp_p, tok_p, cs_p, keep_p, kept_idx, kept_pos, kept_off,
+                    n_kept, ws, st) != cudaSuccess)
         return SP_ERR_CUDA;
+    if (pl.B == 1) return SP_OK;  // the post kernel wrote the kept lists itself
     return to_status(launch_gather_write(pl, params, seq_off, coff, keep_p, kept_idx, kept_pos,
                                          kept_off, n_kept, ws, st));
 }

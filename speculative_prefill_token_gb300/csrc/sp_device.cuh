@@ -117,6 +117,7 @@ __device__ __forceinline__ void stats_flush(RowStats<NH>& st, float2* sm, int qw
             acc = merge_partial(acc, sm[192 + r]);
             out[r] = acc;
         }
+        __threadfence();
     }
     asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
     stats_reset(st);
@@ -126,13 +127,75 @@ __device__ __forceinline__ void stats_flush(RowStats<NH>& st, float2* sm, int qw
 // [floor(W*c/C), floor(W*(c+1)/C)). owner(w) = the CTA owning item w.
 __device__ __forceinline__ int64_t split_start(int64_t W, int64_t C, int64_t c) { return (W * c) / C; }
 
+// largest c with floor(W*c/C) <= w  <=>  W*c < (w+1)*C
 __device__ __forceinline__ int64_t split_owner(int64_t W, int64_t C, int64_t w) {
-    int64_t lo = 0, hi = C - 1;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi + 1) >> 1;
-        if (split_start(W, C, mid) <= w) lo = mid; else hi = mid - 1;
+    return ((w + 1) * C - 1) / W;
+}
+
+// Called by all 128 threads of a warpgroup right after it wrote (and
+// fenced) `contrib` softmax records of segment `seg`. The warpgroup whose
+// contribution completes the segment's count (2 records per CTA that owns
+// items of the segment) merges all of the segment's records into
+// lse2[seg][r] = max + log2(sum) and resets the counter. Nothing waits: the
+// last one to arrive does the work (threadfence + atomic counter).
+__device__ __forceinline__ void segment_done(const int32_t* tile_base, int B, int nslab, int64_t C,
+                                             int64_t seg, int contrib, const float2* rec,
+                                             unsigned* seg_cnt, float* lse2, int R, int Rs,
+                                             float2* sm, volatile int* flag, int qw, int bar_id) {
+    const int lane = threadIdx.x & 31;
+    const int slab = static_cast<int>(seg / B), b = static_cast<int>(seg - static_cast<int64_t>(slab) * B);
+    const int64_t T = tile_base[B];
+    const int64_t W = T * nslab;
+    const int64_t i0 = static_cast<int64_t>(slab) * T + tile_base[b];
+    const int64_t i1 = static_cast<int64_t>(slab) * T + tile_base[b + 1];
+    const int64_t c0 = split_owner(W, C, i0), c1 = split_owner(W, C, i1 - 1);
+    // CTAs in [c0, c1] that own at least one item: all of them when C <= W
+    // (every CTA then owns one or more items), otherwise one per item
+    const int64_t owners = C > W ? (i1 - i0) : (c1 - c0 + 1);
+    if (qw == 0 && lane == 0) {
+        const unsigned target = static_cast<unsigned>(2 * owners);
+        const unsigned prev = atomicAdd(seg_cnt + seg, static_cast<unsigned>(contrib));
+        const int last = (prev + contrib == target) ? 1 : 0;
+        if (last) seg_cnt[seg] = 0u;
+        *flag = last;
     }
-    return lo;
+    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+    const bool last = *flag != 0;
+    if (last) {
+        __threadfence();
+        // warp qw merges the records of CTAs c0 + qw, c0 + qw + 4, ... that own
+        // items; four CTAs' records are loaded before they are merged
+        for (int h = 0; h * 32 < R; ++h) {
+            const int r = h * 32 + lane;
+            float2 acc = make_float2(-INFINITY, 0.0f);
+            if (r < R) {
+                for (int64_t cb = c0 + qw; cb <= c1; cb += 16) {
+                    float2 v[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int64_t c = cb + 4 * u;
+                        const bool own = c <= c1 && (C <= W || split_start(W, C, c + 1) != split_start(W, C, c));
+                        v[2 * u] = own ? __ldcg(rec + ((c + seg) * 2 + 0) * Rs + r) : make_float2(-INFINITY, 0.0f);
+                        v[2 * u + 1] = own ? __ldcg(rec + ((c + seg) * 2 + 1) * Rs + r) : make_float2(-INFINITY, 0.0f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc = merge_partial(acc, v[u]);
+                }
+            }
+            sm[qw * 64 + r] = acc;
+        }
+    }
+    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+    if (last && qw == 0) {
+        for (int r = lane; r < R; r += 32) {
+            float2 acc = sm[r];
+            acc = merge_partial(acc, sm[64 + r]);
+            acc = merge_partial(acc, sm[128 + r]);
+            acc = merge_partial(acc, sm[192 + r]);
+            lse2[seg * Rs + r] = acc.y > 0.0f ? acc.x + log2f(acc.y) : INFINITY;
+        }
+    }
+    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
 }
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }

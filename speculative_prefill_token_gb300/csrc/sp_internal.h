@@ -44,7 +44,7 @@ struct Plan {
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
     // workspace offsets (bytes)
-    size_t o_tile_base, o_chunk_off, o_pblk_base, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
+    size_t o_tile_base, o_chunk_off, o_pblk_base, o_segcnt, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
         o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
 };
 
@@ -53,6 +53,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
 // ------------------------------------------------------------ launchers
 // Each returns cudaSuccess or the launch error.
 
+// Per-call offsets and checks; also zeroes the per-segment record counters.
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
                         cudaStream_t st);
 
@@ -64,9 +65,6 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
                              const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
                              int grid, cudaStream_t st);
 
-// Softmax normalisers of every (slab, prompt) from the records written by a
-// logits launch of `grid` CTAs.
-cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, int grid, cudaStream_t st);
 
 // Softmax, max over heads/layers of the wave; the last wave writes imp.
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
@@ -102,6 +100,14 @@ cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_
                                 const int32_t* chunk_off, const uint8_t* keep, int32_t* kept_idx,
                                 int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
                                 cudaStream_t st);
+
+// Fused per-prompt post-processing (pool, normalise, boost, chunk means,
+// selection, kept counts; kept lists too when the batch has one prompt),
+// one 8-CTA cluster per prompt.
+cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                        const float* imp, float* tok, float* chunk_score, uint8_t* keep,
+                        int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept,
+                        void* ws, cudaStream_t st);
 
 template <typename T>
 inline T* ws_ptr(void* ws, size_t off) {

@@ -22,6 +22,8 @@ struct SimtArgs {
     const uint16_t* k;
     float* logits;   // [nslab][tiles_max * 128][Rs], raw dot products
     float2* rec;     // softmax records [(cta + segment) * 2 + warpgroup][Rs]
+    unsigned* seg_cnt;
+    float* lse2;
     const int32_t* bad;
     int B, Hk, G, L, R, Rs, d, slab0, nslab;
     int64_t rows_per_slab;
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
     if (w0 >= w1) return;
     extern __shared__ float qs[];  // [RMAX][d]
     __shared__ float2 stats[4 * 64];
+    __shared__ int seg_flag;
     const int slab_local = static_cast<int>(w0 / T);
     const int64_t tile = w0 - static_cast<int64_t>(slab_local) * T;
     const int b = search_base(a.tile_base, a.B, tile);
@@ -106,8 +109,13 @@ __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
     if (valid) stats_add<NH>(rs, v, a.scale2);
     const int64_t seg = static_cast<int64_t>(slab_local) * a.B + b;
     float2* out = a.rec + ((blockIdx.x + seg) * 2) * a.Rs;
+    if (t < a.R) {
+        out[a.Rs + t] = make_float2(-INFINITY, 0.0f);  // no second warpgroup here
+        __threadfence();
+    }
     stats_flush<NH>(rs, stats, t >> 5, 1, out, a.R);
-    if (t < a.R) out[a.Rs + t] = make_float2(-INFINITY, 0.0f);  // no second warpgroup here
+    segment_done(a.tile_base, a.B, a.nslab, gridDim.x, seg, 2, a.rec, a.seg_cnt, a.lse2, a.R, a.Rs,
+                 stats, &seg_flag, t >> 5, 1);
 }
 
 }  // namespace
@@ -122,6 +130,8 @@ cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t*
     a.k = k;
     a.logits = ws_ptr<float>(ws, pl.o_logits);
     a.rec = ws_ptr<float2>(ws, pl.o_part);
+    a.seg_cnt = ws_ptr<unsigned>(ws, pl.o_segcnt);
+    a.lse2 = ws_ptr<float>(ws, pl.o_lse);
     a.bad = &ws_ptr<WsHeader>(ws, 0)->bad_input;
     a.B = pl.B;
     a.Hk = pl.Hk;

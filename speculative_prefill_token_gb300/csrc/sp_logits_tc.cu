@@ -46,6 +46,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
 constexpr int kStageOutBytes = kTileTokens * 128;  // 128 tokens x 32 fp32
 constexpr int kMaxStages = 16;
+constexpr int kAcc = 4;                          // TMEM accumulators (tiles in flight)
 constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
 constexpr int64_t kDrainSpin = int64_t(1) << 22;
 
@@ -53,6 +54,8 @@ struct TcArgs {
     const int32_t* seq_off;
     const int32_t* tile_base;
     float2* rec;     // per (CTA, segment, warpgroup) softmax records [.. * 2 + wg][Rs]
+    unsigned* seg_cnt;  // per segment: records written so far (zero between calls)
+    float* lse2;     // per segment normaliser [seg][Rs]
     int32_t* status;
     const int32_t* bad;
     int B, Hk, G, R, Rs, d_blocks, Nmma, Nacc, slab0, nslab, stages;
@@ -62,7 +65,7 @@ struct TcArgs {
 };
 
 struct SmemLayout {
-    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, stats, total;
+    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, seg_flag, stats, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes,
@@ -77,10 +80,12 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
     s.out_buf = off;                                   // [warpgroup][half] 16 KB, swizzled
     off += 2u * static_cast<uint32_t>(nh) * kStageOutBytes;
     s.bars = off;
-    off += 8u * (2 * kMaxStages + 9);
+    off += 8u * (2 * kMaxStages + 13);
     s.tmem_slot = off;
     off += 8;
     s.abort_flag = off;
+    off += 8;
+    s.seg_flag = off;  // [warpgroup] int
     off += 8;
     s.stats = off;
     off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
@@ -132,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_empty = bar_full + 8 * kMaxStages;
     const uint32_t bar_qfull = bar_empty + 8 * kMaxStages;   // [2]
     const uint32_t bar_qempty = bar_qfull + 16;              // [2]
-    const uint32_t bar_tfull = bar_qempty + 16;              // [2]
-    const uint32_t bar_tempty = bar_tfull + 16;              // [2]
-    const uint32_t bar_drain = bar_tempty + 16;              // [1]
+    const uint32_t bar_tfull = bar_qempty + 16;              // [4]
+    const uint32_t bar_tempty = bar_tfull + 32;              // [4]
+    const uint32_t bar_drain = bar_tempty + 32;              // [1]
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L.tmem_slot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
     float2* stats = reinterpret_cast<float2*>(smem + L.stats);
@@ -152,6 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_qfull + 8 * i, 1);
             mbar_init(bar_qempty + 8 * i, 1);
+        }
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(bar_tfull + 8 * i, 1);
             mbar_init(bar_tempty + 8 * i, 128);
         }
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), static_cast<uint32_t>(2 * a.Nacc));
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), static_cast<uint32_t>(kAcc * a.Nacc));
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -266,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++qn;
                     prev_key = key;
                 }
-                const int acc = static_cast<int>(j & 1);
-                if (!mbar_wait_bounded(bar_tempty + 8 * acc, static_cast<uint32_t>(((j >> 1) & 1) ^ 1),
+                const int acc = static_cast<int>(j & (kAcc - 1));
+                if (!mbar_wait_bounded(bar_tempty + 8 * acc, static_cast<uint32_t>(((j >> 2) & 1) ^ 1),
                                        a.spin, abort_flag)) {
                     record_timeout(a, abort_flag);
                     ok = false;
@@ -307,13 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // epilogue warpgroups
-        const int e = warp >> 2;          // warpgroup: owns accumulator e
+        const int e = warp >> 2;          // warpgroup: tiles j with j % 2 == e
         const int qw = warp & 3;          // TMEM lane quarter
         const int bar_id = 1 + e;
         const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
         uint8_t* out_buf = smem + L.out_buf + e * NH * kStageOutBytes;
         const uint32_t out_addr = smem_u32(out_buf);
         float2* st_sm = stats + e * 4 * 64;
+        volatile int* seg_flag = reinterpret_cast<volatile int*>(smem + L.seg_flag) + e;
         const int tl = qw * 32 + lane;   // token row of the tile
         RowStats<NH> rs;
         stats_reset(rs);
@@ -325,15 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item it = decode(a, w, T);
             const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
             if (key != cur_key) {
-                if (cur_key >= 0)
+                if (cur_key >= 0) {
                     stats_flush<NH>(rs, st_sm, qw, bar_id,
                                     a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs, a.R);
+                    segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
+                                 a.R, a.Rs, st_sm, seg_flag, qw, bar_id);
+                }
                 cur_key = key;
             }
             if (static_cast<int>(j & 1) != e) continue;
             // all 128 threads of the warpgroup take the same decision, so the
             // named barriers below never wait for a thread that left
-            const bool got = mbar_wait_bounded(bar_tfull + 8 * e, static_cast<uint32_t>((j >> 1) & 1),
+            const int acc = static_cast<int>(j & (kAcc - 1));
+            const bool got = mbar_wait_bounded(bar_tfull + 8 * acc, static_cast<uint32_t>((j >> 2) & 1),
                                                a.spin, abort_flag);
             if (!bar_sync_and(bar_id, 128, got)) {
                 record_timeout(a, abort_flag);
@@ -342,12 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             float v[NH][32];
-            const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(e * a.Nacc);
+            const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * a.Nacc);
             tmem_ld_32x32b_x32(taddr, v[0]);
             if (NH > 1) tmem_ld_32x32b_x32(taddr + 32, v[NH - 1]);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(bar_tempty + 8 * e);
+            mbar_arrive(bar_tempty + 8 * acc);
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh)
 #pragma unroll
@@ -377,9 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (tl < it.nvalid) stats_add<NH>(rs, v, a.scale2);
         }
-        if (ok && cur_key >= 0)
+        if (ok && cur_key >= 0) {
             stats_flush<NH>(rs, st_sm, qw, bar_id, a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs,
                             a.R);
+            segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
+                         a.Rs, st_sm, seg_flag, qw, bar_id);
+        }
         if (qw == 0 && lane == 0 && stores) bulk_wait0();
     }
 
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(2 * a.Nacc));
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(kAcc * a.Nacc));
     }
 }
 
@@ -476,6 +491,8 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
     a.seq_off = seq_off;
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
     a.rec = ws_ptr<float2>(ws, pl.o_part);
+    a.seg_cnt = ws_ptr<unsigned>(ws, pl.o_segcnt);
+    a.lse2 = ws_ptr<float>(ws, pl.o_lse);
     a.status = &ws_ptr<WsHeader>(ws, 0)->status;
     a.bad = &ws_ptr<WsHeader>(ws, 0)->bad_input;
     a.B = pl.B;

@@ -1,0 +1,290 @@
+// Chunk selection of one prompt by one CTA: radix select on the order
+// (score descending, chunk index ascending) — "SpecPrefill — Implementation
+// Guide" §Chunk Selection (top fraction by average score) and v3 §v3
+// Improvements item 1 (cumulative attention mass).
+//
+// Fixed mode keeps the first k = max(1, ceil(nc * p)) positions of that
+// order; mass mode keeps the shortest prefix whose running score sum reaches
+// mass * (sum of all scores), the crossing chunk included (all chunks when
+// the total is zero). Only the set is needed, so instead of sorting, four
+// MSB-first 8-bit histogram passes find the key of the last kept position;
+// chunks with a smaller key are kept, and ties with that key are resolved by
+// chunk index. Mass mode accumulates scores as exact fixed-point integers
+// (each fp32 score scaled by a power of two chosen per prompt so that the
+// total stays below 2^53, converted with integer operations only), so the
+// sums are exact and independent of the order of the atomic additions.
+#pragma once
+
+#include <cstdint>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+
+namespace sp {
+
+constexpr int kSelectThreads = 1024;
+
+// Ascending order key of a descending score.
+__device__ __forceinline__ uint32_t score_desc_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ~ord;
+}
+
+// round(f * 2^S) for a non-negative finite fp32 f, integer operations only
+// (half rounds up); S chosen by the caller so the result stays below 2^53.
+__device__ __forceinline__ uint64_t fixed_point(float f, int S) {
+    const uint32_t u = __float_as_uint(f) & 0x7fffffffu;
+    int e = static_cast<int>(u >> 23);
+    uint64_t m = u & 0x7fffffu;
+    if (e == 0) e = 1; else m |= 0x800000u;
+    const int sh = e - 150 + S;   // value = m * 2^(e - 150)
+    if (m == 0) return 0;
+    if (sh >= 0) return m << sh;
+    if (sh <= -64) return 0;
+    return (m + (uint64_t(1) << (-sh - 1))) >> (-sh);
+}
+
+struct SelectShared {
+    unsigned cnt[256];
+    unsigned long long sum[256];
+    unsigned long long wtot[32];
+    unsigned wcnt[32];
+    float wmax[32];
+    int digit;
+    unsigned cnt_before;
+    unsigned long long sum_before;
+    int found;
+    unsigned long long total;
+    float smax;
+    unsigned tie_off;
+    unsigned long long tie_sum_off;
+};
+
+// flags[c] |= 1 for every kept chunk c < nc (flags zeroed by the caller).
+// scores: the prompt's nc chunk scores (global). All kSelectThreads threads
+// of the CTA call this with the same arguments; EMAX >= ceil(nc / threads).
+template <int EMAX>
+__device__ __forceinline__ void radix_select_impl(const float* scores, int64_t nc, int mode,
+                                                  float keep_p, float mass, uint8_t* flags,
+                                                  SelectShared& sm) {
+    constexpr int kSelectEmax = EMAX;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int E = static_cast<int>((nc + kSelectThreads - 1) / kSelectThreads);
+    const int64_t c_lo = static_cast<int64_t>(t) * E;
+    uint32_t key[kSelectEmax];
+    float sc[kSelectEmax];
+#pragma unroll
+    for (int e = 0; e < kSelectEmax; ++e) {
+        const int64_t c = c_lo + e;
+        const bool on = e < E && c < nc;
+        sc[e] = on ? scores[c] : 0.0f;
+        key[e] = on ? score_desc_key(sc[e]) : 0xffffffffu;
+    }
+    const bool is_mass = mode == SP_MODE_MASS;
+    int S = 0;
+    double theta = 0.0;
+    uint64_t need = 0;
+    bool all = false;
+    if (is_mass) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kSelectEmax; ++e) mx = fmaxf(mx, sc[e]);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) sm.wmax[warp] = mx;
+        __syncthreads();
+        if (t == 0) {
+            float m = 0.0f;
+            for (int w = 0; w < kSelectThreads / 32; ++w) m = fmaxf(m, sm.wmax[w]);
+            sm.smax = m;
+        }
+        __syncthreads();
+        const float smax = sm.smax;
+        if (smax > 0.0f) {
+            int lg = 0;
+            while ((int64_t(1) << lg) < nc + 1) ++lg;
+            const int e_max = static_cast<int>((__float_as_uint(smax) >> 23) & 0xff) - 127;  // floor(log2)
+            S = 52 - (e_max + 1) - lg;
+        }
+        uint64_t part = 0;
+#pragma unroll
+        for (int e = 0; e < kSelectEmax; ++e) part += fixed_point(sc[e], S);
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sm.wtot[warp] = part;
+        __syncthreads();
+        if (t == 0) {
+            unsigned long long tot = 0;
+            for (int w = 0; w < kSelectThreads / 32; ++w) tot += sm.wtot[w];
+            sm.total = tot;
+        }
+        __syncthreads();
+        const uint64_t total = sm.total;
+        if (total == 0) all = true;
+        theta = static_cast<double>(mass) * static_cast<double>(total);
+    } else {
+        const double kk = ceil(static_cast<double>(nc) * static_cast<double>(keep_p));
+        int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
+        need = static_cast<uint64_t>(k > nc ? nc : k);
+    }
+
+    uint32_t prefix = 0, pmask = 0;
+    uint64_t base_sum = 0;  // mass: fixed-point sum of all keys below the current bucket
+    unsigned final_ties = 0;
+    for (int pass = 0; pass < 4 && !all; ++pass) {
+        const int shift = 24 - 8 * pass;
+        if (t < 256) {
+            sm.cnt[t] = 0;
+            sm.sum[t] = 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kSelectEmax; ++e) {
+            if (e < E && c_lo + e < nc && (key[e] & pmask) == prefix) {
+                const int d = static_cast<int>((key[e] >> shift) & 0xffu);
+                atomicAdd(&sm.cnt[d], 1u);
+                if (is_mass) atomicAdd(&sm.sum[d], static_cast<unsigned long long>(fixed_point(sc[e], S)));
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned lc = 0;
+            unsigned long long ls = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lc += sm.cnt[8 * lane + i];
+                ls += sm.sum[8 * lane + i];
+            }
+            unsigned ic = lc;
+            unsigned long long is = ls;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned uc = __shfl_up_sync(0xffffffffu, ic, o);
+                const unsigned long long us = __shfl_up_sync(0xffffffffu, is, o);
+                if (lane >= o) {
+                    ic += uc;
+                    is += us;
+                }
+            }
+            unsigned cb = ic - lc;             // counts of this pass's bins before the lane
+            unsigned long long sb = is - ls;
+            int hit = -1;
+            unsigned hit_cb = 0;
+            unsigned long long hit_sb = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = 8 * lane + i;
+                const unsigned c = sm.cnt[d];
+                const unsigned long long s = sm.sum[d];
+                bool reach;
+                if (is_mass) reach = static_cast<double>(base_sum + sb + s) >= theta && c > 0;
+                else reach = static_cast<uint64_t>(cb) + c >= need;
+                if (hit < 0 && reach) {
+                    hit = d;
+                    hit_cb = cb;
+                    hit_sb = sb;
+                }
+                cb += c;
+                sb += s;
+            }
+            const unsigned ballot = __ballot_sync(0xffffffffu, hit >= 0);
+            if (ballot == 0) {
+                if (lane == 0) sm.found = 0;
+            } else if (lane == __ffs(ballot) - 1) {
+                sm.found = 1;
+                sm.digit = hit;
+                sm.cnt_before = hit_cb;
+                sm.sum_before = hit_sb;
+            }
+        }
+        __syncthreads();
+        if (!sm.found) {
+            all = true;  // the running sum never reaches theta: every chunk is kept
+        } else {
+            const int d = sm.digit;
+            prefix |= static_cast<uint32_t>(d) << shift;
+            pmask |= 0xffu << shift;
+            if (is_mass) base_sum += sm.sum_before;
+            else need -= sm.cnt_before;
+            final_ties = sm.cnt[d];
+        }
+        __syncthreads();
+    }
+
+    if (all) {
+#pragma unroll
+        for (int e = 0; e < kSelectEmax; ++e)
+            if (e < E && c_lo + e < nc) flags[c_lo + e] |= 1;
+        return;
+    }
+    // keys below the final key are kept; ties with it in chunk-index order
+    unsigned my_ties = 0;
+    unsigned long long my_tie_sum = 0;
+#pragma unroll
+    for (int e = 0; e < kSelectEmax; ++e)
+        if (e < E && c_lo + e < nc && key[e] == prefix) {
+            ++my_ties;
+            if (is_mass) my_tie_sum += fixed_point(sc[e], S);
+        }
+    unsigned tie_before = 0;
+    unsigned long long tie_sum_before = 0;
+    if (final_ties > 1) {
+        // exclusive scans of the tie counts (and sums) in chunk order
+        unsigned ic = my_ties;
+        unsigned long long is = my_tie_sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned uc = __shfl_up_sync(0xffffffffu, ic, o);
+            const unsigned long long us = __shfl_up_sync(0xffffffffu, is, o);
+            if (lane >= o) {
+                ic += uc;
+                is += us;
+            }
+        }
+        if (lane == 31) {
+            sm.wcnt[warp] = ic;
+            sm.wtot[warp] = is;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned wc = sm.wcnt[lane];
+            unsigned long long wsum = sm.wtot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned uc = __shfl_up_sync(0xffffffffu, wc, o);
+                const unsigned long long us = __shfl_up_sync(0xffffffffu, wsum, o);
+                if (lane >= o) {
+                    wc += uc;
+                    wsum += us;
+                }
+            }
+            sm.wcnt[lane] = wc;
+            sm.wtot[lane] = wsum;
+        }
+        __syncthreads();
+        tie_before = ic - my_ties + (warp > 0 ? sm.wcnt[warp - 1] : 0u);
+        tie_sum_before = is - my_tie_sum + (warp > 0 ? sm.wtot[warp - 1] : 0ull);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int e = 0; e < kSelectEmax; ++e) {
+        const int64_t c = c_lo + e;
+        if (!(e < E && c < nc)) continue;
+        bool keep = key[e] < prefix;
+        if (key[e] == prefix) {
+            if (is_mass) keep = static_cast<double>(base_sum + tie_sum_before) < theta;
+            else keep = tie_before < need;
+            ++tie_before;
+            if (is_mass) tie_sum_before += fixed_point(sc[e], S);
+        }
+        if (keep) flags[c] |= 1;
+    }
+}
+
+__device__ __forceinline__ void radix_select(const float* scores, int64_t nc, int mode, float keep_p,
+                                             float mass, uint8_t* flags, SelectShared& sm) {
+    if (nc <= kSelectThreads) radix_select_impl<1>(scores, nc, mode, keep_p, mass, flags, sm);
+    else if (nc <= 4 * kSelectThreads) radix_select_impl<4>(scores, nc, mode, keep_p, mass, flags, sm);
+    else radix_select_impl<kMaxPromptChunks / kSelectThreads>(scores, nc, mode, keep_p, mass, flags, sm);
+}
+
+}  // namespace sp

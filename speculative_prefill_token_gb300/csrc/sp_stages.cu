@@ -20,6 +20,7 @@
 
 #include "sp_device.cuh"
 #include "sp_internal.h"
+#include "sp_select.cuh"
 
 namespace sp {
 namespace {
@@ -37,6 +38,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
                                                             int32_t* tile_base, int32_t* chunk_off,
                                                             int32_t* pblk_base, int32_t* chunk_off_out,
                                                             const int32_t* chunk_off_check,
+                                                            unsigned* seg_cnt, int64_t n_seg_cnt,
                                                             WsHeader* hdr) {
     __shared__ int bad;
     __shared__ int64_t warp_sums[3][32];
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
     __syncthreads();
     for (int b = tid; b < B; b += kPrepThreads)
         if (seq_off[b + 1] < seq_off[b]) bad = 1;
+    for (int64_t i = tid; i < n_seg_cnt; i += kPrepThreads) seg_cnt[i] = 0u;
     __syncthreads();
     const int per = (B + kPrepThreads - 1) / kPrepThreads;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
@@ -116,35 +119,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
     }
 }
 
-// ------------------------------------------------------------ normaliser
-// lse2[slab][b][r] = log2 sum_t exp2(scale2 * s[t, r]) over prompt b's keys,
-// merged from the records the logits kernel wrote per (CTA, segment,
-// warpgroup): only the CTAs whose item range meets the segment are read.
-__global__ void __launch_bounds__(64) lse_kernel(const float2* rec, const int32_t* tile_base,
-                                                 float* lse2, int B, int R, int Rs, int64_t C,
-                                                 int nslab, const int32_t* bad) {
-    if (*bad) return;
-    const int seg = blockIdx.x;  // slab_local * B + b
-    const int slab = seg / B, b = seg - slab * B;
-    const int r = threadIdx.x;
-    if (r >= R) return;
-    const int64_t T = tile_base[B];
-    const int64_t W = T * nslab;
-    const int64_t i0 = static_cast<int64_t>(slab) * T + tile_base[b];
-    const int64_t i1 = static_cast<int64_t>(slab) * T + tile_base[b + 1];
-    float out = INFINITY;
-    if (i1 > i0) {
-        const int64_t c0 = split_owner(W, C, i0), c1 = split_owner(W, C, i1 - 1);
-        float2 acc = make_float2(-INFINITY, 0.0f);
-        for (int64_t c = c0; c <= c1; ++c) {
-            acc = merge_partial(acc, rec[((c + seg) * 2 + 0) * Rs + r]);
-            acc = merge_partial(acc, rec[((c + seg) * 2 + 1) * Rs + r]);
-        }
-        out = acc.y > 0.0f ? acc.x + log2f(acc.y) : INFINITY;
-    }
-    lse2[static_cast<int64_t>(seg) * Rs + r] = out;
-}
-
 // --------------------------------------------------------------- reduce
 // Token importance. One CTA covers TOK tokens of one tile; thread (token,
 // quad) reads the quad's four raw logits of every slab of the wave with one
@@ -185,9 +159,25 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     if (tq < nvalid) {
         const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-        for (int s = 0; s < nslab; ++s) {
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(
-                logits + (static_cast<int64_t>(s) * rows_per_slab + row) * Rs + 4 * c));
+        const float* src = logits + row * Rs + 4 * c;
+        const int64_t slab_stride = rows_per_slab * Rs;
+        int s = 0;
+        for (; s + 4 <= nslab; s += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s + u) * slab_stride));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float* ls = lse_s + (s + u) * Rs + 4 * c;
+                m0 = fmaxf(m0, fmaf(v[u].x, scale2, -ls[0]));
+                m1 = fmaxf(m1, fmaf(v[u].y, scale2, -ls[1]));
+                m2 = fmaxf(m2, fmaf(v[u].z, scale2, -ls[2]));
+                m3 = fmaxf(m3, fmaf(v[u].w, scale2, -ls[3]));
+            }
+        }
+        for (; s < nslab; ++s) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(src + s * slab_stride));
             const float* ls = lse_s + s * Rs + 4 * c;
             m0 = fmaxf(m0, fmaf(v.x, scale2, -ls[0]));
             m1 = fmaxf(m1, fmaf(v.y, scale2, -ls[1]));
@@ -332,13 +322,7 @@ __global__ void __launch_bounds__(256) chunk_kernel(const float* tok, const floa
 }
 
 // --------------------------------------------------------------- select
-constexpr int kSelThreads = 1024;
-
-__device__ __forceinline__ uint32_t desc_key(float f) {
-    const uint32_t u = __float_as_uint(f);
-    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending order key
-    return ~ord;                                                       // descending
-}
+constexpr int kSelThreads = kSelectThreads;
 
 // Block-wide inclusive scan of one int64 per thread.
 __device__ __forceinline__ int64_t block_scan_i64(int64_t v, int64_t* warp_tot) {
@@ -365,34 +349,9 @@ __device__ __forceinline__ int64_t block_scan_i64(int64_t v, int64_t* warp_tot) 
     return r;
 }
 
-__device__ __forceinline__ double block_scan_f64(double v, double* warp_tot) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        double w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0.0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double u = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += u;
-        }
-        warp_tot[lane] = w;
-    }
-    __syncthreads();
-    const double r = v + (warp > 0 ? warp_tot[warp - 1] : 0.0);
-    __syncthreads();
-    return r;
-}
-
 // Per-prompt kept-token counts of each chunk, their exclusive scan, the
 // prompt's total; the last prompt to finish (ticket) writes kept_off and
-// n_kept for the whole batch. `flags` is the prompt's chunk_keep in shared
-// or global memory.
+// n_kept for the whole batch.
 __device__ void scan_kept(const uint8_t* flags, int64_t nc, int64_t n, int C, int force_bos, int b,
                           int B, int32_t* ckoff, int32_t* pcount, int32_t* kept_off,
                           int32_t* n_kept, WsHeader* hdr, int64_t* scratch) {
@@ -440,103 +399,30 @@ __device__ void scan_kept(const uint8_t* flags, int64_t nc, int64_t n, int C, in
     }
 }
 
-struct SelectArgs {
-    const int32_t* seq_off;
-    const int32_t* chunk_off;
-    const float* chunk_score;
-    uint8_t* keep;
-    int32_t* ckoff;
-    int32_t* pcount;
-    int32_t* kept_off;
-    int32_t* n_kept;
-    WsHeader* hdr;
-    int B, C, mode, force_bos, force_last, sort_cap, fuse_scan;
-    float keep_p, mass;
-};
-
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
-    if (a.hdr->bad_input) return;
-    extern __shared__ uint64_t keys[];  // [sort_cap], then flags bytes
-    uint8_t* flags = reinterpret_cast<uint8_t*>(keys + a.sort_cap);
-    __shared__ int64_t scan_i[32];
-    __shared__ double scan_d[32];
-    __shared__ int k_sel;
+// One CTA per prompt: radix selection, then the forced final chunk.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* chunk_off,
+                                                             const float* chunk_score,
+                                                             uint8_t* keep, WsHeader* hdr, int mode,
+                                                             float keep_p, float mass,
+                                                             int force_last) {
+    if (hdr->bad_input) return;
+    extern __shared__ uint8_t flags[];
+    __shared__ SelectShared ss;
     const int b = blockIdx.x;
-    const int64_t c0 = a.chunk_off[b];
-    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - c0;
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - a.seq_off[b];
-    const int tid = threadIdx.x;
-    const bool too_many = nc > a.sort_cap;
-    if (too_many && tid == 0) atomicCAS(&a.hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
-    int64_t P = 1;
-    while (P < nc) P <<= 1;
-    if (!too_many && nc > 0) {
-        for (int64_t i = tid; i < P; i += kSelThreads)
-            keys[i] = i < nc ? (static_cast<uint64_t>(desc_key(a.chunk_score[c0 + i])) << 32) |
-                                   static_cast<uint64_t>(i)
-                             : ~0ull;
-        for (int64_t i = tid; i < nc; i += kSelThreads) flags[i] = 0;
-        __syncthreads();
-        // bitonic sort, ascending: score descending, then chunk index ascending
-        for (int64_t k = 2; k <= P; k <<= 1) {
-            for (int64_t j = k >> 1; j > 0; j >>= 1) {
-                for (int64_t i = tid; i < P; i += kSelThreads) {
-                    const int64_t ixj = i ^ j;
-                    if (ixj > i) {
-                        const uint64_t x = keys[i], y = keys[ixj];
-                        const bool up = (i & k) == 0;
-                        if ((x > y) == up) {
-                            keys[i] = y;
-                            keys[ixj] = x;
-                        }
-                    }
-                }
-                __syncthreads();
-            }
-        }
-        if (a.mode == SP_MODE_FIXED) {
-            if (tid == 0) {
-                const double kk = ceil(static_cast<double>(nc) * static_cast<double>(a.keep_p));
-                int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
-                k_sel = static_cast<int>(k > nc ? nc : k);
-            }
-        } else {
-            // cumulative mass over the ranking, fp64 running sums
-            const int64_t per = (P + kSelThreads - 1) / kSelThreads;
-            const int64_t lo = min64(nc, tid * per), hi = min64(nc, lo + per);
-            double local = 0.0;
-            for (int64_t i = lo; i < hi; ++i)
-                local += static_cast<double>(a.chunk_score[c0 + static_cast<int64_t>(keys[i] & 0xffffffffu)]);
-            const double incl = block_scan_f64(local, scan_d);
-            __shared__ double total_s;
-            if (tid == kSelThreads - 1) total_s = incl;
-            if (tid == 0) k_sel = static_cast<int>(nc);
-            __syncthreads();
-            const double total = total_s;
-            if (total > 0.0) {
-                const double theta = static_cast<double>(a.mass) * total;
-                double cum = incl - local;
-                for (int64_t i = lo; i < hi; ++i) {
-                    const double before = cum;
-                    cum += static_cast<double>(a.chunk_score[c0 + static_cast<int64_t>(keys[i] & 0xffffffffu)]);
-                    if (cum >= theta && before < theta) k_sel = static_cast<int>(i + 1);
-                }
-            }
-        }
-        __syncthreads();
-        const int ks = k_sel;
-        for (int64_t i = tid; i < ks; i += kSelThreads) flags[keys[i] & 0xffffffffu] = 1;
-        __syncthreads();
-        if (a.force_last && tid == 0) flags[nc - 1] |= 2;
-        __syncthreads();
-        for (int64_t i = tid; i < nc; i += kSelThreads) a.keep[c0 + i] = flags[i];
-        __syncthreads();
+    const int64_t c0 = chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(chunk_off[b + 1]) - c0;
+    if (nc > kMaxPromptChunks) {
+        if (threadIdx.x == 0) atomicCAS(&hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
+        return;
     }
-    if (a.fuse_scan) {
-        const int64_t ncs = too_many ? 0 : nc;
-        scan_kept(flags, ncs, n, a.C, a.force_bos, b, a.B, a.ckoff + c0, a.pcount, a.kept_off,
-                  a.n_kept, a.hdr, scan_i);
-    }
+    if (nc == 0) return;
+    for (int64_t i = threadIdx.x; i < nc; i += kSelThreads) flags[i] = 0;
+    __syncthreads();
+    radix_select(chunk_score + c0, nc, mode, keep_p, mass, flags, ss);
+    __syncthreads();
+    if (force_last && threadIdx.x == 0) flags[nc - 1] |= 2;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < nc; i += kSelThreads) keep[c0 + i] = flags[i];
 }
 
 __global__ void __launch_bounds__(kSelThreads) gather_scan_kernel(
@@ -590,7 +476,9 @@ cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_
                                             ws_ptr<int32_t>(ws, pl.o_tile_base),
                                             ws_ptr<int32_t>(ws, pl.o_chunk_off),
                                             ws_ptr<int32_t>(ws, pl.o_pblk_base), chunk_off_out,
-                                            nullptr, ws_ptr<WsHeader>(ws, 0));
+                                            nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
+                                            static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+                                            ws_ptr<WsHeader>(ws, 0));
     return cudaGetLastError();
 }
 
@@ -600,14 +488,9 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
                                             ws_ptr<int32_t>(ws, pl.o_tile_base),
                                             ws_ptr<int32_t>(ws, pl.o_chunk_off),
                                             ws_ptr<int32_t>(ws, pl.o_pblk_base), nullptr,
-                                            chunk_off_check, ws_ptr<WsHeader>(ws, 0));
-    return cudaGetLastError();
-}
-
-cudaError_t launch_lse(const Plan& pl, void* ws, int nslab, int grid, cudaStream_t st) {
-    lse_kernel<<<static_cast<unsigned>(nslab * pl.B), 64, 0, st>>>(
-        ws_ptr<float2>(ws, pl.o_part), ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_lse),
-        pl.B, pl.R, pl.Rs, grid, nslab, &ws_ptr<WsHeader>(ws, 0)->bad_input);
+                                            chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
+                                            static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+                                            ws_ptr<WsHeader>(ws, 0));
     return cudaGetLastError();
 }
 
@@ -659,32 +542,15 @@ cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq
                           const int32_t* chunk_off, const float* chunk_score, uint8_t* keep,
                           void* ws, bool fuse_scan, int32_t* kept_off, int32_t* n_kept,
                           cudaStream_t st) {
-    SelectArgs a;
-    a.seq_off = seq_off;
-    a.chunk_off = chunk_off;
-    a.chunk_score = chunk_score;
-    a.keep = keep;
-    a.ckoff = ws_ptr<int32_t>(ws, pl.o_ckoff);
-    a.pcount = ws_ptr<int32_t>(ws, pl.o_pcount);
-    a.kept_off = kept_off;
-    a.n_kept = n_kept;
-    a.hdr = ws_ptr<WsHeader>(ws, 0);
-    a.B = pl.B;
-    a.C = pl.C;
-    a.mode = p->mode;
-    a.force_bos = p->force_bos;
-    a.force_last = p->force_last_chunk;
-    a.sort_cap = pl.sort_cap;
-    a.fuse_scan = fuse_scan ? 1 : 0;
-    a.keep_p = p->keep_p;
-    a.mass = p->mass;
-    const size_t smem = static_cast<size_t>(pl.sort_cap) * 9;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    select_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, smem, st>>>(a);
+    (void)seq_off;
+    (void)fuse_scan;
+    (void)kept_off;
+    (void)n_kept;
+    const int64_t max_nc = (pl.Ntot + pl.C - 1) / pl.C;
+    const size_t smem = static_cast<size_t>(max_nc < kMaxPromptChunks ? max_nc : kMaxPromptChunks);
+    select_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, smem, st>>>(
+        chunk_off, chunk_score, keep, ws_ptr<WsHeader>(ws, 0), p->mode, p->keep_p, p->mass,
+        p->force_last_chunk);
     return cudaGetLastError();
 }
 

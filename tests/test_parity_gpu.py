@@ -75,8 +75,12 @@ def _run(cuda_lib, q_np, k_np, off_np, kw):
     q = torch.from_numpy(np.ascontiguousarray(q_np).view(np.int16)).cuda()
     k = torch.from_numpy(np.ascontiguousarray(k_np).view(np.int16)).cuda()
     off = torch.from_numpy(np.asarray(off_np, dtype=np.int32)).cuda()
-    out = sp.specprefill_score(q, k, off, _params(sp, kw))
+    p = _params(sp, kw)
+    # a workspace full of NaN bytes: any read of scratch nobody wrote shows up
+    ws = sp.make_workspace(sp.shape_of(q, k), p, poison=True)
+    out = sp.specprefill_score(q, k, off, p, ws=ws)
     torch.cuda.synchronize()
+    assert sp.device_status(ws) == 0
     return gh.out_to_numpy(out), (q, k, off)
 
 
