@@ -136,6 +136,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_imp = take(static_cast<size_t>(P.Ntot) * 4);
     P.o_tok = take(static_cast<size_t>(P.Ntot) * 4);
     P.o_ppart = take(static_cast<size_t>(P.pblk_max) * 8);
+    P.o_rpart = take(static_cast<size_t>(P.tiles_max) * 8);  // per 128-token pool CTA
+    P.o_csum = take(static_cast<size_t>(P.chunks_max) * 8);
     P.o_cscore = take(static_cast<size_t>(P.chunks_max) * 4);
     P.o_ckeep = take(static_cast<size_t>(P.chunks_max));
     P.o_ckoff = take(static_cast<size_t>(P.chunks_max) * 4);
@@ -169,7 +171,8 @@ int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, 
         if (w == pl.waves - 1 && prof && prof->logits_stop)
             if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_stop), st) != cudaSuccess)
                 return SP_ERR_CUDA;
-        if ((e = launch_reduce(pl, seq_off, ws, ns, w, imp, st)) != cudaSuccess) return SP_ERR_CUDA;
+        if ((e = launch_reduce(pl, seq_off, ws, ns, w, imp, st)) != cudaSuccess)
+            return SP_ERR_CUDA;
     }
     return SP_OK;
 }
@@ -298,11 +301,24 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
     uint8_t* keep_p = chunk_keep ? chunk_keep : ws_ptr<uint8_t>(ws, pl.o_ckeep);
     const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
-    if ((rc = importance_waves(pl, shape, seq_off, q, k, imp_p, ws, st, false, prof)) != SP_OK) return rc;
-    if (launch_post(pl, params, seq_off, imp_p, tok_p, cs_p, keep_p, kept_idx, kept_pos, kept_off,
-                    n_kept, ws, st) != cudaSuccess)
-        return SP_ERR_CUDA;
-    if (pl.B == 1) return SP_OK;  // the post kernel wrote the kept lists itself
+    if ((rc = importance_waves(pl, shape, seq_off, q, k, imp_p, ws, st, false, prof)) != SP_OK)
+        return rc;
+    if (fused_post_ok(params)) {
+        if (launch_pool_sums(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess)
+            return SP_ERR_CUDA;
+        if (launch_post(pl, params, seq_off, imp_p, tok_p, cs_p, keep_p, kept_idx, kept_pos,
+                        kept_off, n_kept, ws, st) != cudaSuccess)
+            return SP_ERR_CUDA;
+    } else {
+        if (launch_pool(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+        if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+        if (launch_select(pl, params, seq_off, coff, cs_p, keep_p, ws, false, nullptr, nullptr, st) !=
+            cudaSuccess)
+            return SP_ERR_CUDA;
+        if (launch_gather_scan(pl, params, seq_off, coff, keep_p, ws, kept_off, n_kept, st) !=
+            cudaSuccess)
+            return SP_ERR_CUDA;
+    }
     return to_status(launch_gather_write(pl, params, seq_off, coff, keep_p, kept_idx, kept_pos,
                                          kept_off, n_kept, ws, st));
 }

@@ -198,6 +198,20 @@ __device__ __forceinline__ void segment_done(const int32_t* tile_base, int B, in
     asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
 }
 
+// Chunk score = mean over the chunk of boost(t) * normalise(x(t)). The
+// min-max normalisation is affine, so with S_bx = sum boost*x and
+// S_b = sum boost (token order) the mean is
+// (S_bx - min * S_b) / (max - min) / count; a constant prompt (max == min)
+// normalises to all ones, giving S_b / count. Clamped at zero (rounding of
+// the difference of two nearly equal sums).
+__device__ __forceinline__ float chunk_score_from_sums(float sbx, float sb, float mn, float mx,
+                                                       int normalize, int64_t count) {
+    const float cnt = static_cast<float>(count);
+    if (!normalize) return sbx / cnt;
+    if (mx == mn) return sb / cnt;
+    return fmaxf(fmaf(-mn, sb, sbx), 0.0f) / (mx - mn) / cnt;
+}
+
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 

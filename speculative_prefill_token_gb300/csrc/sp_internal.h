@@ -45,6 +45,7 @@ struct Plan {
     int64_t spin;         // bounded-wait poll limit
     // workspace offsets (bytes)
     size_t o_tile_base, o_chunk_off, o_pblk_base, o_segcnt, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
+        o_rpart, o_csum,
         o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
 };
 
@@ -69,6 +70,15 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
 // Softmax, max over heads/layers of the wave; the last wave writes imp.
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
                           float* imp, cudaStream_t st);
+
+// Fused-path pooling: pooled scores, per-tile min / max and per-chunk sums
+// (requires fused_post_ok: the pool halo fits and chunks never straddle a
+// 128-token tile).
+inline bool fused_post_ok(const sp_params* p) {
+    return p->pool_w / 2 <= 64 && 128 % p->chunk == 0;
+}
+cudaError_t launch_pool_sums(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                             const float* imp, float* tok, void* ws, cudaStream_t st);
 
 cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                         const float* imp, float* tok, void* ws, cudaStream_t st);

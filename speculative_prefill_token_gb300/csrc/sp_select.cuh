@@ -22,7 +22,8 @@
 
 namespace sp {
 
-constexpr int kSelectThreads = 1024;
+constexpr int kSelectThreads = 256;
+constexpr int kSelectWarps = kSelectThreads / 32;
 
 // Ascending order key of a descending score.
 __device__ __forceinline__ uint32_t score_desc_key(float f) {
@@ -46,6 +47,8 @@ __device__ __forceinline__ uint64_t fixed_point(float f, int S) {
 }
 
 struct SelectShared {
+    unsigned wcnt_h[kSelectWarps][256];            // per-warp histograms
+    unsigned long long wsum_h[kSelectWarps][256];
     unsigned cnt[256];
     unsigned long long sum[256];
     unsigned long long wtot[32];
@@ -57,30 +60,17 @@ struct SelectShared {
     int found;
     unsigned long long total;
     float smax;
-    unsigned tie_off;
-    unsigned long long tie_sum_off;
 };
 
 // flags[c] |= 1 for every kept chunk c < nc (flags zeroed by the caller).
-// scores: the prompt's nc chunk scores (global). All kSelectThreads threads
-// of the CTA call this with the same arguments; EMAX >= ceil(nc / threads).
-template <int EMAX>
-__device__ __forceinline__ void radix_select_impl(const float* scores, int64_t nc, int mode,
-                                                  float keep_p, float mass, uint8_t* flags,
-                                                  SelectShared& sm) {
-    constexpr int kSelectEmax = EMAX;
+// scores: the prompt's nc chunk scores in shared memory. All kSelectThreads
+// threads of the CTA call this; thread t owns chunks [t*E, t*E + E).
+__device__ __forceinline__ void radix_select(const float* scores, int64_t nc, int mode, float keep_p,
+                                             float mass, uint8_t* flags, SelectShared& sm) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int E = static_cast<int>((nc + kSelectThreads - 1) / kSelectThreads);
     const int64_t c_lo = static_cast<int64_t>(t) * E;
-    uint32_t key[kSelectEmax];
-    float sc[kSelectEmax];
-#pragma unroll
-    for (int e = 0; e < kSelectEmax; ++e) {
-        const int64_t c = c_lo + e;
-        const bool on = e < E && c < nc;
-        sc[e] = on ? scores[c] : 0.0f;
-        key[e] = on ? score_desc_key(sc[e]) : 0xffffffffu;
-    }
+    const int64_t c_hi = c_lo + E < nc ? c_lo + E : nc;
     const bool is_mass = mode == SP_MODE_MASS;
     int S = 0;
     double theta = 0.0;
@@ -88,14 +78,13 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
     bool all = false;
     if (is_mass) {
         float mx = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kSelectEmax; ++e) mx = fmaxf(mx, sc[e]);
+        for (int64_t c = c_lo; c < c_hi; ++c) mx = fmaxf(mx, scores[c]);
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0) sm.wmax[warp] = mx;
         __syncthreads();
         if (t == 0) {
             float m = 0.0f;
-            for (int w = 0; w < kSelectThreads / 32; ++w) m = fmaxf(m, sm.wmax[w]);
+            for (int w = 0; w < kSelectWarps; ++w) m = fmaxf(m, sm.wmax[w]);
             sm.smax = m;
         }
         __syncthreads();
@@ -107,14 +96,13 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
             S = 52 - (e_max + 1) - lg;
         }
         uint64_t part = 0;
-#pragma unroll
-        for (int e = 0; e < kSelectEmax; ++e) part += fixed_point(sc[e], S);
+        for (int64_t c = c_lo; c < c_hi; ++c) part += fixed_point(scores[c], S);
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) sm.wtot[warp] = part;
         __syncthreads();
         if (t == 0) {
             unsigned long long tot = 0;
-            for (int w = 0; w < kSelectThreads / 32; ++w) tot += sm.wtot[w];
+            for (int w = 0; w < kSelectWarps; ++w) tot += sm.wtot[w];
             sm.total = tot;
         }
         __syncthreads();
@@ -132,18 +120,33 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
     unsigned final_ties = 0;
     for (int pass = 0; pass < 4 && !all; ++pass) {
         const int shift = 24 - 8 * pass;
-        if (t < 256) {
-            sm.cnt[t] = 0;
-            sm.sum[t] = 0;
+        for (int i = t; i < kSelectWarps * 256; i += kSelectThreads) {
+            (&sm.wcnt_h[0][0])[i] = 0u;
+            if (is_mass) (&sm.wsum_h[0][0])[i] = 0ull;
         }
         __syncthreads();
-#pragma unroll
-        for (int e = 0; e < kSelectEmax; ++e) {
-            if (e < E && c_lo + e < nc && (key[e] & pmask) == prefix) {
-                const int d = static_cast<int>((key[e] >> shift) & 0xffu);
-                atomicAdd(&sm.cnt[d], 1u);
-                if (is_mass) atomicAdd(&sm.sum[d], static_cast<unsigned long long>(fixed_point(sc[e], S)));
+        // each warp counts into its own histogram: no contention across warps
+        for (int64_t c = c_lo; c < c_hi; ++c) {
+            const float sc = scores[c];
+            const uint32_t key = score_desc_key(sc);
+            if ((key & pmask) == prefix) {
+                const int d = static_cast<int>((key >> shift) & 0xffu);
+                atomicAdd(&sm.wcnt_h[warp][d], 1u);
+                if (is_mass) atomicAdd(&sm.wsum_h[warp][d], static_cast<unsigned long long>(fixed_point(sc, S)));
             }
+        }
+        __syncthreads();
+        {
+            const int d = t;  // kSelectThreads == 256 bins
+            unsigned c = 0;
+            unsigned long long sv = 0;
+#pragma unroll
+            for (int w = 0; w < kSelectWarps; ++w) {
+                c += sm.wcnt_h[w][d];
+                if (is_mass) sv += sm.wsum_h[w][d];
+            }
+            sm.cnt[d] = c;
+            sm.sum[d] = sv;
         }
         __syncthreads();
         if (warp == 0) {
@@ -174,9 +177,9 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
             for (int i = 0; i < 8; ++i) {
                 const int d = 8 * lane + i;
                 const unsigned c = sm.cnt[d];
-                const unsigned long long s = sm.sum[d];
+                const unsigned long long sv = sm.sum[d];
                 bool reach;
-                if (is_mass) reach = static_cast<double>(base_sum + sb + s) >= theta && c > 0;
+                if (is_mass) reach = c > 0 && static_cast<double>(base_sum + sb + sv) >= theta;
                 else reach = static_cast<uint64_t>(cb) + c >= need;
                 if (hit < 0 && reach) {
                     hit = d;
@@ -184,7 +187,7 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
                     hit_sb = sb;
                 }
                 cb += c;
-                sb += s;
+                sb += sv;
             }
             const unsigned ballot = __ballot_sync(0xffffffffu, hit >= 0);
             if (ballot == 0) {
@@ -211,19 +214,16 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
     }
 
     if (all) {
-#pragma unroll
-        for (int e = 0; e < kSelectEmax; ++e)
-            if (e < E && c_lo + e < nc) flags[c_lo + e] |= 1;
+        for (int64_t c = c_lo; c < c_hi; ++c) flags[c] |= 1;
         return;
     }
     // keys below the final key are kept; ties with it in chunk-index order
     unsigned my_ties = 0;
     unsigned long long my_tie_sum = 0;
-#pragma unroll
-    for (int e = 0; e < kSelectEmax; ++e)
-        if (e < E && c_lo + e < nc && key[e] == prefix) {
+    for (int64_t c = c_lo; c < c_hi; ++c)
+        if (score_desc_key(scores[c]) == prefix) {
             ++my_ties;
-            if (is_mass) my_tie_sum += fixed_point(sc[e], S);
+            if (is_mass) my_tie_sum += fixed_point(scores[c], S);
         }
     unsigned tie_before = 0;
     unsigned long long tie_sum_before = 0;
@@ -246,8 +246,8 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
         }
         __syncthreads();
         if (warp == 0) {
-            unsigned wc = sm.wcnt[lane];
-            unsigned long long wsum = sm.wtot[lane];
+            unsigned wc = lane < kSelectWarps ? sm.wcnt[lane] : 0u;
+            unsigned long long wsum = lane < kSelectWarps ? sm.wtot[lane] : 0ull;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const unsigned uc = __shfl_up_sync(0xffffffffu, wc, o);
@@ -265,26 +265,17 @@ __device__ __forceinline__ void radix_select_impl(const float* scores, int64_t n
         tie_sum_before = is - my_tie_sum + (warp > 0 ? sm.wtot[warp - 1] : 0ull);
         __syncthreads();
     }
-#pragma unroll
-    for (int e = 0; e < kSelectEmax; ++e) {
-        const int64_t c = c_lo + e;
-        if (!(e < E && c < nc)) continue;
-        bool keep = key[e] < prefix;
-        if (key[e] == prefix) {
+    for (int64_t c = c_lo; c < c_hi; ++c) {
+        const uint32_t key = score_desc_key(scores[c]);
+        bool keep = key < prefix;
+        if (key == prefix) {
             if (is_mass) keep = static_cast<double>(base_sum + tie_sum_before) < theta;
             else keep = tie_before < need;
             ++tie_before;
-            if (is_mass) tie_sum_before += fixed_point(sc[e], S);
+            if (is_mass) tie_sum_before += fixed_point(scores[c], S);
         }
         if (keep) flags[c] |= 1;
     }
-}
-
-__device__ __forceinline__ void radix_select(const float* scores, int64_t nc, int mode, float keep_p,
-                                             float mass, uint8_t* flags, SelectShared& sm) {
-    if (nc <= kSelectThreads) radix_select_impl<1>(scores, nc, mode, keep_p, mass, flags, sm);
-    else if (nc <= 4 * kSelectThreads) radix_select_impl<4>(scores, nc, mode, keep_p, mass, flags, sm);
-    else radix_select_impl<kMaxPromptChunks / kSelectThreads>(scores, nc, mode, keep_p, mass, flags, sm);
 }
 
 }  // namespace sp

@@ -120,14 +120,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 }
 
 // --------------------------------------------------------------- reduce
-// Token importance. One CTA covers TOK tokens of one tile; thread (token,
-// quad) reads the quad's four raw logits of every slab of the wave with one
-// coalesced 16-byte load each, and keeps the running max over slabs of
-// scale2 * s - lse2 (the log2 softmax probability). One thread per token
+// Token importance. One CTA covers TOK = 1024 / Rs tokens of one tile; thread
+// (token, quad) loads the quad's four raw logits of 4 slabs of the wave at a
+// time (coalesced 16-byte loads; few registers keep many CTAs resident) and keeps the max over slabs of
+// scale2 * s - lse2 (log2 of the softmax probability). One thread per token
 // then takes the max over the G heads of each lookahead step, combines it
 // with earlier waves, and (last wave) writes
 // imp[t] = (1/L) sum_l exp2(max over layers, heads).
 constexpr int kReduceThreads = 256;
+constexpr int kReduceSlabBatch = 4;
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     const float* logits, const float* lse2, const int32_t* seq_off, const int32_t* tile_base,
@@ -154,36 +155,30 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
         const int s = idx / Rs, r = idx - s * Rs;
         lse_s[idx] = lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
     }
-    __syncthreads();
     const int tq = threadIdx.x / Q4, c = threadIdx.x - tq * Q4;
-    if (tq < nvalid) {
-        const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
-        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-        const float* src = logits + row * Rs + 4 * c;
-        const int64_t slab_stride = rows_per_slab * Rs;
-        int s = 0;
-        for (; s + 4 <= nslab; s += 4) {
-            float4 v[4];
+    const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
+    const float* src = logits + row * Rs + 4 * c;
+    const int64_t slab_stride = rows_per_slab * Rs;
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    for (int s0 = 0; s0 < nslab; s0 += kReduceSlabBatch) {
+        float4 v[kReduceSlabBatch];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s + u) * slab_stride));
+        for (int u = 0; u < kReduceSlabBatch; ++u)
+            if (tq < nvalid && s0 + u < nslab)
+                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s0 + u) * slab_stride));
+        __syncthreads();  // lse_s ready (first batch)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float* ls = lse_s + (s + u) * Rs + 4 * c;
+        for (int u = 0; u < kReduceSlabBatch; ++u) {
+            if (tq < nvalid && s0 + u < nslab) {
+                const float* ls = lse_s + (s0 + u) * Rs + 4 * c;
                 m0 = fmaxf(m0, fmaf(v[u].x, scale2, -ls[0]));
                 m1 = fmaxf(m1, fmaf(v[u].y, scale2, -ls[1]));
                 m2 = fmaxf(m2, fmaf(v[u].z, scale2, -ls[2]));
                 m3 = fmaxf(m3, fmaf(v[u].w, scale2, -ls[3]));
             }
         }
-        for (; s < nslab; ++s) {
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(src + s * slab_stride));
-            const float* ls = lse_s + s * Rs + 4 * c;
-            m0 = fmaxf(m0, fmaf(v.x, scale2, -ls[0]));
-            m1 = fmaxf(m1, fmaf(v.y, scale2, -ls[1]));
-            m2 = fmaxf(m2, fmaf(v.z, scale2, -ls[2]));
-            m3 = fmaxf(m3, fmaf(v.w, scale2, -ls[3]));
-        }
+    }
+    if (tq < nvalid) {
         float* mrow = ms + tq * (Rs + 1) + 4 * c;
         mrow[0] = m0;
         mrow[1] = m1;
@@ -204,6 +199,95 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
             else alog[l * Ntot + tok] = a;
         }
         if (last_wave) imp[tok] = total / static_cast<float>(L);
+    }
+}
+
+// --------------------------------------------------------- pool + chunk sums
+// Fused-path pooling: one CTA per 128-token tile of a prompt (chunks never
+// straddle tiles: C divides 128). Loads imp of the tile plus a W/2 halo
+// (clipped to the prompt) into shared memory with all loads in flight,
+// writes the pooled scores x, their min / max (per tile) and, per chunk,
+// S_bx = sum boost(t) * x(t) and S_b = sum boost(t) in token order.
+constexpr int kPoolThreads = 128;
+constexpr int kPoolMaxHalo = 64;
+
+__global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(
+    const float* imp, float* tok, float2* rpart, float2* csum, const int32_t* seq_off,
+    const int32_t* tile_base, const int32_t* chunk_off, int B, int W, int C, int bf_n,
+    float bf_mult, int bl_n, float bl_mult, const int32_t* bad) {
+    if (*bad) return;
+    const int64_t tile = blockIdx.x;
+    if (tile >= tile_base[B]) return;
+    __shared__ float win[kTileTokens + 2 * kPoolMaxHalo];
+    __shared__ float xs[kTileTokens];
+    __shared__ float red_mn[kPoolThreads / 32], red_mx[kPoolThreads / 32];
+    const int b = search_base(tile_base, B, tile);
+    const int64_t i = tile - tile_base[b];
+    const int64_t start = seq_off[b];
+    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    const int64_t t0 = i * kTileTokens, t1 = min64(n, t0 + kTileTokens);
+    const int h = W / 2;
+    const int64_t lo = max64(0, t0 - h), hi = min64(n, t1 + h);
+    constexpr int kWin = (kTileTokens + 2 * kPoolMaxHalo + kPoolThreads - 1) / kPoolThreads;
+    float r[kWin];
+#pragma unroll
+    for (int k = 0; k < kWin; ++k) {
+        const int64_t u = lo + threadIdx.x + k * kPoolThreads;
+        r[k] = u < hi ? imp[start + u] : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kWin; ++k) {
+        const int64_t u = lo + threadIdx.x + k * kPoolThreads;
+        if (u < hi) win[u - lo] = r[k];
+    }
+    __syncthreads();
+    float mn = INFINITY, mx = -INFINITY;
+    const int64_t tt = t0 + threadIdx.x;
+    if (tt < t1) {
+        const int64_t u0 = max64(0, tt - h), u1 = min64(n - 1, tt + h);
+        float s = 0.0f;
+        for (int64_t u = u0; u <= u1; ++u) s += win[u - lo];
+        const float x = s / static_cast<float>(u1 - u0 + 1);
+        tok[start + tt] = x;
+        xs[threadIdx.x] = x;
+        mn = x;
+        mx = x;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        red_mn[warp] = mn;
+        red_mx[warp] = mx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kPoolThreads / 32; ++w) {
+            mn = fminf(mn, red_mn[w]);
+            mx = fmaxf(mx, red_mx[w]);
+        }
+        rpart[tile] = make_float2(mn, mx);
+    }
+    const int64_t c_lo = t0 / C, c_hi = (t1 + C - 1) / C;
+    for (int64_t c = c_lo + threadIdx.x; c < c_hi; c += kPoolThreads) {
+        const int64_t a0 = c * C, a1 = min64(t1, a0 + C);
+        float sbx = 0.0f, sb = 0.0f;
+        for (int64_t t = a0; t < a1; ++t) {
+            float bx = xs[t - t0], bb = 1.0f;
+            if (t < bf_n) {
+                bx *= bf_mult;
+                bb *= bf_mult;
+            }
+            if (t >= n - bl_n) {
+                bx *= bl_mult;
+                bb *= bl_mult;
+            }
+            sbx += bx;
+            sb += bb;
+        }
+        csum[chunk_off[b] + c] = make_float2(sbx, sb);
     }
 }
 
@@ -304,20 +388,26 @@ __global__ void __launch_bounds__(256) chunk_kernel(const float* tok, const floa
         __syncthreads();
     }
     const float mn = normalize ? s_mn : 0.0f, mx = normalize ? s_mx : 0.0f;
-    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-        float y = tok[start + t];
-        if (normalize) y = (mx == mn) ? 1.0f : (y - mn) / (mx - mn);
-        if (t < bf_n) y *= bf_mult;
-        if (t >= n - bl_n) y *= bl_mult;
-        ys[t - t0] = y;
-    }
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) ys[t - t0] = tok[start + t];
     __syncthreads();
     const int64_t c0 = t0 / C, c1 = (t1 + C - 1) / C;
     for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
         const int64_t a0 = c * C, a1 = min64(t1, a0 + C);
-        float s = 0.0f;
-        for (int64_t t = a0; t < a1; ++t) s += ys[t - t0];
-        chunk_score[chunk_off[b] + c] = s / static_cast<float>(a1 - a0);
+        float sbx = 0.0f, sb = 0.0f;
+        for (int64_t t = a0; t < a1; ++t) {
+            float bx = ys[t - t0], bb = 1.0f;
+            if (t < bf_n) {
+                bx *= bf_mult;
+                bb *= bf_mult;
+            }
+            if (t >= n - bl_n) {
+                bx *= bl_mult;
+                bb *= bl_mult;
+            }
+            sbx += bx;
+            sb += bb;
+        }
+        chunk_score[chunk_off[b] + c] = chunk_score_from_sums(sbx, sb, mn, mx, normalize, a1 - a0);
     }
 }
 
@@ -406,8 +496,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* chun
                                                              float keep_p, float mass,
                                                              int force_last) {
     if (hdr->bad_input) return;
-    extern __shared__ uint8_t flags[];
-    __shared__ SelectShared ss;
+    extern __shared__ __align__(16) unsigned char dyn[];
+    SelectShared& ss = *reinterpret_cast<SelectShared*>(dyn);
+    float* sc_s = reinterpret_cast<float*>(dyn + ((sizeof(SelectShared) + 15) & ~size_t(15)));
+    uint8_t* flags = reinterpret_cast<uint8_t*>(sc_s + kMaxPromptChunks);
     const int b = blockIdx.x;
     const int64_t c0 = chunk_off[b];
     const int64_t nc = static_cast<int64_t>(chunk_off[b + 1]) - c0;
@@ -416,9 +508,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* chun
         return;
     }
     if (nc == 0) return;
-    for (int64_t i = threadIdx.x; i < nc; i += kSelThreads) flags[i] = 0;
+    for (int64_t i = threadIdx.x; i < nc; i += kSelThreads) {
+        flags[i] = 0;
+        sc_s[i] = chunk_score[c0 + i];
+    }
     __syncthreads();
-    radix_select(chunk_score + c0, nc, mode, keep_p, mass, flags, ss);
+    radix_select(sc_s, nc, mode, keep_p, mass, flags, ss);
     __syncthreads();
     if (force_last && threadIdx.x == 0) flags[nc - 1] |= 2;
     __syncthreads();
@@ -499,12 +594,27 @@ cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int 
     const int tok = kReduceThreads / (pl.Rs / 4);
     const size_t smem = sizeof(float) * (static_cast<size_t>(nslab) * pl.Rs +
                                          static_cast<size_t>(tok) * (pl.Rs + 1));
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
     const unsigned grid = static_cast<unsigned>(pl.tiles_max * (kTileTokens / tok));
     reduce_kernel<<<grid, kReduceThreads, smem, st>>>(
         ws_ptr<float>(ws, pl.o_logits), ws_ptr<float>(ws, pl.o_lse), seq_off,
         ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
         pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.scale2, wave == 0 ? 1 : 0,
         wave == pl.waves - 1 ? 1 : 0, &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool_sums(const Plan& pl, const sp_params* p, const int32_t* seq_off,
+                             const float* imp, float* tok, void* ws, cudaStream_t st) {
+    pool_sums_kernel<<<static_cast<unsigned>(pl.tiles_max), kPoolThreads, 0, st>>>(
+        imp, tok, ws_ptr<float2>(ws, pl.o_rpart), ws_ptr<float2>(ws, pl.o_csum), seq_off,
+        ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<int32_t>(ws, pl.o_chunk_off), pl.B, p->pool_w,
+        pl.C, p->boost_first_n, p->boost_first_mult, p->boost_last_n, p->boost_last_mult,
+        &ws_ptr<WsHeader>(ws, 0)->bad_input);
     return cudaGetLastError();
 }
 
@@ -547,7 +657,11 @@ cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq
     (void)kept_off;
     (void)n_kept;
     const int64_t max_nc = (pl.Ntot + pl.C - 1) / pl.C;
-    const size_t smem = static_cast<size_t>(max_nc < kMaxPromptChunks ? max_nc : kMaxPromptChunks);
+    (void)max_nc;
+    const size_t smem = ((sizeof(SelectShared) + 15) & ~size_t(15)) + static_cast<size_t>(kMaxPromptChunks) * 5;
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     select_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, smem, st>>>(
         chunk_off, chunk_score, keep, ws_ptr<WsHeader>(ws, 0), p->mode, p->keep_p, p->mass,
         p->force_last_chunk);
