@@ -37,12 +37,12 @@ namespace {
 constexpr int kPostThreads = kSelectThreads;
 
 struct PostArgs {
-    const int32_t* seq_off;
+    const int32_t* __restrict__ seq_off;
     const int32_t* chunk_off;  // workspace copy
     const int32_t* tile_base;
     const float2* rpart;       // per pool CTA (min, max) of the pooled scores
-    const float2* csum;        // per chunk (sum boost * x, sum boost)
-    float* chunk_score;
+    const float2* __restrict__ csum;  // per chunk (sum boost * x, sum boost)
+    float* __restrict__ chunk_score;
     uint8_t* keep;
     int32_t* ckoff;
     int32_t* pcount;
@@ -171,39 +171,50 @@ __global__ void __launch_bounds__(kPostThreads) post_kernel(const PostArgs a) {
             mn = s_mn;
             mx = s_mx;
         }
-        // chunk scores from the per-chunk sums of the reduce kernel
-        for (int64_t c = t; c < nc; c += kPostThreads) {
-            const float2 v = a.csum[coff + c];
-            const float cs = chunk_score_from_sums(v.x, v.y, mn, mx, a.normalize,
-                                                   min64(a.C, n - c * a.C));
-            cs_s[c] = cs;
-            a.chunk_score[coff + c] = cs;
+        // chunk scores from the per-chunk sums (all of a thread's loads first)
+        for (int64_t c0 = t; c0 < nc; c0 += kPostThreads * 8) {
+            float2 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int64_t c = c0 + k * kPostThreads;
+                v[k] = c < nc ? a.csum[coff + c] : make_float2(0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int64_t c = c0 + k * kPostThreads;
+                if (c < nc) {
+                    const float cs = chunk_score_from_sums(v[k].x, v[k].y, mn, mx, a.normalize,
+                                                           min64(a.C, n - c * a.C));
+                    cs_s[c] = cs;
+                    a.chunk_score[coff + c] = cs;
+                }
+            }
         }
         for (int64_t c = t; c < nc; c += kPostThreads) flags[c] = 0;
         __syncthreads();
         radix_select(cs_s, nc, a.mode, a.keep_p, a.mass, flags, ss);
         __syncthreads();
         if (a.force_last && t == 0) flags[nc - 1] |= 2;
-        if (t == 0) carry = 0;
         __syncthreads();
         for (int64_t c = t; c < nc; c += kPostThreads) a.keep[coff + c] = flags[c];
-        // kept tokens per chunk and their exclusive scan, in chunk order
-        for (int64_t base = 0; base < nc; base += kPostThreads) {
-            const int64_t c = base + t;
-            int64_t cnt = 0;
-            if (c < nc) {
-                const int64_t size = min64(a.C, n - c * a.C);
-                cnt = flags[c] ? size : ((c == 0 && a.force_bos && n > 0) ? 1 : 0);
-            }
-            const int64_t incl = block_scan_i64(cnt, scan_i);
-            if (c < nc) {
-                const int32_t o = static_cast<int32_t>(carry + incl - cnt);
-                a.ckoff[coff + c] = o;
-            }
-            __syncthreads();
-            if (t == kPostThreads - 1) carry += incl;
-            __syncthreads();
+        // kept tokens per chunk and their exclusive scan, in chunk order:
+        // thread t owns chunks [t*E, t*E + E), one block scan of the totals
+        const int64_t E = (nc + kPostThreads - 1) / kPostThreads;
+        const int64_t c_lo = min64(nc, static_cast<int64_t>(t) * E), c_hi = min64(nc, c_lo + E);
+        int64_t mine = 0;
+        for (int64_t c = c_lo; c < c_hi; ++c) {
+            const int64_t size = min64(a.C, n - c * a.C);
+            mine += flags[c] ? size : ((c == 0 && a.force_bos && n > 0) ? 1 : 0);
         }
+        const int64_t incl = block_scan_i64(mine, scan_i);
+        int64_t run = incl - mine;
+        for (int64_t c = c_lo; c < c_hi; ++c) {
+            const int64_t size = min64(a.C, n - c * a.C);
+            a.ckoff[coff + c] = static_cast<int32_t>(run);
+            run += flags[c] ? size : ((c == 0 && a.force_bos && n > 0) ? 1 : 0);
+        }
+        if (t == kPostThreads - 1) carry = incl;
+        __syncthreads();
         count = carry;
     }
     finish_batch(a, b, count, scan_i);

@@ -55,6 +55,8 @@ struct SelectShared {
     unsigned wcnt[32];
     float wmax[32];
     int digit;
+    unsigned long long need_b;   // fixed: rank to find; mass: ceil(theta) (integer threshold)
+    int all_b;
     unsigned cnt_before;
     unsigned long long sum_before;
     int found;
@@ -72,10 +74,11 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
     const int64_t c_lo = static_cast<int64_t>(t) * E;
     const int64_t c_hi = c_lo + E < nc ? c_lo + E : nc;
     const bool is_mass = mode == SP_MODE_MASS;
+    // GB300 runs FP64 at a small fraction of the FP32 rate: the few float64
+    // operations (k = ceil(nc * p), theta = mass * total) run in one thread
+    // and every comparison afterwards is an integer one (for an integer
+    // running sum, cum >= theta <=> cum >= ceil(theta)).
     int S = 0;
-    double theta = 0.0;
-    uint64_t need = 0;
-    bool all = false;
     if (is_mass) {
         float mx = 0.0f;
         for (int64_t c = c_lo; c < c_hi; ++c) mx = fmaxf(mx, scores[c]);
@@ -103,18 +106,18 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
         if (t == 0) {
             unsigned long long tot = 0;
             for (int w = 0; w < kSelectWarps; ++w) tot += sm.wtot[w];
-            sm.total = tot;
+            sm.all_b = tot == 0 ? 1 : 0;
+            sm.need_b = static_cast<unsigned long long>(ceil(static_cast<double>(mass) * static_cast<double>(tot)));
         }
-        __syncthreads();
-        const uint64_t total = sm.total;
-        if (total == 0) all = true;
-        theta = static_cast<double>(mass) * static_cast<double>(total);
-    } else {
+    } else if (t == 0) {
         const double kk = ceil(static_cast<double>(nc) * static_cast<double>(keep_p));
-        int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
-        need = static_cast<uint64_t>(k > nc ? nc : k);
+        const int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
+        sm.need_b = static_cast<unsigned long long>(k > nc ? nc : k);
+        sm.all_b = 0;
     }
-
+    __syncthreads();
+    uint64_t need = sm.need_b;     // fixed: rank; mass: integer threshold
+    bool all = sm.all_b != 0;
     uint32_t prefix = 0, pmask = 0;
     uint64_t base_sum = 0;  // mass: fixed-point sum of all keys below the current bucket
     unsigned final_ties = 0;
@@ -179,7 +182,7 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
                 const unsigned c = sm.cnt[d];
                 const unsigned long long sv = sm.sum[d];
                 bool reach;
-                if (is_mass) reach = c > 0 && static_cast<double>(base_sum + sb + sv) >= theta;
+                if (is_mass) reach = c > 0 && base_sum + sb + sv >= need;
                 else reach = static_cast<uint64_t>(cb) + c >= need;
                 if (hit < 0 && reach) {
                     hit = d;
@@ -269,7 +272,7 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
         const uint32_t key = score_desc_key(scores[c]);
         bool keep = key < prefix;
         if (key == prefix) {
-            if (is_mass) keep = static_cast<double>(base_sum + tie_sum_before) < theta;
+            if (is_mass) keep = base_sum + tie_sum_before < need;
             else keep = tie_before < need;
             ++tie_before;
             if (is_mass) tie_sum_before += fixed_point(scores[c], S);
