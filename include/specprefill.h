@@ -115,6 +115,11 @@ typedef struct sp_profile {
     sp_event_t logits_stop;
 } sp_profile;
 
+/* Number of kernels one sp_specprefill_score call with this shape and these
+ * parameters launches on its stream (all of them this library's own), so a
+ * caller can account for the launches it issues. */
+int sp_kernels_per_call(const sp_shape* shape, const sp_params* params, int32_t* n_kernels);
+
 /* Upper bound on the number of chunks of a packed batch:
  * floor(Ntot / chunk) + B. Chunk arrays must hold this many entries. */
 int sp_max_chunks(const sp_shape* shape, const sp_params* params, int64_t* n_chunks);

@@ -121,6 +121,7 @@ def load(path: Optional[str] = None):
     i32 = ctypes.c_int
     sigs = {
         "sp_max_chunks": [sp, pp, ctypes.POINTER(ctypes.c_int64)],
+        "sp_kernels_per_call": [sp, pp, ctypes.POINTER(i32)],
         "sp_workspace_size": [sp, pp, ctypes.POINTER(_SZ)],
         "sp_workspace_init": [_P, _SZ, _P],
         "sp_attn_importance": [sp, pp, _P, _P, _P, _P, _P, _SZ, _P],
@@ -204,6 +205,14 @@ def max_chunks(shape: _Shape, params: SelectionParams) -> int:
     n = ctypes.c_int64()
     _check(lib().sp_max_chunks(ctypes.byref(shape), ctypes.byref(params._c()), ctypes.byref(n)),
            "sp_max_chunks")
+    return int(n.value)
+
+
+def kernels_per_call(shape: _Shape, params: SelectionParams) -> int:
+    """Kernels one specprefill_score call launches (all of them this library's)."""
+    n = ctypes.c_int()
+    _check(lib().sp_kernels_per_call(ctypes.byref(shape), ctypes.byref(params._c()),
+                                     ctypes.byref(n)), "sp_kernels_per_call")
     return int(n.value)
 
 

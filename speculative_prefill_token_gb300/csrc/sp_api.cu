@@ -206,6 +206,17 @@ int sp_max_chunks(const sp_shape* shape, const sp_params* params, int64_t* n_chu
     return SP_OK;
 }
 
+int sp_kernels_per_call(const sp_shape* shape, const sp_params* params, int32_t* n_kernels) {
+    Plan pl;
+    const int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!n_kernels) return SP_ERR_INVALID_ARG;
+    // prep, (logits, reduce) per wave, pool sums + post or pool, chunk,
+    // select, gather scan; then the gather write
+    *n_kernels = 1 + 2 * pl.waves + (fused_post_ok(params) ? 2 : 4) + 1;
+    return SP_OK;
+}
+
 int sp_workspace_size(const sp_shape* shape, const sp_params* params, size_t* bytes) {
     Plan pl;
     const int rc = make_plan(shape, params, &pl);

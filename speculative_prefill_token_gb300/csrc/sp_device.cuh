@@ -6,6 +6,19 @@
 
 namespace sp {
 
+// Programmatic dependent launch. grid_dep_wait() returns once the kernel
+// that precedes this one in the stream has completed and its memory writes
+// are visible (that kernel itself waited for its predecessor, so everything
+// earlier in the stream is complete too); without the launch attribute it
+// returns at once. grid_dep_launch() lets the next kernel of the stream be
+// scheduled: its CTAs may become resident early and then block in their own
+// grid_dep_wait(). Every kernel of this library calls both before its first
+// global-memory access.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Butterfly reduction of 32 rows held by every lane (v[r] = row r of this
 // lane's token): afterwards v[0] of lane r holds op over the 32 lanes of
 // row r. 31 shuffles instead of 32 separate 5-step reductions.

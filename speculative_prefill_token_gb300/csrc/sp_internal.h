@@ -119,6 +119,26 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
                         int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept,
                         void* ws, cudaStream_t st);
 
+// Launch with programmatic stream serialisation: the kernel may be
+// scheduled while its predecessor in the stream is still running and waits
+// for it in grid_dep_wait() (every kernel of this library does so before
+// touching global memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 template <typename T>
 inline T* ws_ptr(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);

@@ -38,6 +38,8 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 // One work item (tile of one slab) per CTA; CTAs past the last item exit.
 template <int NH>
 __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*a.bad) return;
     constexpr int RMAX = 32 * NH;
     const int64_t T = a.tile_base[a.B];
@@ -159,8 +161,7 @@ cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t*
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, 128, sm, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(kern, grid, 128, sm, st, a);
 }
 
 }  // namespace sp

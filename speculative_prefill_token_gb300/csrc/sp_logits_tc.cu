@@ -125,7 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
-    if (*a.bad) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -186,7 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int64_t T = a.tile_base[a.B];
+    // everything above touched only this CTA's shared and tensor memory; the
+    // offsets and counters below come from the preceding kernel
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t T = *a.bad ? 0 : a.tile_base[a.B];  // invalid offsets: no work, normal teardown
     const int64_t W = T * a.nslab;
     const int64_t C = gridDim.x;
     const int64_t w_begin = split_start(W, C, blockIdx.x);
@@ -520,8 +523,7 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, smem, st>>>(tk, tq, ts, a);
-    return cudaGetLastError();
+    return launch_k(kern, grid, kThreads, smem, st, tk, tq, ts, a);
 }
 
 }  // namespace sp

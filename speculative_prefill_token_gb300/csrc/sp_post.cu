@@ -120,6 +120,8 @@ __device__ void finish_batch(const PostArgs& a, int b, int64_t count, int64_t* s
 }
 
 __global__ void __launch_bounds__(kPostThreads) post_kernel(const PostArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (a.hdr->bad_input) return;
     extern __shared__ __align__(16) unsigned char dyn[];
     // [SelectShared][max nc floats: chunk scores][max nc flag bytes]
@@ -260,8 +262,7 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
     cudaError_t e = cudaFuncSetAttribute(post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    post_kernel<<<static_cast<unsigned>(pl.B), kPostThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_k(post_kernel, static_cast<unsigned>(pl.B), kPostThreads, smem, st, a);
 }
 
 }  // namespace sp

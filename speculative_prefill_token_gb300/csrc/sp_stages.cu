@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
                                                             const int32_t* chunk_off_check,
                                                             unsigned* seg_cnt, int64_t n_seg_cnt,
                                                             WsHeader* hdr) {
+    grid_dep_wait();
+    grid_dep_launch();
     __shared__ int bad;
     __shared__ int64_t warp_sums[3][32];
     const int tid = threadIdx.x;
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     const float* logits, const float* lse2, const int32_t* seq_off, const int32_t* tile_base,
     float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab, int64_t Ntot,
     int64_t rows_per_slab, float scale2, int first_wave, int last_wave, const int32_t* bad) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*bad) return;
     const int Q4 = Rs / 4;
     const int TOK = kReduceThreads / Q4;
@@ -215,6 +219,8 @@ __global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(
     const float* imp, float* tok, float2* rpart, float2* csum, const int32_t* seq_off,
     const int32_t* tile_base, const int32_t* chunk_off, int B, int W, int C, int bf_n,
     float bf_mult, int bl_n, float bl_mult, const int32_t* bad) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*bad) return;
     const int64_t tile = blockIdx.x;
     if (tile >= tile_base[B]) return;
@@ -297,6 +303,8 @@ __global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(
 __global__ void __launch_bounds__(256) pool_kernel(const float* imp, float* tok, float2* ppart,
                                                    const int32_t* seq_off, const int32_t* pblk_base,
                                                    int B, int W, int64_t Tb, const int32_t* bad) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*bad) return;
     const int64_t blk = blockIdx.x;
     if (blk >= pblk_base[B]) return;
@@ -349,6 +357,8 @@ __global__ void __launch_bounds__(256) chunk_kernel(const float* tok, const floa
                                                     int B, int C, int64_t Tb, int normalize,
                                                     float bf_mult, int bf_n, float bl_mult, int bl_n,
                                                     const int32_t* bad) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*bad) return;
     const int64_t blk = blockIdx.x;
     if (blk >= pblk_base[B]) return;
@@ -495,6 +505,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* chun
                                                              uint8_t* keep, WsHeader* hdr, int mode,
                                                              float keep_p, float mass,
                                                              int force_last) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (hdr->bad_input) return;
     extern __shared__ __align__(16) unsigned char dyn[];
     SelectShared& ss = *reinterpret_cast<SelectShared*>(dyn);
@@ -524,6 +536,8 @@ __global__ void __launch_bounds__(kSelThreads) gather_scan_kernel(
     const int32_t* seq_off, const int32_t* chunk_off, const uint8_t* keep, int32_t* ckoff,
     int32_t* pcount, int32_t* kept_off, int32_t* n_kept, WsHeader* hdr, int B, int C,
     int force_bos) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (hdr->bad_input) return;
     __shared__ int64_t scan_i[32];
     const int b = blockIdx.x;
@@ -540,6 +554,8 @@ __global__ void __launch_bounds__(256) gather_write_kernel(
     const int32_t* seq_off, const int32_t* chunk_off, const uint8_t* keep, const int32_t* ckoff,
     const int32_t* kept_off, int32_t* kept_idx, int32_t* kept_pos, int B, int C, int force_bos,
     const int32_t* bad) {
+    grid_dep_wait();
+    grid_dep_launch();
     if (*bad) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t cg = static_cast<int64_t>(blockIdx.x) * 8 + warp;
@@ -567,26 +583,24 @@ __global__ void __launch_bounds__(256) gather_write_kernel(
 
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
                         cudaStream_t st) {
-    prep_kernel<<<1, kPrepThreads, 0, st>>>(seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
-                                            ws_ptr<int32_t>(ws, pl.o_tile_base),
-                                            ws_ptr<int32_t>(ws, pl.o_chunk_off),
-                                            ws_ptr<int32_t>(ws, pl.o_pblk_base), chunk_off_out,
-                                            nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
-                                            static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
-                                            ws_ptr<WsHeader>(ws, 0));
-    return cudaGetLastError();
+    return launch_k(prep_kernel, 1, kPrepThreads, 0, st, seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
+        ws_ptr<int32_t>(ws, pl.o_tile_base),
+        ws_ptr<int32_t>(ws, pl.o_chunk_off),
+        ws_ptr<int32_t>(ws, pl.o_pblk_base), chunk_off_out,
+        nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
+        static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+        ws_ptr<WsHeader>(ws, 0));
 }
 
 cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
                               const int32_t* chunk_off_check, cudaStream_t st) {
-    prep_kernel<<<1, kPrepThreads, 0, st>>>(seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
-                                            ws_ptr<int32_t>(ws, pl.o_tile_base),
-                                            ws_ptr<int32_t>(ws, pl.o_chunk_off),
-                                            ws_ptr<int32_t>(ws, pl.o_pblk_base), nullptr,
-                                            chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
-                                            static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
-                                            ws_ptr<WsHeader>(ws, 0));
-    return cudaGetLastError();
+    return launch_k(prep_kernel, 1, kPrepThreads, 0, st, seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
+        ws_ptr<int32_t>(ws, pl.o_tile_base),
+        ws_ptr<int32_t>(ws, pl.o_chunk_off),
+        ws_ptr<int32_t>(ws, pl.o_pblk_base), nullptr,
+        chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
+        static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+        ws_ptr<WsHeader>(ws, 0));
 }
 
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
@@ -600,22 +614,20 @@ cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int 
         if (e != cudaSuccess) return e;
     }
     const unsigned grid = static_cast<unsigned>(pl.tiles_max * (kTileTokens / tok));
-    reduce_kernel<<<grid, kReduceThreads, smem, st>>>(
+    return launch_k(reduce_kernel, grid, kReduceThreads, smem, st,
         ws_ptr<float>(ws, pl.o_logits), ws_ptr<float>(ws, pl.o_lse), seq_off,
         ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
         pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.scale2, wave == 0 ? 1 : 0,
         wave == pl.waves - 1 ? 1 : 0, &ws_ptr<WsHeader>(ws, 0)->bad_input);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_pool_sums(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                              const float* imp, float* tok, void* ws, cudaStream_t st) {
-    pool_sums_kernel<<<static_cast<unsigned>(pl.tiles_max), kPoolThreads, 0, st>>>(
+    return launch_k(pool_sums_kernel, static_cast<unsigned>(pl.tiles_max), kPoolThreads, 0, st,
         imp, tok, ws_ptr<float2>(ws, pl.o_rpart), ws_ptr<float2>(ws, pl.o_csum), seq_off,
         ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<int32_t>(ws, pl.o_chunk_off), pl.B, p->pool_w,
         pl.C, p->boost_first_n, p->boost_first_mult, p->boost_last_n, p->boost_last_mult,
         &ws_ptr<WsHeader>(ws, 0)->bad_input);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_off,
@@ -626,10 +638,9 @@ cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_o
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    pool_kernel<<<static_cast<unsigned>(pl.pblk_max), 256, smem, st>>>(
+    return launch_k(pool_kernel, static_cast<unsigned>(pl.pblk_max), 256, smem, st,
         imp, tok, ws_ptr<float2>(ws, pl.o_ppart), seq_off, ws_ptr<int32_t>(ws, pl.o_pblk_base),
         pl.B, p->pool_w, pl.Tb, &ws_ptr<WsHeader>(ws, 0)->bad_input);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_chunk(const Plan& pl, const sp_params* p, const int32_t* seq_off,
@@ -640,12 +651,11 @@ cudaError_t launch_chunk(const Plan& pl, const sp_params* p, const int32_t* seq_
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    chunk_kernel<<<static_cast<unsigned>(pl.pblk_max), 256, smem, st>>>(
+    return launch_k(chunk_kernel, static_cast<unsigned>(pl.pblk_max), 256, smem, st,
         tok, ws_ptr<float2>(ws, pl.o_ppart), chunk_score, seq_off,
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_chunk_off), pl.B, pl.C, pl.Tb,
         p->normalize, p->boost_first_mult, p->boost_first_n, p->boost_last_mult, p->boost_last_n,
         &ws_ptr<WsHeader>(ws, 0)->bad_input);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq_off,
@@ -662,19 +672,17 @@ cudaError_t launch_select(const Plan& pl, const sp_params* p, const int32_t* seq
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    select_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, smem, st>>>(
+    return launch_k(select_kernel, static_cast<unsigned>(pl.B), kSelThreads, smem, st,
         chunk_off, chunk_score, keep, ws_ptr<WsHeader>(ws, 0), p->mode, p->keep_p, p->mass,
         p->force_last_chunk);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_scan(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                                const int32_t* chunk_off, const uint8_t* keep, void* ws,
                                int32_t* kept_off, int32_t* n_kept, cudaStream_t st) {
-    gather_scan_kernel<<<static_cast<unsigned>(pl.B), kSelThreads, 0, st>>>(
+    return launch_k(gather_scan_kernel, static_cast<unsigned>(pl.B), kSelThreads, 0, st,
         seq_off, chunk_off, keep, ws_ptr<int32_t>(ws, pl.o_ckoff), ws_ptr<int32_t>(ws, pl.o_pcount),
         kept_off, n_kept, ws_ptr<WsHeader>(ws, 0), pl.B, pl.C, p->force_bos);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_t* seq_off,
@@ -683,10 +691,9 @@ cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_
                                 cudaStream_t st) {
     (void)n_kept;
     const unsigned grid = static_cast<unsigned>((pl.chunks_max + 7) / 8);
-    gather_write_kernel<<<grid, 256, 0, st>>>(seq_off, chunk_off, keep, ws_ptr<int32_t>(ws, pl.o_ckoff),
-                                              kept_off, kept_idx, kept_pos, pl.B, pl.C, p->force_bos,
-                                              &ws_ptr<WsHeader>(ws, 0)->bad_input);
-    return cudaGetLastError();
+    return launch_k(gather_write_kernel, grid, 256, 0, st, seq_off, chunk_off, keep,
+                    ws_ptr<int32_t>(ws, pl.o_ckoff), kept_off, kept_idx, kept_pos, pl.B, pl.C,
+                    p->force_bos, &ws_ptr<WsHeader>(ws, 0)->bad_input);
 }
 
 }  // namespace sp

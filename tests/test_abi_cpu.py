@@ -73,6 +73,17 @@ def test_workspace_size_valid(lib):
     assert n >= 12 * 32768 * 32 * 4
 
 
+def test_kernels_per_call(lib):
+    # one wave of 12 slabs: prep, logits, reduce, pool sums, post, gather write
+    assert sp.kernels_per_call(_shape(), sp.SelectionParams(mode="fixed", keep_p=0.15)) == 6
+    # a pool window wider than the fused kernel's halo takes the staged path
+    # (pool, chunk, select, gather scan instead of pool sums + post)
+    assert sp.kernels_per_call(_shape(), sp.SelectionParams(pool_w=201)) == 8
+    n = ctypes.c_int()
+    assert lib.sp_kernels_per_call(ctypes.byref(_shape(head_dim=96)),
+                                   ctypes.byref(sp.SelectionParams()._c()), ctypes.byref(n)) == 2
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=96), 2),          # unsupported head_dim
     (dict(n_q_heads=6, n_kv_heads=4), 1),  # Hq not a multiple of Hk
