@@ -100,6 +100,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.chunks_max = P.Ntot / P.C + P.B;
     P.Tb = P.C <= kPostBlockTarget ? static_cast<int64_t>(P.C) * (kPostBlockTarget / P.C) : P.C;
     P.pblk_max = P.Ntot / P.Tb + P.B;
+    P.slices_max = P.chunks_max / kSliceChunks + P.B;
     int64_t maxnc = (P.Ntot + P.C - 1) / P.C;
     if (maxnc > kMaxPromptChunks) maxnc = kMaxPromptChunks;
     P.sort_cap = 1;
@@ -128,6 +129,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_tile_base = take(B1 * 4);
     P.o_chunk_off = take(B1 * 4);
     P.o_pblk_base = take(B1 * 4);
+    P.o_slice_base = take(B1 * 4);
+    P.o_scount = take(static_cast<size_t>(P.slices_max) * 4);
     P.o_segcnt = take(static_cast<size_t>(P.slabs_per_wave) * P.B * 4);
     P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 4);
     P.o_part = take(static_cast<size_t>(P.rec_slots) * P.Rs * 8);
@@ -211,9 +214,9 @@ int sp_kernels_per_call(const sp_shape* shape, const sp_params* params, int32_t*
     const int rc = make_plan(shape, params, &pl);
     if (rc != SP_OK) return rc;
     if (!n_kernels) return SP_ERR_INVALID_ARG;
-    // prep, (logits, reduce) per wave, pool sums + post or pool, chunk,
-    // select, gather scan; then the gather write
-    *n_kernels = 1 + 2 * pl.waves + (fused_post_ok(params) ? 2 : 4) + 1;
+    // prep, (logits, reduce) per wave, then pool sums, rank, gather or
+    // pool, chunk, select, gather scan, gather write
+    *n_kernels = 1 + 2 * pl.waves + (fused_post_ok(params) ? 3 : 5);
     return SP_OK;
 }
 
@@ -317,9 +320,8 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
     if (fused_post_ok(params)) {
         if (launch_pool_sums(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess)
             return SP_ERR_CUDA;
-        if (launch_post(pl, params, seq_off, imp_p, tok_p, cs_p, keep_p, kept_idx, kept_pos,
-                        kept_off, n_kept, ws, st) != cudaSuccess)
-            return SP_ERR_CUDA;
+        return to_status(launch_post(pl, params, seq_off, cs_p, keep_p, kept_idx, kept_pos, kept_off,
+                                     n_kept, ws, st));
     } else {
         if (launch_pool(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
         if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;

@@ -16,7 +16,8 @@ constexpr int kPostBlockTarget = 1024;
 constexpr int kMaxSeqs = 65536;
 constexpr int kMaxChunk = 8192;
 constexpr int kMaxPool = 8191;
-constexpr int kMaxPromptChunks = 16384;  // per-prompt chunk count the in-CTA sort handles
+constexpr int kMaxPromptChunks = 16384;  // per-prompt chunk count the in-CTA selection handles
+constexpr int kSliceChunks = 32;         // chunks per CTA of the fused rank / gather kernels
 constexpr int64_t kDefaultSpin = int64_t(1) << 22;  // ~4 s of polls with a 1 us suspend hint
 
 // Workspace header (first 256 bytes of every workspace).
@@ -39,12 +40,13 @@ struct Plan {
     int C, W;
     int64_t Tb;           // tokens per post-processing block (multiple of C)
     int64_t pblk_max;     // >= sum_b ceil(n_b / Tb)
+    int64_t slices_max;   // >= sum_b ceil(ceil(n_b / C) / kSliceChunks)
     int sort_cap;         // power of two >= max chunks of one prompt
     int slabs_per_wave, waves;
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
     // workspace offsets (bytes)
-    size_t o_tile_base, o_chunk_off, o_pblk_base, o_segcnt, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
+    size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
         o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
 };
@@ -111,13 +113,12 @@ cudaError_t launch_gather_write(const Plan& pl, const sp_params* p, const int32_
                                 int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
                                 cudaStream_t st);
 
-// Fused per-prompt post-processing (pool, normalise, boost, chunk means,
-// selection, kept counts; kept lists too when the batch has one prompt),
-// one 8-CTA cluster per prompt.
+// Fused post-processing after launch_pool_sums: the rank kernel (chunk
+// scores, selection, force-last, kept tokens per 32-chunk slice) and the
+// gather kernel (kept lists, per-prompt offsets, total), one CTA per slice.
 cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_off,
-                        const float* imp, float* tok, float* chunk_score, uint8_t* keep,
-                        int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept,
-                        void* ws, cudaStream_t st);
+                        float* chunk_score, uint8_t* keep, int32_t* kept_idx, int32_t* kept_pos,
+                        int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st);
 
 // Launch with programmatic stream serialisation: the kernel may be
 // scheduled while its predecessor in the stream is still running and waits

@@ -46,6 +46,30 @@ __device__ __forceinline__ uint64_t fixed_point(float f, int S) {
     return (m + (uint64_t(1) << (-sh - 1))) >> (-sh);
 }
 
+// Fixed mode: k = max(1, ceil(nc * p)), at most nc (float64, as the
+// oracle's definition; one thread).
+__device__ __forceinline__ uint64_t fixed_keep_count(int64_t nc, float keep_p) {
+    const double kk = ceil(static_cast<double>(nc) * static_cast<double>(keep_p));
+    const int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
+    return static_cast<uint64_t>(k > nc ? nc : k);
+}
+
+// Mass mode: the power-of-two scale S of the fixed-point scores, from the
+// prompt's largest score, so that the sum of nc scores stays below 2^52.
+__device__ __forceinline__ int mass_scale(int64_t nc, float smax) {
+    if (!(smax > 0.0f)) return 0;
+    int lg = 0;
+    while ((int64_t(1) << lg) < nc + 1) ++lg;
+    const int e_max = static_cast<int>((__float_as_uint(smax) >> 23) & 0xff) - 127;  // floor(log2)
+    return 52 - (e_max + 1) - lg;
+}
+
+// Mass mode: integer threshold ceil(mass * total); for an integer running
+// sum, cum >= mass * total <=> cum >= ceil(mass * total).
+__device__ __forceinline__ uint64_t mass_threshold(uint64_t total, float mass) {
+    return static_cast<uint64_t>(ceil(static_cast<double>(mass) * static_cast<double>(total)));
+}
+
 struct SelectShared {
     unsigned wcnt_h[kSelectWarps][256];            // per-warp histograms
     unsigned long long wsum_h[kSelectWarps][256];
@@ -91,13 +115,7 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
             sm.smax = m;
         }
         __syncthreads();
-        const float smax = sm.smax;
-        if (smax > 0.0f) {
-            int lg = 0;
-            while ((int64_t(1) << lg) < nc + 1) ++lg;
-            const int e_max = static_cast<int>((__float_as_uint(smax) >> 23) & 0xff) - 127;  // floor(log2)
-            S = 52 - (e_max + 1) - lg;
-        }
+        S = mass_scale(nc, sm.smax);
         uint64_t part = 0;
         for (int64_t c = c_lo; c < c_hi; ++c) part += fixed_point(scores[c], S);
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -107,12 +125,10 @@ __device__ __forceinline__ void radix_select(const float* scores, int64_t nc, in
             unsigned long long tot = 0;
             for (int w = 0; w < kSelectWarps; ++w) tot += sm.wtot[w];
             sm.all_b = tot == 0 ? 1 : 0;
-            sm.need_b = static_cast<unsigned long long>(ceil(static_cast<double>(mass) * static_cast<double>(tot)));
+            sm.need_b = mass_threshold(tot, mass);
         }
     } else if (t == 0) {
-        const double kk = ceil(static_cast<double>(nc) * static_cast<double>(keep_p));
-        const int64_t k = kk < 1.0 ? 1 : static_cast<int64_t>(kk);
-        sm.need_b = static_cast<unsigned long long>(k > nc ? nc : k);
+        sm.need_b = fixed_keep_count(nc, keep_p);
         sm.all_b = 0;
     }
     __syncthreads();

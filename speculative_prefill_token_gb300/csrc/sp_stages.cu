@@ -36,14 +36,15 @@ constexpr int kPrepThreads = 1024;
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_off, int B,
                                                             int64_t Ntot, int C, int64_t Tb,
                                                             int32_t* tile_base, int32_t* chunk_off,
-                                                            int32_t* pblk_base, int32_t* chunk_off_out,
+                                                            int32_t* pblk_base, int32_t* slice_base,
+                                                            int32_t* chunk_off_out,
                                                             const int32_t* chunk_off_check,
                                                             unsigned* seg_cnt, int64_t n_seg_cnt,
                                                             WsHeader* hdr) {
     grid_dep_wait();
     grid_dep_launch();
     __shared__ int bad;
-    __shared__ int64_t warp_sums[3][32];
+    __shared__ int64_t warp_sums[4][32];
     const int tid = threadIdx.x;
     if (tid == 0) {
         bad = (seq_off[0] != 0 || static_cast<int64_t>(seq_off[B]) != Ntot) ? 1 : 0;
@@ -56,20 +57,21 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
     __syncthreads();
     const int per = (B + kPrepThreads - 1) / kPrepThreads;
     const int lo = min(B, tid * per), hi = min(B, lo + per);
-    int64_t sums[3] = {0, 0, 0};
+    int64_t sums[4] = {0, 0, 0, 0};
     if (!bad) {
         for (int b = lo; b < hi; ++b) {
             const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
             sums[0] += (n + kTileTokens - 1) / kTileTokens;
             sums[1] += (n + C - 1) / C;
             sums[2] += (n + Tb - 1) / Tb;
+            sums[3] += ((n + C - 1) / C + kSliceChunks - 1) / kSliceChunks;
         }
     }
     // block exclusive scan of the three per-thread totals
     const int lane = tid & 31, warp = tid >> 5;
-    int64_t incl[3];
+    int64_t incl[4];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
+    for (int k = 0; k < 4; ++k) {
         int64_t v = sums[k];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
+        for (int k = 0; k < 4; ++k) {
             int64_t v = warp_sums[k][lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -93,24 +95,27 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
         }
     }
     __syncthreads();
-    int64_t run[3];
+    int64_t run[4];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) run[k] = incl[k] - sums[k] + (warp > 0 ? warp_sums[k][warp - 1] : 0);
+    for (int k = 0; k < 4; ++k) run[k] = incl[k] - sums[k] + (warp > 0 ? warp_sums[k][warp - 1] : 0);
     for (int b = lo; b < hi; ++b) {
         const int64_t n = bad ? 0 : static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
         tile_base[b] = static_cast<int32_t>(run[0]);
         chunk_off[b] = static_cast<int32_t>(run[1]);
         pblk_base[b] = static_cast<int32_t>(run[2]);
+        slice_base[b] = static_cast<int32_t>(run[3]);
         if (chunk_off_out) chunk_off_out[b] = static_cast<int32_t>(run[1]);
         if (chunk_off_check && chunk_off_check[b] != static_cast<int32_t>(run[1])) bad = 1;
         run[0] += (n + kTileTokens - 1) / kTileTokens;
         run[1] += (n + C - 1) / C;
         run[2] += (n + Tb - 1) / Tb;
+        run[3] += ((n + C - 1) / C + kSliceChunks - 1) / kSliceChunks;
     }
     if (hi == B && lo < hi) {
         tile_base[B] = static_cast<int32_t>(run[0]);
         chunk_off[B] = static_cast<int32_t>(run[1]);
         pblk_base[B] = static_cast<int32_t>(run[2]);
+        slice_base[B] = static_cast<int32_t>(run[3]);
         if (chunk_off_out) chunk_off_out[B] = static_cast<int32_t>(run[1]);
         if (chunk_off_check && chunk_off_check[B] != static_cast<int32_t>(run[1])) bad = 1;
     }
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 constexpr int kReduceThreads = 256;
 constexpr int kReduceSlabBatch = 4;
 
-__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
+__global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
     const float* logits, const float* lse2, const int32_t* seq_off, const int32_t* tile_base,
     float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab, int64_t Ntot,
     int64_t rows_per_slab, float scale2, int first_wave, int last_wave, const int32_t* bad) {
@@ -155,25 +160,27 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
     const int64_t first = i * kTileTokens + static_cast<int64_t>(sub) * TOK;  // within the prompt
     const int nvalid = static_cast<int>(min64(TOK, n - first));
     if (nvalid <= 0) return;
+    const int tq = threadIdx.x / Q4, c = threadIdx.x - tq * Q4;
+    const bool act = tq < nvalid;
+    const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
+    const float* src = logits + row * Rs + 4 * c;
+    const int64_t slab_stride = rows_per_slab * Rs;
+    // the first batch of logits is requested before the normalisers, and
+    // later batches while the current one is reduced: no barrier in the loop
+    float4 v[kReduceSlabBatch];
+#pragma unroll
+    for (int u = 0; u < kReduceSlabBatch; ++u)
+        if (act && u < nslab) v[u] = __ldcs(reinterpret_cast<const float4*>(src + u * slab_stride));
     for (int idx = threadIdx.x; idx < nslab * Rs; idx += kReduceThreads) {
         const int s = idx / Rs, r = idx - s * Rs;
         lse_s[idx] = lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
     }
-    const int tq = threadIdx.x / Q4, c = threadIdx.x - tq * Q4;
-    const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
-    const float* src = logits + row * Rs + 4 * c;
-    const int64_t slab_stride = rows_per_slab * Rs;
+    __syncthreads();
     float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
     for (int s0 = 0; s0 < nslab; s0 += kReduceSlabBatch) {
-        float4 v[kReduceSlabBatch];
-#pragma unroll
-        for (int u = 0; u < kReduceSlabBatch; ++u)
-            if (tq < nvalid && s0 + u < nslab)
-                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s0 + u) * slab_stride));
-        __syncthreads();  // lse_s ready (first batch)
 #pragma unroll
         for (int u = 0; u < kReduceSlabBatch; ++u) {
-            if (tq < nvalid && s0 + u < nslab) {
+            if (act && s0 + u < nslab) {
                 const float* ls = lse_s + (s0 + u) * Rs + 4 * c;
                 m0 = fmaxf(m0, fmaf(v[u].x, scale2, -ls[0]));
                 m1 = fmaxf(m1, fmaf(v[u].y, scale2, -ls[1]));
@@ -181,6 +188,11 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(
                 m3 = fmaxf(m3, fmaf(v[u].w, scale2, -ls[3]));
             }
         }
+        const int s1 = s0 + kReduceSlabBatch;
+#pragma unroll
+        for (int u = 0; u < kReduceSlabBatch; ++u)
+            if (act && s1 + u < nslab)
+                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s1 + u) * slab_stride));
     }
     if (tq < nvalid) {
         float* mrow = ms + tq * (Rs + 1) + 4 * c;
@@ -586,7 +598,7 @@ cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_
     return launch_k(prep_kernel, 1, kPrepThreads, 0, st, seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
         ws_ptr<int32_t>(ws, pl.o_tile_base),
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
-        ws_ptr<int32_t>(ws, pl.o_pblk_base), chunk_off_out,
+        ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), chunk_off_out,
         nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
         static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
         ws_ptr<WsHeader>(ws, 0));
@@ -597,7 +609,7 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
     return launch_k(prep_kernel, 1, kPrepThreads, 0, st, seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
         ws_ptr<int32_t>(ws, pl.o_tile_base),
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
-        ws_ptr<int32_t>(ws, pl.o_pblk_base), nullptr,
+        ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), nullptr,
         chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
         static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
         ws_ptr<WsHeader>(ws, 0));
