@@ -13,9 +13,9 @@
 namespace sp {
 namespace {
 
-// Scratch budget of one wave of slabs (fp32 logits): about half the L2 of
-// a GB300, so the logits written by one wave are still resident when the
-// softmax/importance kernel of the same wave reads them.
+// Scratch budget of one wave of slabs (quantised logits): about half the L2
+// of a GB300, so the logits written by one wave are still resident when the
+// importance kernel of the same wave reads them.
 constexpr int64_t kWaveScratchBytes = int64_t(60) << 20;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -105,7 +105,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     if (maxnc > kMaxPromptChunks) maxnc = kMaxPromptChunks;
     P.sort_cap = 1;
     while (P.sort_cap < maxnc) P.sort_cap <<= 1;
-    const int64_t per_slab = (P.tiles_max * kTileTokens) * P.Rs * static_cast<int64_t>(sizeof(float));
+    // quantised logits (2 bytes) plus one fp32 maximum per warp quarter and row
+    const int64_t per_slab = (P.tiles_max * kTileTokens) * P.Rs * 2 + P.tiles_max * 4 * P.Rs * 4;
     int64_t spw = kWaveScratchBytes / per_slab;
     if (spw < 1) spw = 1;
     if (spw > P.slabs) spw = P.slabs;
@@ -132,7 +133,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_slice_base = take(B1 * 4);
     P.o_scount = take(static_cast<size_t>(P.slices_max) * 4);
     P.o_segcnt = take(static_cast<size_t>(P.slabs_per_wave) * P.B * 4);
-    P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 4);
+    P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 2);
+    P.o_lmax = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * 4 * P.Rs * 4);
     P.o_part = take(static_cast<size_t>(P.rec_slots) * P.Rs * 8);
     P.o_lse = take(static_cast<size_t>(P.slabs_per_wave) * P.B * P.Rs * 4);
     P.o_alog = take(P.waves > 1 ? static_cast<size_t>(P.L) * P.Ntot * 4 : 0);

@@ -19,6 +19,22 @@ __device__ __forceinline__ void grid_dep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Logits scratch format. A scaled logit y = s * scale * log2(e) is stored
+// as the unsigned 16-bit fixed-point value of M - y, where M is the row's
+// maximum over the valid tokens of the warp quarter (32 tokens) of its tile,
+// with kLogitQuant steps per unit and clamped at kLogitQuantMax (M - y > 32).
+// M never exceeds the row's log2 softmax normaliser, so every probability
+// above 2^-32 has M - y < 32 and is reconstructed to within half a step
+// (2^-12 in log2 units: a relative error below 1.7e-4).
+constexpr float kLogitQuant = 2048.0f;
+constexpr float kLogitQuantInv = 1.0f / 2048.0f;
+constexpr uint32_t kLogitQuantMax = 65535u;
+
+__device__ __forceinline__ uint32_t quant_logit(float M, float y) {
+    const float d = (M - y) * kLogitQuant;  // >= 0 for the tokens that are read back
+    return d < static_cast<float>(kLogitQuantMax) ? __float2uint_rn(d) : kLogitQuantMax;
+}
+
 // Butterfly reduction of 32 rows held by every lane (v[r] = row r of this
 // lane's token): afterwards v[0] of lane r holds op over the 32 lanes of
 // row r. 31 shuffles instead of 32 separate 5-step reductions.

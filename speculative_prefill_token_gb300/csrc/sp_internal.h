@@ -46,7 +46,7 @@ struct Plan {
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
     // workspace offsets (bytes)
-    size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_part, o_lse, o_alog, o_imp, o_tok,
+    size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_lmax, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
         o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
 };

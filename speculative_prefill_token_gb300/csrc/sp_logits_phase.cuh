@@ -1,0 +1,493 @@
+// The logits phase of the SpecPrefill scoring path on fifth-generation
+// tensor cores (sm_103a), shared by the stand-alone logits kernel and the
+// persistent fused kernel.
+//
+// For one (layer l, KV head g) "slab" and one prompt, the logits are
+//   s[t, r] = <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>   (unscaled)
+// for the prompt's tokens t and the R = L*G query rows r = step*G + head
+// sharing KV head g ("SpecPrefill — Implementation Guide", §How It Works /
+// Attention Capture and Token Importance: one post-softmax row per head and
+// lookahead step; the attention matrix is Q K^T, §Sliding Window / The OOM
+// Problem). Only R rows per slab are needed, so this is a tall-skinny GEMM
+// that streams every key exactly once from HBM:
+//   A = 128 keys x 64 head-dim elements (one TMA box, 128-byte swizzle),
+//   B = R query rows x 64 elements, D = 128 x N fp32 in tensor memory.
+//
+// Roles (320 threads, one CTA per SM, persistent over a contiguous range of
+// (slab, prompt, 128-token tile) work items):
+//   warp 8      TMA producer: K boxes into a ring of 16 KB stages, Q per
+//               (slab, prompt) into one of two buffers;
+//   warp 9      tcgen05.mma issuer (one thread) and TMEM owner;
+//   warps 0-7   two epilogue warpgroups; warpgroup e drains TMEM accumulator
+//               e (tiles alternate), stages the tile's logits in swizzled
+//               shared memory for one TMA store into the scratch (one
+//               128-token slot per tile), and keeps per-thread running
+//               softmax statistics (row max reference, sum of exp2) that it
+//               reduces across threads once per (slab, prompt) segment; the
+//               last contribution to a segment merges its records into the
+//               segment's log2 normaliser.
+// Every mbarrier wait is bounded; a wait that gives up records
+// SP_ERR_TIMEOUT in the workspace status word, and the CTA then drains its
+// own copies, stores and MMAs in flight before it leaves the phase.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+#include "sp_ptx.cuh"
+
+namespace sp {
+
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
+constexpr int kStageOutBytes = kTileTokens * 64;   // 128 tokens x 32 quantised 16-bit logits
+constexpr int kMaxStages = 16;
+constexpr int kAcc = 4;                          // TMEM accumulators (tiles in flight)
+constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
+constexpr int64_t kDrainSpin = int64_t(1) << 22;
+
+struct TcArgs {
+    const int32_t* seq_off;
+    const int32_t* tile_base;
+    float* lmax;     // per (slab, tile, warp quarter) row maxima of the scaled logits [..][Rs]
+    int64_t tiles_max;
+    float2* rec;     // per (CTA, segment, warpgroup) softmax records [.. * 2 + wg][Rs]
+    unsigned* seg_cnt;  // per segment: records written so far (zero between calls)
+    float* lse2;     // per segment normaliser [seg][Rs]
+    int32_t* status;
+    const int32_t* bad;
+    int B, Hk, G, R, Rs, d_blocks, Nmma, Nacc, slab0, nslab, stages;
+    uint32_t q_block_bytes;  // Nmma * 128
+    float scale2;
+    int64_t spin;
+};
+
+struct SmemLayout {
+    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, seg_flag, stats, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes,
+                                                  int nh) {
+    SmemLayout s;
+    uint32_t off = 0;
+    s.k_ring = off;
+    off += static_cast<uint32_t>(stages) * kKBlockBytes;
+    s.q_buf = off;
+    off += 2u * static_cast<uint32_t>(d_blocks) * q_block_bytes;
+    off = (off + 1023u) & ~1023u;
+    s.out_buf = off;                                   // [warpgroup][half] 16 KB, swizzled
+    off += 2u * static_cast<uint32_t>(nh) * kStageOutBytes;
+    s.bars = off;
+    off += 8u * (2 * kMaxStages + 13);
+    s.tmem_slot = off;
+    off += 8;
+    s.abort_flag = off;
+    off += 8;
+    s.seg_flag = off;  // [warpgroup] int
+    off += 8;
+    s.stats = off;
+    off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
+    s.total = off;
+    return s;
+}
+
+struct Item {
+    int slab;      // local slab index in [0, nslab)
+    int b;         // prompt
+    int64_t tile;  // flattened tile index of the slab (scratch slot)
+    int64_t tok0;  // first global token of the tile
+    int nvalid;    // tokens of the tile inside the prompt
+};
+
+__device__ __forceinline__ Item decode(const TcArgs& a, int64_t w, int64_t T) {
+    Item it;
+    it.slab = static_cast<int>(w / T);
+    it.tile = w - static_cast<int64_t>(it.slab) * T;
+    it.b = search_base(a.tile_base, a.B, it.tile);
+    const int64_t i = it.tile - a.tile_base[it.b];
+    const int64_t start = a.seq_off[it.b];
+    const int64_t n = static_cast<int64_t>(a.seq_off[it.b + 1]) - start;
+    it.tok0 = start + i * kTileTokens;
+    const int64_t rem = n - i * kTileTokens;
+    it.nvalid = static_cast<int>(rem < kTileTokens ? rem : kTileTokens);
+    return it;
+}
+
+__device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_TIMEOUT));
+}
+
+
+// Shared-memory addresses of one CTA of the logits phase.
+struct LogitsCtx {
+    uint8_t* smem;
+    SmemLayout L;
+    uint32_t base, k_ring, q_buf, bar_full, bar_empty, bar_qfull, bar_qempty, bar_tfull, bar_tempty,
+        bar_drain, q_stage_bytes, tmem_base;
+    volatile uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    float2* stats;
+};
+
+template <int NH>
+__device__ __forceinline__ LogitsCtx logits_ctx(uint8_t* smem_raw, const TcArgs& a) {
+    LogitsCtx c;
+    c.smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                        ~static_cast<uintptr_t>(1023));
+    c.L = smem_layout(a.stages, a.d_blocks, a.q_block_bytes, NH);
+    c.base = smem_u32(c.smem);
+    c.k_ring = c.base + c.L.k_ring;
+    c.q_buf = c.base + c.L.q_buf;
+    c.bar_full = c.base + c.L.bars;
+    c.bar_empty = c.bar_full + 8 * kMaxStages;
+    c.bar_qfull = c.bar_empty + 8 * kMaxStages;   // [2]
+    c.bar_qempty = c.bar_qfull + 16;              // [2]
+    c.bar_tfull = c.bar_qempty + 16;              // [4]
+    c.bar_tempty = c.bar_tfull + 32;              // [4]
+    c.bar_drain = c.bar_tempty + 32;              // [1]
+    c.tmem_slot = reinterpret_cast<volatile uint32_t*>(c.smem + c.L.tmem_slot);
+    c.abort_flag = reinterpret_cast<volatile int*>(c.smem + c.L.abort_flag);
+    c.stats = reinterpret_cast<float2*>(c.smem + c.L.stats);
+    c.q_stage_bytes = static_cast<uint32_t>(a.d_blocks) * a.q_block_bytes;
+    c.tmem_base = 0;
+    return c;
+}
+
+// Initialise the phase's mbarriers and abort flag (thread 0; the caller
+// synchronises the CTA before any thread uses them).
+__device__ __forceinline__ void logits_init_barriers(const LogitsCtx& c, const TcArgs& a) {
+    for (int s = 0; s < a.stages; ++s) {
+        mbar_init(c.bar_full + 8 * s, 1);
+        mbar_init(c.bar_empty + 8 * s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+        mbar_init(c.bar_qfull + 8 * i, 1);
+        mbar_init(c.bar_qempty + 8 * i, 1);
+    }
+    for (int i = 0; i < kAcc; ++i) {
+        mbar_init(c.bar_tfull + 8 * i, 1);
+        mbar_init(c.bar_tempty + 8 * i, 128);
+    }
+    mbar_init(c.bar_drain, 1);
+    *c.abort_flag = 0;
+    fence_mbar_init();
+}
+
+// Setup by all kThreads threads, touching only this CTA's shared and tensor
+// memory: barriers, zeroed Q buffers (rows >= R stay zero), TMEM.
+__device__ __forceinline__ void logits_setup(LogitsCtx& c, const TcArgs& a, const CUtensorMap* tmap_k,
+                                             const CUtensorMap* tmap_q, const CUtensorMap* tmap_s) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) logits_init_barriers(c, a);
+    {
+        uint4* qz = reinterpret_cast<uint4*>(c.smem + c.L.q_buf);
+        const int n16 = static_cast<int>(2 * c.q_stage_bytes / 16);
+        for (int i = threadIdx.x; i < n16; i += kThreads) qz[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(c.tmem_slot)), static_cast<uint32_t>(kAcc * a.Nacc));
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(tmap_k);
+        prefetch_tmap(tmap_q);
+        prefetch_tmap(tmap_s);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem_base = *c.tmem_slot;
+}
+
+// Frees the tensor memory (all kThreads threads).
+__device__ __forceinline__ void logits_teardown(const LogitsCtx& c, const TcArgs& a) {
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(c.tmem_base, static_cast<uint32_t>(kAcc * a.Nacc));
+    }
+}
+
+// The work of CTA `cta` of C over the T tiles of each of the wave's slabs.
+// On return every TMA store of this CTA has completed; the CTA is not
+// synchronised.
+template <int NH>
+__device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a, const CUtensorMap* tmap_k,
+                                             const CUtensorMap* tmap_q, const CUtensorMap* tmap_s,
+                                             int64_t T, int64_t C, int64_t cta) {
+    uint8_t* const smem = c.smem;
+    const SmemLayout& L = c.L;
+    const uint32_t k_ring = c.k_ring, q_buf = c.q_buf, bar_full = c.bar_full, bar_empty = c.bar_empty,
+                   bar_qfull = c.bar_qfull, bar_qempty = c.bar_qempty, bar_tfull = c.bar_tfull,
+                   bar_tempty = c.bar_tempty, bar_drain = c.bar_drain, q_stage_bytes = c.q_stage_bytes,
+                   tmem_base = c.tmem_base;
+    volatile int* abort_flag = c.abort_flag;
+    float2* stats = c.stats;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t W = T * a.nslab;
+    const int64_t w_begin = split_start(W, C, cta);
+    const int64_t w_end = split_start(W, C, cta + 1);
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            int qn = 0;
+            int64_t prev_key = -1;
+            uint32_t issued_phase[kMaxStages];
+            bool issued[kMaxStages];
+            for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
+            bool ok = true;
+            for (int64_t w = w_begin; w < w_end && ok; ++w) {
+                const Item it = decode(a, w, T);
+                const int slab = a.slab0 + it.slab;
+                const int layer = slab / a.Hk, g = slab - layer * a.Hk;
+                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+                if (key != prev_key) {
+                    const int qb = qn & 1;
+                    if (!mbar_wait_bounded(bar_qempty + 8 * qb, ((qn >> 1) & 1) ^ 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_qfull + 8 * qb,
+                                          static_cast<uint32_t>(a.R) * 128u * a.d_blocks);
+                    for (int kb = 0; kb < a.d_blocks; ++kb)
+                        tma_load_5d(q_buf + qb * q_stage_bytes + kb * a.q_block_bytes, tmap_q,
+                                    bar_qfull + 8 * qb, kb * 64, g * a.G, 0, layer, it.b);
+                    ++qn;
+                    prev_key = key;
+                }
+                for (int kb = 0; kb < a.d_blocks; ++kb) {
+                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * stage, kKBlockBytes);
+                    tma_load_4d(k_ring + stage * kKBlockBytes, tmap_k, bar_full + 8 * stage,
+                                kb * 64, static_cast<int>(it.tok0), g, layer, pol);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // drain: every copy this thread issued must land before exit
+            for (int s = 0; s < a.stages; ++s)
+                if (issued[s]) mbar_wait_spin(bar_full + 8 * s, issued_phase[s], kDrainSpin);
+            for (int i = 0; i < 2 && i < qn; ++i) {
+                const int last = (qn - 1 - i);
+                mbar_wait_spin(bar_qfull + 8 * (last & 1), (last >> 1) & 1, kDrainSpin);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, a.Nmma);
+            int stage = 0;
+            uint32_t phase = 0;
+            int qn = 0;
+            int64_t prev_key = -1;
+            int64_t j = 0;
+            int qb = 0;
+            bool ok = true;
+            bool any_mma = false;
+            for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
+                const Item it = decode(a, w, T);
+                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+                if (key != prev_key) {
+                    if (qn > 0) tc_commit(bar_qempty + 8 * ((qn - 1) & 1));
+                    qb = qn & 1;
+                    if (!mbar_wait_bounded(bar_qfull + 8 * qb, (qn >> 1) & 1, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ++qn;
+                    prev_key = key;
+                }
+                const int acc = static_cast<int>(j & (kAcc - 1));
+                if (!mbar_wait_bounded(bar_tempty + 8 * acc, static_cast<uint32_t>(((j >> 2) & 1) ^ 1),
+                                       a.spin, abort_flag)) {
+                    record_timeout(a, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * a.Nacc);
+                for (int kb = 0; kb < a.d_blocks; ++kb) {
+                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, a.spin, abort_flag)) {
+                        record_timeout(a, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = k_ring + stage * kKBlockBytes;
+                    const uint32_t b_addr = q_buf + qb * q_stage_bytes + kb * a.q_block_bytes;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + 32 * k4),
+                                    smem_desc_sw128(b_addr + 32 * k4), idesc, (kb | k4) != 0);
+                    }
+                    any_mma = true;
+                    tc_commit(bar_empty + 8 * stage);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar_tfull + 8 * acc);
+            }
+            // drain: all MMAs issued by this thread complete before TMEM is freed
+            if (any_mma) {
+                tc_commit(bar_drain);
+                mbar_wait_spin(bar_drain, 0, kDrainSpin);
+            }
+        }
+    } else {
+        // epilogue warpgroups
+        const int e = warp >> 2;          // warpgroup: tiles j with j % 2 == e
+        const int qw = warp & 3;          // TMEM lane quarter
+        const int bar_id = 1 + e;
+        const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+        uint8_t* out_buf = smem + L.out_buf + e * NH * kStageOutBytes;
+        const uint32_t out_addr = smem_u32(out_buf);
+        float2* st_sm = stats + e * 4 * 64;
+        volatile int* seg_flag = reinterpret_cast<volatile int*>(smem + L.seg_flag) + e;
+        const int tl = qw * 32 + lane;   // token row of the tile
+        RowStats<NH> rs;
+        stats_reset(rs);
+        int64_t cur_key = -1;
+        bool stores = false;
+        bool ok = true;
+        int64_t j = 0;
+        for (int64_t w = w_begin; w < w_end; ++w, ++j) {
+            const Item it = decode(a, w, T);
+            const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+            if (key != cur_key) {
+                if (cur_key >= 0) {
+                    stats_flush<NH>(rs, st_sm, qw, bar_id,
+                                    a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
+                    segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
+                                 a.R, a.Rs, st_sm, seg_flag, qw, bar_id);
+                }
+                cur_key = key;
+            }
+            if (static_cast<int>(j & 1) != e) continue;
+            // all 128 threads of the warpgroup take the same decision, so the
+            // named barriers below never wait for a thread that left
+            const int acc = static_cast<int>(j & (kAcc - 1));
+            const bool got = mbar_wait_bounded(bar_tfull + 8 * acc, static_cast<uint32_t>((j >> 2) & 1),
+                                               a.spin, abort_flag);
+            if (!bar_sync_and(bar_id, 128, got)) {
+                record_timeout(a, abort_flag);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float v[NH][32];
+            const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * a.Nacc);
+            tmem_ld_32x32b_x32(taddr, v[0]);
+            if (NH > 1) tmem_ld_32x32b_x32(taddr + 32, v[NH - 1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+                for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
+                    if (hh * 32 + r >= a.Nmma) v[hh][r] = 0.0f;
+            const bool valid = tl < it.nvalid;
+            if (valid) stats_add<NH>(rs, v, a.scale2);
+            // row maxima of the scaled logits over the warp quarter's valid tokens
+            float m_own[NH];
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r) v[hh][r] = valid ? v[hh][r] * a.scale2 : -INFINITY;
+                m_own[hh] = warp_rows_reduce<true>(v[hh]);
+                if (hh * 32 + lane < a.Rs)
+                    a.lmax[((static_cast<int64_t>(it.slab) * a.tiles_max + it.tile) * 4 + qw) * a.Rs + hh * 32 +
+                           lane] = m_own[hh];
+            }
+            // the reduction consumed the values: read the accumulator again, then free it
+            tmem_ld_32x32b_x32(taddr, v[0]);
+            if (NH > 1) tmem_ld_32x32b_x32(taddr + 32, v[NH - 1]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(bar_tempty + 8 * acc);
+
+            // stage the quantised logits and store the tile with TMA
+            if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int r = 0; r < 32; r += 2) {
+                    const float M0 = __shfl_sync(0xffffffffu, m_own[hh], r);
+                    const float M1 = __shfl_sync(0xffffffffu, m_own[hh], r + 1);
+                    pk[r / 2] = quant_logit(M0, v[hh][r] * a.scale2) |
+                                (quant_logit(M1, v[hh][r + 1] * a.scale2) << 16);
+                }
+                uint4* row = reinterpret_cast<uint4*>(out_buf + hh * kStageOutBytes + tl * 64);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    row[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+            if (qw == 0 && lane == 0) {
+                const int y = static_cast<int>(it.tile * kTileTokens);
+#pragma unroll
+                for (int hh = 0; hh < NH; ++hh)
+                    tma_store_3d(tmap_s, out_addr + hh * kStageOutBytes, hh * 32, y, it.slab);
+                bulk_commit();
+                stores = true;
+            }
+        }
+        if (ok && cur_key >= 0) {
+            stats_flush<NH>(rs, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs,
+                            a.R);
+            segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
+                         a.Rs, st_sm, seg_flag, qw, bar_id);
+        }
+        if (qw == 0 && lane == 0 && stores) bulk_wait0();
+    }
+
+}
+
+// ------------------------------------------------------------------ host
+
+struct LogitsMaps {
+    CUtensorMap k, q, s;
+};
+
+// Tensor maps of the keys, queries and the wave's logits scratch.
+cudaError_t make_logits_maps(const Plan& pl, const sp_shape* s, const uint16_t* q, const uint16_t* k,
+                             void* ws, int nslab, LogitsMaps* m);
+
+// Ring stages, dynamic shared memory and 32-row halves (1 or 2) of the
+// logits phase for this plan.
+cudaError_t logits_smem(const Plan& pl, int* stages, uint32_t* smem, int* nh);
+
+// Kernel arguments and shared-memory size of the logits phase for the
+// slabs [slab0, slab0 + nslab); *nh = 1 or 2 (32-row halves of the rows).
+cudaError_t logits_config(const Plan& pl, const int32_t* seq_off, void* ws, int slab0, int nslab,
+                          TcArgs* a, uint32_t* smem, int* nh);
+
+}  // namespace sp

@@ -1,5 +1,5 @@
 // CUDA-core (FP32 FMA) variant of the logits kernel. Same contract and
-// scratch layout as the tensor-core kernel: one CTA per (128-token tile,
+// quantised scratch format as the tensor-core kernel: one CTA per (128-token tile,
 // slab), one thread per key, fp32 accumulation of the R dot products
 // against queries staged in shared memory. It is the independent
 // cross-check of the tensor-core kernel in the GPU tests; the library's
@@ -20,13 +20,14 @@ struct SimtArgs {
     const int32_t* tile_base;
     const uint16_t* q;
     const uint16_t* k;
-    float* logits;   // [nslab][tiles_max * 128][Rs], raw dot products
+    uint16_t* logits;  // [nslab][tiles_max * 128][Rs], quantised scaled logits
+    float* lmax;       // [nslab][tiles_max][4][Rs] warp-quarter row maxima
     float2* rec;     // softmax records [(cta + segment) * 2 + warpgroup][Rs]
     unsigned* seg_cnt;
     float* lse2;
     const int32_t* bad;
     int B, Hk, G, L, R, Rs, d, slab0, nslab;
-    int64_t rows_per_slab;
+    int64_t rows_per_slab, tiles_max;
     int64_t ks_layer, ks_token, ks_head, qs_seq, qs_layer, qs_step, qs_head;
     float scale2;
 };
@@ -99,16 +100,37 @@ __global__ void __launch_bounds__(128) logits_simt_kernel(const SimtArgs a) {
                     for (int e = 0; e < 8; ++e) v[h][r] = fmaf(kf[e], qr[e], v[h][r]);
                 }
         }
-        float* dst = a.logits + (static_cast<int64_t>(slab_local) * a.rows_per_slab +
-                                 tile * kTileTokens + t) * a.Rs;
-#pragma unroll
-        for (int h = 0; h < NH; ++h)
-#pragma unroll
-            for (int r = 0; r < 32; ++r) dst[h * 32 + r] = v[h][r];
     }
     RowStats<NH> rs;
     stats_reset(rs);
     if (valid) stats_add<NH>(rs, v, a.scale2);
+    // quantised scratch, same format as the tensor-core kernel: row maxima
+    // over the warp's valid tokens, then M - y in 16-bit fixed point
+    {
+        const int lane = t & 31, qw = t >> 5;
+        float m_own[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            float w[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) w[r] = valid ? v[h][r] * a.scale2 : -INFINITY;
+            m_own[h] = warp_rows_reduce<true>(w);
+            if (h * 32 + lane < a.Rs)
+                a.lmax[((static_cast<int64_t>(slab_local) * a.tiles_max + tile) * 4 + qw) * a.Rs + h * 32 + lane] =
+                    m_own[h];
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(
+            a.logits + (static_cast<int64_t>(slab_local) * a.rows_per_slab + tile * kTileTokens + t) * a.Rs);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int r = 0; r < 32; r += 2) {
+                const float M0 = __shfl_sync(0xffffffffu, m_own[h], r);
+                const float M1 = __shfl_sync(0xffffffffu, m_own[h], r + 1);
+                const uint32_t pk = quant_logit(M0, v[h][r] * a.scale2) | (quant_logit(M1, v[h][r + 1] * a.scale2) << 16);
+                if (valid) dst[h * 16 + r / 2] = pk;
+            }
+    }
     const int64_t seg = static_cast<int64_t>(slab_local) * a.B + b;
     float2* out = a.rec + ((blockIdx.x + seg) * 2) * a.Rs;
     if (t < a.R) {
@@ -130,7 +152,9 @@ cudaError_t launch_logits_simt(const Plan& pl, const sp_shape* s, const int32_t*
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
     a.q = q;
     a.k = k;
-    a.logits = ws_ptr<float>(ws, pl.o_logits);
+    a.logits = ws_ptr<uint16_t>(ws, pl.o_logits);
+    a.lmax = ws_ptr<float>(ws, pl.o_lmax);
+    a.tiles_max = pl.tiles_max;
     a.rec = ws_ptr<float2>(ws, pl.o_part);
     a.seg_cnt = ws_ptr<unsigned>(ws, pl.o_segcnt);
     a.lse2 = ws_ptr<float>(ws, pl.o_lse);

@@ -1,31 +1,7 @@
-// Logits kernel of the SpecPrefill scoring path on fifth-generation tensor
-// cores (sm_103a).
-//
-// For one (layer l, KV head g) "slab" and one prompt, the logits are
-//   s[t, r] = <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>   (unscaled)
-// for the prompt's tokens t and the R = L*G query rows r = step*G + head
-// sharing KV head g ("SpecPrefill — Implementation Guide", §How It Works /
-// Attention Capture and Token Importance: one post-softmax row per head and
-// lookahead step; the attention matrix is Q K^T, §Sliding Window / The OOM
-// Problem). Only R rows per slab are needed, so this is a tall-skinny GEMM
-// that streams every key exactly once from HBM:
-//   A = 128 keys x 64 head-dim elements (one TMA box, 128-byte swizzle),
-//   B = R query rows x 64 elements, D = 128 x N fp32 in tensor memory.
-//
-// Roles (320 threads, one CTA per SM, persistent over a contiguous range of
-// (slab, prompt, 128-token tile) work items):
-//   warp 8      TMA producer: K boxes into a ring of 16 KB stages, Q per
-//               (slab, prompt) into one of two buffers;
-//   warp 9      tcgen05.mma issuer (one thread) and TMEM owner;
-//   warps 0-7   two epilogue warpgroups; warpgroup e drains TMEM accumulator
-//               e (tiles alternate), stages the tile's logits in swizzled
-//               shared memory for one TMA store into the scratch (one
-//               128-token slot per tile), and keeps per-thread running
-//               softmax statistics (row max reference, sum of exp2) that it
-//               reduces across threads once per (slab, prompt) segment.
-// Every mbarrier wait is bounded; a wait that gives up records
-// SP_ERR_TIMEOUT in the workspace status word, and the CTA then drains its
-// own copies, stores and MMAs in flight, frees TMEM and returns.
+// Stand-alone logits kernel of the SpecPrefill scoring path (the logits
+// phase of sp_logits_phase.cuh on its own), used by sp_attn_importance and
+// the multi-wave path, and the host side of the phase: tensor maps, kernel
+// arguments and shared-memory size.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -35,90 +11,11 @@
 
 #include "sp_device.cuh"
 #include "sp_internal.h"
+#include "sp_logits_phase.cuh"
 #include "sp_ptx.cuh"
 
 namespace sp {
 namespace {
-
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
-constexpr int kStageOutBytes = kTileTokens * 128;  // 128 tokens x 32 fp32
-constexpr int kMaxStages = 16;
-constexpr int kAcc = 4;                          // TMEM accumulators (tiles in flight)
-constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
-constexpr int64_t kDrainSpin = int64_t(1) << 22;
-
-struct TcArgs {
-    const int32_t* seq_off;
-    const int32_t* tile_base;
-    float2* rec;     // per (CTA, segment, warpgroup) softmax records [.. * 2 + wg][Rs]
-    unsigned* seg_cnt;  // per segment: records written so far (zero between calls)
-    float* lse2;     // per segment normaliser [seg][Rs]
-    int32_t* status;
-    const int32_t* bad;
-    int B, Hk, G, R, Rs, d_blocks, Nmma, Nacc, slab0, nslab, stages;
-    uint32_t q_block_bytes;  // Nmma * 128
-    float scale2;
-    int64_t spin;
-};
-
-struct SmemLayout {
-    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, seg_flag, stats, total;
-};
-
-__host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes,
-                                                  int nh) {
-    SmemLayout s;
-    uint32_t off = 0;
-    s.k_ring = off;
-    off += static_cast<uint32_t>(stages) * kKBlockBytes;
-    s.q_buf = off;
-    off += 2u * static_cast<uint32_t>(d_blocks) * q_block_bytes;
-    off = (off + 1023u) & ~1023u;
-    s.out_buf = off;                                   // [warpgroup][half] 16 KB, swizzled
-    off += 2u * static_cast<uint32_t>(nh) * kStageOutBytes;
-    s.bars = off;
-    off += 8u * (2 * kMaxStages + 13);
-    s.tmem_slot = off;
-    off += 8;
-    s.abort_flag = off;
-    off += 8;
-    s.seg_flag = off;  // [warpgroup] int
-    off += 8;
-    s.stats = off;
-    off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
-    s.total = off;
-    return s;
-}
-
-struct Item {
-    int slab;      // local slab index in [0, nslab)
-    int b;         // prompt
-    int64_t tile;  // flattened tile index of the slab (scratch slot)
-    int64_t tok0;  // first global token of the tile
-    int nvalid;    // tokens of the tile inside the prompt
-};
-
-__device__ __forceinline__ Item decode(const TcArgs& a, int64_t w, int64_t T) {
-    Item it;
-    it.slab = static_cast<int>(w / T);
-    it.tile = w - static_cast<int64_t>(it.slab) * T;
-    it.b = search_base(a.tile_base, a.B, it.tile);
-    const int64_t i = it.tile - a.tile_base[it.b];
-    const int64_t start = a.seq_off[it.b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[it.b + 1]) - start;
-    it.tok0 = start + i * kTileTokens;
-    const int64_t rem = n - i * kTileTokens;
-    it.nvalid = static_cast<int>(rem < kTileTokens ? rem : kTileTokens);
-    return it;
-}
-
-__device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag) {
-    *abort_flag = 1;
-    atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_TIMEOUT));
-}
 
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -126,287 +23,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmap_q,
                      const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-    const SmemLayout L = smem_layout(a.stages, a.d_blocks, a.q_block_bytes, NH);
-    const uint32_t base = smem_u32(smem);
-    const uint32_t k_ring = base + L.k_ring;
-    const uint32_t q_buf = base + L.q_buf;
-    const uint32_t bar_full = base + L.bars;
-    const uint32_t bar_empty = bar_full + 8 * kMaxStages;
-    const uint32_t bar_qfull = bar_empty + 8 * kMaxStages;   // [2]
-    const uint32_t bar_qempty = bar_qfull + 16;              // [2]
-    const uint32_t bar_tfull = bar_qempty + 16;              // [4]
-    const uint32_t bar_tempty = bar_tfull + 32;              // [4]
-    const uint32_t bar_drain = bar_tempty + 32;              // [1]
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L.tmem_slot);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
-    float2* stats = reinterpret_cast<float2*>(smem + L.stats);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t q_stage_bytes = static_cast<uint32_t>(a.d_blocks) * a.q_block_bytes;
-
-    // ---- setup: barriers, zeroed Q buffers (rows >= R stay zero), TMEM
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_qfull + 8 * i, 1);
-            mbar_init(bar_qempty + 8 * i, 1);
-        }
-        for (int i = 0; i < kAcc; ++i) {
-            mbar_init(bar_tfull + 8 * i, 1);
-            mbar_init(bar_tempty + 8 * i, 128);
-        }
-        mbar_init(bar_drain, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    {
-        uint4* qz = reinterpret_cast<uint4*>(smem + L.q_buf);
-        const int n16 = static_cast<int>(2 * q_stage_bytes / 16);
-        for (int i = threadIdx.x; i < n16; i += kThreads) qz[i] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), static_cast<uint32_t>(kAcc * a.Nacc));
-        tmem_relinquish();
-    }
-    if (warp == kProducerWarp && lane == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_q);
-        prefetch_tmap(&tmap_s);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
+    LogitsCtx c = logits_ctx<NH>(smem_raw, a);
+    logits_setup(c, a, &tmap_k, &tmap_q, &tmap_s);
     // everything above touched only this CTA's shared and tensor memory; the
     // offsets and counters below come from the preceding kernel
     grid_dep_wait();
     grid_dep_launch();
     const int64_t T = *a.bad ? 0 : a.tile_base[a.B];  // invalid offsets: no work, normal teardown
-    const int64_t W = T * a.nslab;
-    const int64_t C = gridDim.x;
-    const int64_t w_begin = split_start(W, C, blockIdx.x);
-    const int64_t w_end = split_start(W, C, blockIdx.x + 1);
-
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
-            int qn = 0;
-            int64_t prev_key = -1;
-            uint32_t issued_phase[kMaxStages];
-            bool issued[kMaxStages];
-            for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
-            bool ok = true;
-            for (int64_t w = w_begin; w < w_end && ok; ++w) {
-                const Item it = decode(a, w, T);
-                const int slab = a.slab0 + it.slab;
-                const int layer = slab / a.Hk, g = slab - layer * a.Hk;
-                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
-                if (key != prev_key) {
-                    const int qb = qn & 1;
-                    if (!mbar_wait_bounded(bar_qempty + 8 * qb, ((qn >> 1) & 1) ^ 1, a.spin, abort_flag)) {
-                        record_timeout(a, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar_qfull + 8 * qb,
-                                          static_cast<uint32_t>(a.R) * 128u * a.d_blocks);
-                    for (int kb = 0; kb < a.d_blocks; ++kb)
-                        tma_load_5d(q_buf + qb * q_stage_bytes + kb * a.q_block_bytes, &tmap_q,
-                                    bar_qfull + 8 * qb, kb * 64, g * a.G, 0, layer, it.b);
-                    ++qn;
-                    prev_key = key;
-                }
-                for (int kb = 0; kb < a.d_blocks; ++kb) {
-                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1, a.spin, abort_flag)) {
-                        record_timeout(a, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar_full + 8 * stage, kKBlockBytes);
-                    tma_load_4d(k_ring + stage * kKBlockBytes, &tmap_k, bar_full + 8 * stage,
-                                kb * 64, static_cast<int>(it.tok0), g, layer, pol);
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == a.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            // drain: every copy this thread issued must land before exit
-            for (int s = 0; s < a.stages; ++s)
-                if (issued[s]) mbar_wait_spin(bar_full + 8 * s, issued_phase[s], kDrainSpin);
-            for (int i = 0; i < 2 && i < qn; ++i) {
-                const int last = (qn - 1 - i);
-                mbar_wait_spin(bar_qfull + 8 * (last & 1), (last >> 1) & 1, kDrainSpin);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, a.Nmma);
-            int stage = 0;
-            uint32_t phase = 0;
-            int qn = 0;
-            int64_t prev_key = -1;
-            int64_t j = 0;
-            int qb = 0;
-            bool ok = true;
-            bool any_mma = false;
-            for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
-                const Item it = decode(a, w, T);
-                const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
-                if (key != prev_key) {
-                    if (qn > 0) tc_commit(bar_qempty + 8 * ((qn - 1) & 1));
-                    qb = qn & 1;
-                    if (!mbar_wait_bounded(bar_qfull + 8 * qb, (qn >> 1) & 1, a.spin, abort_flag)) {
-                        record_timeout(a, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    ++qn;
-                    prev_key = key;
-                }
-                const int acc = static_cast<int>(j & (kAcc - 1));
-                if (!mbar_wait_bounded(bar_tempty + 8 * acc, static_cast<uint32_t>(((j >> 2) & 1) ^ 1),
-                                       a.spin, abort_flag)) {
-                    record_timeout(a, abort_flag);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * a.Nacc);
-                for (int kb = 0; kb < a.d_blocks; ++kb) {
-                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, a.spin, abort_flag)) {
-                        record_timeout(a, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = k_ring + stage * kKBlockBytes;
-                    const uint32_t b_addr = q_buf + qb * q_stage_bytes + kb * a.q_block_bytes;
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + 32 * k4),
-                                    smem_desc_sw128(b_addr + 32 * k4), idesc, (kb | k4) != 0);
-                    }
-                    any_mma = true;
-                    tc_commit(bar_empty + 8 * stage);
-                    if (++stage == a.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(bar_tfull + 8 * acc);
-            }
-            // drain: all MMAs issued by this thread complete before TMEM is freed
-            if (any_mma) {
-                tc_commit(bar_drain);
-                mbar_wait_spin(bar_drain, 0, kDrainSpin);
-            }
-        }
-    } else {
-        // epilogue warpgroups
-        const int e = warp >> 2;          // warpgroup: tiles j with j % 2 == e
-        const int qw = warp & 3;          // TMEM lane quarter
-        const int bar_id = 1 + e;
-        const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-        uint8_t* out_buf = smem + L.out_buf + e * NH * kStageOutBytes;
-        const uint32_t out_addr = smem_u32(out_buf);
-        float2* st_sm = stats + e * 4 * 64;
-        volatile int* seg_flag = reinterpret_cast<volatile int*>(smem + L.seg_flag) + e;
-        const int tl = qw * 32 + lane;   // token row of the tile
-        RowStats<NH> rs;
-        stats_reset(rs);
-        int64_t cur_key = -1;
-        bool stores = false;
-        bool ok = true;
-        int64_t j = 0;
-        for (int64_t w = w_begin; w < w_end; ++w, ++j) {
-            const Item it = decode(a, w, T);
-            const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
-            if (key != cur_key) {
-                if (cur_key >= 0) {
-                    stats_flush<NH>(rs, st_sm, qw, bar_id,
-                                    a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs, a.R);
-                    segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
-                                 a.R, a.Rs, st_sm, seg_flag, qw, bar_id);
-                }
-                cur_key = key;
-            }
-            if (static_cast<int>(j & 1) != e) continue;
-            // all 128 threads of the warpgroup take the same decision, so the
-            // named barriers below never wait for a thread that left
-            const int acc = static_cast<int>(j & (kAcc - 1));
-            const bool got = mbar_wait_bounded(bar_tfull + 8 * acc, static_cast<uint32_t>((j >> 2) & 1),
-                                               a.spin, abort_flag);
-            if (!bar_sync_and(bar_id, 128, got)) {
-                record_timeout(a, abort_flag);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float v[NH][32];
-            const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * a.Nacc);
-            tmem_ld_32x32b_x32(taddr, v[0]);
-            if (NH > 1) tmem_ld_32x32b_x32(taddr + 32, v[NH - 1]);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(bar_tempty + 8 * acc);
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh)
-#pragma unroll
-                for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
-                    if (hh * 32 + r >= a.Nmma) v[hh][r] = 0.0f;
-
-            // stage the raw logits (128-byte swizzle) and store the tile with TMA
-            if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
-            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                uint8_t* row = out_buf + hh * kStageOutBytes + tl * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4*>(row + ((c ^ (tl & 7)) << 4)) =
-                        make_float4(v[hh][4 * c], v[hh][4 * c + 1], v[hh][4 * c + 2], v[hh][4 * c + 3]);
-            }
-            fence_proxy_async_smem();
-            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
-            if (qw == 0 && lane == 0) {
-                const int y = static_cast<int>(it.tile * kTileTokens);
-#pragma unroll
-                for (int hh = 0; hh < NH; ++hh)
-                    tma_store_3d(&tmap_s, out_addr + hh * kStageOutBytes, hh * 32, y, it.slab);
-                bulk_commit();
-                stores = true;
-            }
-            if (tl < it.nvalid) stats_add<NH>(rs, v, a.scale2);
-        }
-        if (ok && cur_key >= 0) {
-            stats_flush<NH>(rs, st_sm, qw, bar_id, a.rec + ((blockIdx.x + cur_key) * 2 + e) * a.Rs,
-                            a.R);
-            segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
-                         a.Rs, st_sm, seg_flag, qw, bar_id);
-        }
-        if (qw == 0 && lane == 0 && stores) bulk_wait0();
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(kAcc * a.Nacc));
-    }
+    logits_phase<NH>(c, a, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    logits_teardown(c, a);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -427,23 +52,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+
 }  // namespace
 
-int logits_tc_grid(const Plan& pl, int nslab) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t work = pl.tiles_max * nslab;
-    return static_cast<int>(work < sms ? work : sms);
-}
-
-cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
-                             const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                             int grid, cudaStream_t st) {
+cudaError_t make_logits_maps(const Plan& pl, const sp_shape* s, const uint16_t* q, const uint16_t* k,
+                             void* ws, int nslab, LogitsMaps* m) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int d = pl.d;
-    CUtensorMap tk, tq, ts;
     {
         // K: dims (d, token, kv head, layer); unused strides get a harmless value
         const int64_t sh = pl.Hk > 1 ? s->k_stride_head : d;
@@ -454,7 +70,7 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
                                  static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sl) * 2};
         cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileTokens), 1, 1};
         cuuint32_t es[4] = {1, 1, 1, 1};
-        if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(k), dims, strides,
+        if (enc(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(k), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -472,27 +88,48 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
                                  static_cast<cuuint64_t>(sl) * 2, static_cast<cuuint64_t>(sb) * 2};
         cuuint32_t box[5] = {64, static_cast<cuuint32_t>(pl.G), static_cast<cuuint32_t>(pl.L), 1, 1};
         cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<uint16_t*>(q), dims, strides,
+        if (enc(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<uint16_t*>(q), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
-        // logits scratch: dims (row value, tile slot row, slab); box = 32 values x 128 rows
+        // quantised logits scratch: dims (row value, tile slot row, slab); box = 32
+        // values x 128 rows, staged densely (64-byte rows)
         const uint64_t rows = static_cast<uint64_t>(pl.tiles_max) * kTileTokens;
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(pl.Rs), rows, static_cast<cuuint64_t>(nslab)};
-        cuuint64_t strides[2] = {static_cast<cuuint64_t>(pl.Rs) * 4,
-                                 static_cast<cuuint64_t>(rows * pl.Rs * 4)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(pl.Rs) * 2,
+                                 static_cast<cuuint64_t>(rows * pl.Rs * 2)};
         cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTileTokens), 1};
         cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws_ptr<float>(ws, pl.o_logits), dims,
-                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (enc(&m->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, ws_ptr<uint16_t>(ws, pl.o_logits), dims,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    TcArgs a;
+    return cudaSuccess;
+}
+
+cudaError_t logits_smem(const Plan& pl, int* stages, uint32_t* smem, int* nh) {
+    const int d_blocks = pl.d / 64;
+    const uint32_t q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
+    *nh = pl.Rs > 32 ? 2 : 1;
+    const uint32_t fixed = smem_layout(0, d_blocks, q_block_bytes, *nh).total + 1024;
+    int st = static_cast<int>((kSmemLimit - static_cast<int>(fixed)) / kKBlockBytes);
+    if (st > kMaxStages) st = kMaxStages;
+    if (st < 2) return cudaErrorInvalidConfiguration;
+    *stages = st;
+    *smem = smem_layout(st, d_blocks, q_block_bytes, *nh).total + 1024;
+    return cudaSuccess;
+}
+
+cudaError_t logits_config(const Plan& pl, const int32_t* seq_off, void* ws, int slab0, int nslab,
+                          TcArgs* ap, uint32_t* smem, int* nh) {
+    TcArgs& a = *ap;
     a.seq_off = seq_off;
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
+    a.lmax = ws_ptr<float>(ws, pl.o_lmax);
+    a.tiles_max = pl.tiles_max;
     a.rec = ws_ptr<float2>(ws, pl.o_part);
     a.seg_cnt = ws_ptr<unsigned>(ws, pl.o_segcnt);
     a.lse2 = ws_ptr<float>(ws, pl.o_lse);
@@ -503,7 +140,7 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
     a.G = pl.G;
     a.R = pl.R;
     a.Rs = pl.Rs;
-    a.d_blocks = d / 64;
+    a.d_blocks = pl.d / 64;
     a.Nmma = pl.Nmma;
     a.Nacc = pl.Nacc;
     a.slab0 = slab0;
@@ -511,19 +148,31 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
     a.q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
     a.scale2 = pl.scale2;
     a.spin = pl.spin;
+    return logits_smem(pl, &a.stages, smem, nh);
+}
 
-    const int nh = pl.Rs > 32 ? 2 : 1;
-    const uint32_t fixed = smem_layout(0, a.d_blocks, a.q_block_bytes, nh).total + 1024;
-    int stages = static_cast<int>((kSmemLimit - static_cast<int>(fixed)) / kKBlockBytes);
-    if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2) return cudaErrorInvalidConfiguration;
-    a.stages = stages;
-    const uint32_t smem = smem_layout(stages, a.d_blocks, a.q_block_bytes, nh).total + 1024;
-    auto kern = nh == 2 ? logits_tc_kernel<2> : logits_tc_kernel<1>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+int logits_tc_grid(const Plan& pl, int nslab) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t work = pl.tiles_max * nslab;
+    return static_cast<int>(work < sms ? work : sms);
+}
+
+cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
+                             const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
+                             int grid, cudaStream_t st) {
+    LogitsMaps m;
+    cudaError_t err = make_logits_maps(pl, s, q, k, ws, nslab, &m);
     if (err != cudaSuccess) return err;
-    return launch_k(kern, grid, kThreads, smem, st, tk, tq, ts, a);
+    TcArgs a;
+    uint32_t smem = 0;
+    int nh = 1;
+    if ((err = logits_config(pl, seq_off, ws, slab0, nslab, &a, &smem, &nh)) != cudaSuccess) return err;
+    auto kern = nh == 2 ? logits_tc_kernel<2> : logits_tc_kernel<1>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    return launch_k(kern, grid, kThreads, smem, st, m.k, m.q, m.s, a);
 }
 
 }  // namespace sp

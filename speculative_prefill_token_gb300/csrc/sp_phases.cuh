@@ -1,0 +1,424 @@
+// Per-item phases of the SpecPrefill scoring path after the token
+// importance, written as device functions for a group of threads so that
+// the stand-alone kernels (one item per CTA) and the persistent fused kernel
+// (items strided over a fixed grid, phases separated by grid barriers) run
+// the same code:
+//
+//   pool_tile     one 128-token tile: W-window mean of the importance
+//                 (llama.cpp PR "Speculative prefill" §Approach item 3), the
+//                 tile's min / max and the per-chunk sums of boost * x and of
+//                 boost ("SpecPrefill — Implementation Guide" v3 item 2,
+//                 §Chunk Selection)
+//   rank_slice    chunk scores (min-max normalisation, guide v3.1 item 5)
+//                 and the selection of one slice of 32 chunks (guide
+//                 §Chunk Selection, v3 item 1; PR §Approach item 4)
+//   gather_slice  kept token indices and positions of one slice (guide
+//                 §How It Works / Sparse Prefill) and the per-prompt offsets
+//
+// Values written by other CTAs (in the persistent kernel: earlier in the
+// same launch) are read through L2 (ld.global.cg), never from a possibly
+// stale L1 line.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "sp_device.cuh"
+#include "sp_internal.h"
+#include "sp_select.cuh"
+
+namespace sp {
+
+// Named barrier over the first-to-last `n` threads of a warp-aligned group.
+struct GroupBar {
+    int id, n;
+    __device__ __forceinline__ void sync() const {
+        asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+    }
+};
+
+// ------------------------------------------------------------------ pool
+constexpr int kPoolThreads = 128;
+constexpr int kPoolMaxHalo = 64;
+
+struct PoolArgs {
+    const float* imp;
+    float* tok;
+    float2* rpart;   // per tile (min, max) of the pooled scores
+    float2* csum;    // per chunk (sum boost * x, sum boost)
+    const int32_t* seq_off;
+    const int32_t* tile_base;
+    const int32_t* chunk_off;
+    int B, W, C, bf_n, bl_n;
+    float bf_mult, bl_mult;
+};
+
+struct PoolShared {
+    float win[kTileTokens + 2 * kPoolMaxHalo];
+    float xs[kTileTokens];
+    float red_mn[kPoolThreads / 32], red_mx[kPoolThreads / 32];
+};
+
+// One tile by kPoolThreads threads (tid = thread index within the group).
+// Chunks never straddle tiles (C divides 128); the halo is W/2 <= 64 tokens
+// clipped to the prompt. Per-chunk sums run in token order.
+__device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int tid, GroupBar g,
+                                          PoolShared& sh) {
+    const int b = search_base(a.tile_base, a.B, tile);
+    const int64_t i = tile - a.tile_base[b];
+    const int64_t start = a.seq_off[b];
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
+    const int64_t t0 = i * kTileTokens, t1 = min64(n, t0 + kTileTokens);
+    const int h = a.W / 2;
+    const int64_t lo = max64(0, t0 - h), hi = min64(n, t1 + h);
+    constexpr int kWin = (kTileTokens + 2 * kPoolMaxHalo + kPoolThreads - 1) / kPoolThreads;
+    float r[kWin];
+#pragma unroll
+    for (int k = 0; k < kWin; ++k) {
+        const int64_t u = lo + tid + k * kPoolThreads;
+        r[k] = u < hi ? __ldcg(a.imp + start + u) : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kWin; ++k) {
+        const int64_t u = lo + tid + k * kPoolThreads;
+        if (u < hi) sh.win[u - lo] = r[k];
+    }
+    g.sync();
+    float mn = INFINITY, mx = -INFINITY;
+    const int64_t tt = t0 + tid;
+    if (tt < t1) {
+        const int64_t u0 = max64(0, tt - h), u1 = min64(n - 1, tt + h);
+        float s = 0.0f;
+        for (int64_t u = u0; u <= u1; ++u) s += sh.win[u - lo];
+        const float x = s / static_cast<float>(u1 - u0 + 1);
+        a.tok[start + tt] = x;
+        sh.xs[tid] = x;
+        mn = x;
+        mx = x;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane == 0) {
+        sh.red_mn[warp] = mn;
+        sh.red_mx[warp] = mx;
+    }
+    g.sync();
+    if (tid == 0) {
+        for (int w = 1; w < kPoolThreads / 32; ++w) {
+            mn = fminf(mn, sh.red_mn[w]);
+            mx = fmaxf(mx, sh.red_mx[w]);
+        }
+        a.rpart[tile] = make_float2(mn, mx);
+    }
+    const int64_t c_lo = t0 / a.C, c_hi = (t1 + a.C - 1) / a.C;
+    for (int64_t c = c_lo + tid; c < c_hi; c += kPoolThreads) {
+        const int64_t a0 = c * a.C, a1 = min64(t1, a0 + a.C);
+        float sbx = 0.0f, sb = 0.0f;
+        for (int64_t t = a0; t < a1; ++t) {
+            float bx = sh.xs[t - t0], bb = 1.0f;
+            if (t < a.bf_n) {
+                bx *= a.bf_mult;
+                bb *= a.bf_mult;
+            }
+            if (t >= n - a.bl_n) {
+                bx *= a.bl_mult;
+                bb *= a.bl_mult;
+            }
+            sbx += bx;
+            sb += bb;
+        }
+        a.csum[a.chunk_off[b] + c] = make_float2(sbx, sb);
+    }
+    g.sync();  // the group's shared memory may be reused for the next tile
+}
+
+// ------------------------------------------------------ rank and gather
+constexpr int kRankThreads = 256;
+constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kWarpChunks = kSliceChunks / kRankWarps;  // chunks ranked by each warp
+static_assert(kSliceChunks == 32, "the gather scan uses one lane per chunk of a slice");
+
+struct PostArgs {
+    const int32_t* __restrict__ seq_off;
+    const int32_t* chunk_off;   // workspace copy
+    const int32_t* tile_base;
+    const int32_t* slice_base;
+    const float2* rpart;        // per pool tile: (min, max) of the pooled scores
+    const float2* csum;         // per chunk (sum boost * x, sum boost)
+    float* chunk_score;
+    uint8_t* keep;
+    int32_t* scount;            // kept tokens per slice
+    int32_t* kept_idx;
+    int32_t* kept_pos;
+    int32_t* kept_off;
+    int32_t* n_kept;
+    WsHeader* hdr;
+    int B, C, mode, normalize, force_bos, force_last;
+    float keep_p, mass;
+};
+
+struct RankShared {
+    float red_mn[kRankWarps], red_mx[kRankWarps];
+    unsigned long long red_u[kRankWarps];
+    float mn, mx;
+    unsigned long long need;
+    int all, S;
+    int32_t warp_cnt[kRankWarps];
+    int64_t red[kRankWarps];
+    int64_t base[kSliceChunks];
+};
+
+__device__ __forceinline__ int64_t chunk_tokens(int64_t n, int C, int64_t c) { return min64(C, n - c * C); }
+
+// Slice s (< number of slices) by kRankThreads threads; cs_s holds room for
+// the prompt's chunk scores (kMaxPromptChunks floats at most).
+//
+// Rebuilds every chunk score of the prompt (the min-max normalisation is
+// affine, so the chunk mean comes from the pool kernel's sums) and decides
+// the slice's chunks by their position in the order (score descending,
+// chunk index ascending): fixed mode keeps a chunk when fewer than
+// k = max(1, ceil(nc p)) chunks precede it, mass mode when the exact
+// fixed-point sum of the scores preceding it is below ceil(mass * total)
+// (the shortest prefix that reaches the mass, crossing chunk included).
+// The final chunk is forced. Writes the chunk scores, keep flags and the
+// slice's kept-token count (chunk 0 counts its BOS token when it is not
+// selected). The set equals that of the radix selection behind sp_select.
+__device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, GroupBar g,
+                                           float* cs_s, RankShared& sh) {
+    const int lane = t & 31, warp = t >> 5;
+    const int b = search_base(a.slice_base, a.B, s);
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - a.seq_off[b];
+    const int64_t coff = a.chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
+    if (nc > kMaxPromptChunks) {
+        // reported; the slice keeps nothing so that the gather stays in bounds
+        if (t == 0) {
+            atomicCAS(&a.hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
+            a.scount[s] = 0;
+        }
+        return;
+    }
+    const int64_t c_lo = (s - a.slice_base[b]) * kSliceChunks;
+    const int64_t c_hi = min64(nc, c_lo + kSliceChunks);
+
+    // each thread's first chunk sums and its tile min / max are requested
+    // together (one round trip); larger prompts loop
+    constexpr int kPre = 8;
+    float2 v[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int64_t c = t + k * kRankThreads;
+        v[k] = c < nc ? __ldcg(a.csum + coff + c) : make_float2(0.0f, 0.0f);
+    }
+    float mn = 0.0f, mx = 0.0f;
+    if (a.normalize) {
+        mn = INFINITY;
+        mx = -INFINITY;
+        for (int64_t p = a.tile_base[b] + t; p < a.tile_base[b + 1]; p += kRankThreads) {
+            const float2 r = __ldcg(a.rpart + p);
+            mn = fminf(mn, r.x);
+            mx = fmaxf(mx, r.y);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (lane == 0) {
+            sh.red_mn[warp] = mn;
+            sh.red_mx[warp] = mx;
+        }
+        g.sync();
+        if (t == 0) {
+            for (int w = 1; w < kRankWarps; ++w) {
+                mn = fminf(mn, sh.red_mn[w]);
+                mx = fmaxf(mx, sh.red_mx[w]);
+            }
+            sh.mn = mn;
+            sh.mx = mx;
+        }
+        g.sync();
+        mn = sh.mn;
+        mx = sh.mx;
+    }
+    float smax = 0.0f;
+    for (int64_t c0 = t;; c0 += kRankThreads * kPre) {
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int64_t c = c0 + k * kRankThreads;
+            if (c < nc) {
+                const float cs = chunk_score_from_sums(v[k].x, v[k].y, mn, mx, a.normalize,
+                                                       chunk_tokens(n, a.C, c));
+                cs_s[c] = cs;
+                smax = fmaxf(smax, cs);
+                if (c >= c_lo && c < c_hi) a.chunk_score[coff + c] = cs;
+            }
+        }
+        if (c0 + kRankThreads * kPre >= nc) break;
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int64_t c = c0 + kRankThreads * kPre + k * kRankThreads;
+            v[k] = c < nc ? __ldcg(a.csum + coff + c) : make_float2(0.0f, 0.0f);
+        }
+    }
+    const bool is_mass = a.mode == SP_MODE_MASS;
+    if (is_mass) {
+        for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        if (lane == 0) sh.red_mx[warp] = smax;
+    }
+    g.sync();  // cs_s complete (and the per-warp maxima)
+    if (is_mass) {
+        if (t == 0) {
+            float m = 0.0f;
+            for (int w = 0; w < kRankWarps; ++w) m = fmaxf(m, sh.red_mx[w]);
+            sh.S = mass_scale(nc, m);
+        }
+        g.sync();
+        const int S = sh.S;
+        uint64_t part = 0;
+        for (int64_t c = t; c < nc; c += kRankThreads) part += fixed_point(cs_s[c], S);
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) sh.red_u[warp] = part;
+        g.sync();
+        if (t == 0) {
+            unsigned long long tot = 0;
+            for (int w = 0; w < kRankWarps; ++w) tot += sh.red_u[w];
+            sh.all = tot == 0 ? 1 : 0;
+            sh.need = mass_threshold(tot, a.mass);
+        }
+    } else if (t == 0) {
+        sh.need = fixed_keep_count(nc, a.keep_p);
+        sh.all = 0;
+    }
+    g.sync();
+    const uint64_t need = sh.need;
+    const bool all = sh.all != 0;
+    const int S = is_mass ? sh.S : 0;
+
+    // warp w ranks chunks c_lo + w + kRankWarps * q of the slice: the count
+    // (fixed) or fixed-point mass (mass mode) of the chunks ordered before
+    // it. The order key (descending score, ascending index) is one 64-bit
+    // integer so that the comparison is branch-free.
+    int64_t ci[kWarpChunks];
+    uint64_t ki[kWarpChunks];
+    uint64_t acc[kWarpChunks];
+#pragma unroll
+    for (int q = 0; q < kWarpChunks; ++q) {
+        ci[q] = c_lo + warp + kRankWarps * q;
+        ki[q] = ci[q] < c_hi ? (static_cast<uint64_t>(score_desc_key(cs_s[ci[q]])) << 32) |
+                                   static_cast<uint32_t>(ci[q])
+                             : 0u;
+        acc[q] = 0;
+    }
+    if (!all) {
+        for (int j = lane; j < static_cast<int>(nc); j += 32) {
+            const float sj = cs_s[j];
+            const uint64_t kj = (static_cast<uint64_t>(score_desc_key(sj)) << 32) | static_cast<uint32_t>(j);
+            const uint64_t wj = is_mass ? fixed_point(sj, S) : 1u;
+#pragma unroll
+            for (int q = 0; q < kWarpChunks; ++q) acc[q] += kj < ki[q] ? wj : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < kWarpChunks; ++q)
+            for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+    }
+    if (lane == 0) {
+        int32_t my_cnt = 0;
+#pragma unroll
+        for (int q = 0; q < kWarpChunks; ++q) {
+            const int64_t c = ci[q];
+            if (c >= c_hi) continue;
+            // fixed: fewer than k chunks before it; mass: mass before it below the threshold
+            uint8_t f = (all || acc[q] < need) ? 1 : 0;
+            if (a.force_last && c == nc - 1) f |= 2;
+            a.keep[coff + c] = f;
+            my_cnt += static_cast<int32_t>(f ? chunk_tokens(n, a.C, c)
+                                             : ((c == 0 && a.force_bos && n > 0) ? 1 : 0));
+        }
+        sh.warp_cnt[warp] = my_cnt;
+    }
+    g.sync();
+    if (t == 0) {
+        int32_t tot = 0;
+        for (int w = 0; w < kRankWarps; ++w) tot += sh.warp_cnt[w];
+        a.scount[s] = tot;
+    }
+    g.sync();  // shared memory may be reused for the next slice
+}
+
+// Slice s in [0, S] by kRankThreads threads, S = number of slices: offsets
+// the slice by the kept tokens of all earlier slices and writes its kept
+// token indices and positions; s == S writes the batch total and the
+// offsets of prompts without tokens at the end of the batch.
+__device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int64_t S, int t, GroupBar g,
+                                             RankShared& sh) {
+    const int lane = t & 31, warp = t >> 5;
+    int64_t part = 0;
+    for (int64_t i = t; i < s; i += kRankThreads) part += __ldcg(a.scount + i);
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) sh.red[warp] = part;
+    g.sync();
+    int64_t P = 0;
+    for (int w = 0; w < kRankWarps; ++w) P += sh.red[w];
+    if (s == S) {
+        if (t == 0) {
+            for (int b = a.B - 1; b >= 0 && a.slice_base[b] == S; --b) a.kept_off[b] = static_cast<int32_t>(P);
+            a.kept_off[a.B] = static_cast<int32_t>(P);
+            *a.n_kept = static_cast<int32_t>(P);
+        }
+        g.sync();
+        return;
+    }
+    const int b = search_base(a.slice_base, a.B, s);
+    if (t == 0 && s == a.slice_base[b]) {
+        // first slice of prompt b: its offset, and that of empty prompts before it
+        for (int bb = b; bb >= 0 && a.slice_base[bb] == s; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
+    }
+    const int64_t start = a.seq_off[b];
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
+    const int64_t coff = a.chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
+    const bool ok = nc <= kMaxPromptChunks;  // else reported by the rank; nothing kept
+    const int64_t c_lo = (s - a.slice_base[b]) * kSliceChunks;
+    // exclusive scan of the slice's per-chunk kept tokens (lane = chunk)
+    if (warp == 0) {
+        const int64_t c = c_lo + lane;
+        int64_t cnt = 0;
+        if (ok && c < nc) {
+            const uint8_t f = __ldcg(a.keep + coff + c);
+            cnt = f ? chunk_tokens(n, a.C, c) : ((c == 0 && a.force_bos && n > 0) ? 1 : 0);
+        }
+        int64_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        sh.base[lane] = P + incl - cnt;
+    }
+    g.sync();
+    if (ok) {
+        for (int q = warp; q < kSliceChunks; q += kRankWarps) {
+            const int64_t c = c_lo + q;
+            if (c >= nc) break;
+            const int64_t base = sh.base[q];
+            if (__ldcg(a.keep + coff + c)) {
+                const int64_t a0 = c * a.C, a1 = min64(n, a0 + a.C);
+                for (int64_t tt = a0 + lane; tt < a1; tt += 32) {
+                    a.kept_idx[base + (tt - a0)] = static_cast<int32_t>(start + tt);
+                    a.kept_pos[base + (tt - a0)] = static_cast<int32_t>(tt);
+                }
+            } else if (c == 0 && a.force_bos && n > 0 && lane == 0) {
+                a.kept_idx[base] = static_cast<int32_t>(start);
+                a.kept_pos[base] = 0;
+            }
+        }
+    }
+    g.sync();
+}
+
+}  // namespace sp

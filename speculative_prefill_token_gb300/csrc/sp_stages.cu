@@ -20,6 +20,7 @@
 
 #include "sp_device.cuh"
 #include "sp_internal.h"
+#include "sp_phases.cuh"
 #include "sp_select.cuh"
 
 namespace sp {
@@ -127,32 +128,47 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 }
 
 // --------------------------------------------------------------- reduce
-// Token importance. One CTA covers TOK = 1024 / Rs tokens of one tile; thread
-// (token, quad) loads the quad's four raw logits of 4 slabs of the wave at a
-// time (coalesced 16-byte loads; few registers keep many CTAs resident) and keeps the max over slabs of
-// scale2 * s - lse2 (log2 of the softmax probability). One thread per token
-// then takes the max over the G heads of each lookahead step, combines it
-// with earlier waves, and (last wave) writes
+// Token importance from the wave's quantised logits. One CTA covers TOK =
+// 2048 / Rs tokens of one tile (Rs / 8 threads per token, 8 rows each):
+// every thread loads its eight 16-bit values of every slab (16 bytes,
+// coalesced) and keeps the max over slabs of
+// y - lse2 = (M - lse2) - q / kLogitQuant, the log2 softmax probability,
+// with M - lse2 taken from a per-CTA table [warp quarter][slab][row]. One
+// thread per token then takes the max over the G heads of each lookahead
+// step, combines it with earlier waves, and (last wave) writes
 // imp[t] = (1/L) sum_l exp2(max over layers, heads).
 constexpr int kReduceThreads = 256;
 constexpr int kReduceSlabBatch = 4;
 
-__global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
-    const float* logits, const float* lse2, const int32_t* seq_off, const int32_t* tile_base,
-    float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab, int64_t Ntot,
-    int64_t rows_per_slab, float scale2, int first_wave, int last_wave, const int32_t* bad) {
+__global__ void __launch_bounds__(kReduceThreads, 4) reduce_kernel(
+    const uint16_t* logits, const float* lmax, const float* lse2, const int32_t* seq_off,
+    const int32_t* tile_base, float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab,
+    int64_t Ntot, int64_t rows_per_slab, int64_t tiles_max, int first_wave, int last_wave,
+    const int32_t* bad) {
     grid_dep_wait();
     grid_dep_launch();
-    if (*bad) return;
-    const int Q4 = Rs / 4;
-    const int TOK = kReduceThreads / Q4;
+    const int Q8 = Rs / 8;
+    const int TOK = kReduceThreads / Q8;
     const int subs = kTileTokens / TOK;
     const int64_t tile = blockIdx.x / subs;
     const int sub = blockIdx.x - static_cast<int>(tile) * subs;
+    const int tq = threadIdx.x / Q8, c = threadIdx.x - tq * Q8;
+    const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
+    const uint4* src = reinterpret_cast<const uint4*>(logits + row * Rs + 8 * c);
+    const int64_t slab_stride = rows_per_slab * Rs / 8;  // in 16-byte units
+    // the first batch depends on the block index only (every tile slot of the
+    // scratch exists), so it is requested before the offsets and maxima;
+    // later batches while the current one is reduced
+    uint4 v[kReduceSlabBatch];
+#pragma unroll
+    for (int u = 0; u < kReduceSlabBatch; ++u)
+        if (u < nslab) v[u] = __ldcs(src + u * slab_stride);
+    if (*bad) return;
     if (tile >= tile_base[B]) return;
     extern __shared__ float sm[];
-    float* lse_s = sm;                  // [nslab][Rs]
-    float* ms = lse_s + nslab * Rs;     // [TOK][Rs + 1]
+    const int q0 = sub * TOK / 32, nq = (TOK + 31) / 32;  // warp quarters of the CTA's tokens
+    float* off_s = sm;                       // [nq][nslab][Rs]: M - lse2
+    float* ms = off_s + nq * nslab * Rs;     // [TOK][Rs + 1]
     const int b = search_base(tile_base, B, tile);
     const int64_t i = tile - tile_base[b];
     const int64_t start = seq_off[b];
@@ -160,46 +176,40 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
     const int64_t first = i * kTileTokens + static_cast<int64_t>(sub) * TOK;  // within the prompt
     const int nvalid = static_cast<int>(min64(TOK, n - first));
     if (nvalid <= 0) return;
-    const int tq = threadIdx.x / Q4, c = threadIdx.x - tq * Q4;
     const bool act = tq < nvalid;
-    const int64_t row = tile * kTileTokens + static_cast<int64_t>(sub) * TOK + tq;
-    const float* src = logits + row * Rs + 4 * c;
-    const int64_t slab_stride = rows_per_slab * Rs;
-    // the first batch of logits is requested before the normalisers, and
-    // later batches while the current one is reduced: no barrier in the loop
-    float4 v[kReduceSlabBatch];
-#pragma unroll
-    for (int u = 0; u < kReduceSlabBatch; ++u)
-        if (act && u < nslab) v[u] = __ldcs(reinterpret_cast<const float4*>(src + u * slab_stride));
-    for (int idx = threadIdx.x; idx < nslab * Rs; idx += kReduceThreads) {
-        const int s = idx / Rs, r = idx - s * Rs;
-        lse_s[idx] = lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
+    for (int idx = threadIdx.x; idx < nq * nslab * Rs; idx += kReduceThreads) {
+        const int qq = idx / (nslab * Rs), rem = idx - qq * nslab * Rs;
+        const int s = rem / Rs, r = rem - s * Rs;
+        off_s[idx] = lmax[((static_cast<int64_t>(s) * tiles_max + tile) * 4 + q0 + qq) * Rs + r] -
+                     lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
     }
     __syncthreads();
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    const float* ot = off_s + (tq / 32) * nslab * Rs + 8 * c;  // this token's quarter
+    float m[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
     for (int s0 = 0; s0 < nslab; s0 += kReduceSlabBatch) {
 #pragma unroll
         for (int u = 0; u < kReduceSlabBatch; ++u) {
             if (act && s0 + u < nslab) {
-                const float* ls = lse_s + (s0 + u) * Rs + 4 * c;
-                m0 = fmaxf(m0, fmaf(v[u].x, scale2, -ls[0]));
-                m1 = fmaxf(m1, fmaf(v[u].y, scale2, -ls[1]));
-                m2 = fmaxf(m2, fmaf(v[u].z, scale2, -ls[2]));
-                m3 = fmaxf(m3, fmaf(v[u].w, scale2, -ls[3]));
+                const float* os = ot + (s0 + u) * Rs;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    m[2 * k] = fmaxf(m[2 * k], fmaf(-static_cast<float>(w[k] & 0xffffu), kLogitQuantInv, os[2 * k]));
+                    m[2 * k + 1] = fmaxf(m[2 * k + 1], fmaf(-static_cast<float>(w[k] >> 16), kLogitQuantInv, os[2 * k + 1]));
+                }
             }
         }
         const int s1 = s0 + kReduceSlabBatch;
 #pragma unroll
         for (int u = 0; u < kReduceSlabBatch; ++u)
-            if (act && s1 + u < nslab)
-                v[u] = __ldcs(reinterpret_cast<const float4*>(src + (s1 + u) * slab_stride));
+            if (act && s1 + u < nslab) v[u] = __ldcs(src + (s1 + u) * slab_stride);
     }
-    if (tq < nvalid) {
-        float* mrow = ms + tq * (Rs + 1) + 4 * c;
-        mrow[0] = m0;
-        mrow[1] = m1;
-        mrow[2] = m2;
-        mrow[3] = m3;
+    if (act) {
+        float* mrow = ms + tq * (Rs + 1) + 8 * c;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mrow[k] = m[k];
     }
     __syncthreads();
     const int t = threadIdx.x;
@@ -219,94 +229,15 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
 }
 
 // --------------------------------------------------------- pool + chunk sums
-// Fused-path pooling: one CTA per 128-token tile of a prompt (chunks never
-// straddle tiles: C divides 128). Loads imp of the tile plus a W/2 halo
-// (clipped to the prompt) into shared memory with all loads in flight,
-// writes the pooled scores x, their min / max (per tile) and, per chunk,
-// S_bx = sum boost(t) * x(t) and S_b = sum boost(t) in token order.
-constexpr int kPoolThreads = 128;
-constexpr int kPoolMaxHalo = 64;
-
-__global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(
-    const float* imp, float* tok, float2* rpart, float2* csum, const int32_t* seq_off,
-    const int32_t* tile_base, const int32_t* chunk_off, int B, int W, int C, int bf_n,
-    float bf_mult, int bl_n, float bl_mult, const int32_t* bad) {
+// Fused-path pooling: one CTA per 128-token tile of a prompt (pool_tile).
+__global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(const PoolArgs a, const int32_t* bad) {
     grid_dep_wait();
     grid_dep_launch();
     if (*bad) return;
     const int64_t tile = blockIdx.x;
-    if (tile >= tile_base[B]) return;
-    __shared__ float win[kTileTokens + 2 * kPoolMaxHalo];
-    __shared__ float xs[kTileTokens];
-    __shared__ float red_mn[kPoolThreads / 32], red_mx[kPoolThreads / 32];
-    const int b = search_base(tile_base, B, tile);
-    const int64_t i = tile - tile_base[b];
-    const int64_t start = seq_off[b];
-    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
-    const int64_t t0 = i * kTileTokens, t1 = min64(n, t0 + kTileTokens);
-    const int h = W / 2;
-    const int64_t lo = max64(0, t0 - h), hi = min64(n, t1 + h);
-    constexpr int kWin = (kTileTokens + 2 * kPoolMaxHalo + kPoolThreads - 1) / kPoolThreads;
-    float r[kWin];
-#pragma unroll
-    for (int k = 0; k < kWin; ++k) {
-        const int64_t u = lo + threadIdx.x + k * kPoolThreads;
-        r[k] = u < hi ? imp[start + u] : 0.0f;
-    }
-#pragma unroll
-    for (int k = 0; k < kWin; ++k) {
-        const int64_t u = lo + threadIdx.x + k * kPoolThreads;
-        if (u < hi) win[u - lo] = r[k];
-    }
-    __syncthreads();
-    float mn = INFINITY, mx = -INFINITY;
-    const int64_t tt = t0 + threadIdx.x;
-    if (tt < t1) {
-        const int64_t u0 = max64(0, tt - h), u1 = min64(n - 1, tt + h);
-        float s = 0.0f;
-        for (int64_t u = u0; u <= u1; ++u) s += win[u - lo];
-        const float x = s / static_cast<float>(u1 - u0 + 1);
-        tok[start + tt] = x;
-        xs[threadIdx.x] = x;
-        mn = x;
-        mx = x;
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) {
-        red_mn[warp] = mn;
-        red_mx[warp] = mx;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < kPoolThreads / 32; ++w) {
-            mn = fminf(mn, red_mn[w]);
-            mx = fmaxf(mx, red_mx[w]);
-        }
-        rpart[tile] = make_float2(mn, mx);
-    }
-    const int64_t c_lo = t0 / C, c_hi = (t1 + C - 1) / C;
-    for (int64_t c = c_lo + threadIdx.x; c < c_hi; c += kPoolThreads) {
-        const int64_t a0 = c * C, a1 = min64(t1, a0 + C);
-        float sbx = 0.0f, sb = 0.0f;
-        for (int64_t t = a0; t < a1; ++t) {
-            float bx = xs[t - t0], bb = 1.0f;
-            if (t < bf_n) {
-                bx *= bf_mult;
-                bb *= bf_mult;
-            }
-            if (t >= n - bl_n) {
-                bx *= bl_mult;
-                bb *= bl_mult;
-            }
-            sbx += bx;
-            sb += bb;
-        }
-        csum[chunk_off[b] + c] = make_float2(sbx, sb);
-    }
+    if (tile >= a.tile_base[a.B]) return;
+    __shared__ PoolShared sh;
+    pool_tile(a, tile, threadIdx.x, GroupBar{1, kPoolThreads}, sh);
 }
 
 // ----------------------------------------------------------------- pool
@@ -617,8 +548,9 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
 
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
                           float* imp, cudaStream_t st) {
-    const int tok = kReduceThreads / (pl.Rs / 4);
-    const size_t smem = sizeof(float) * (static_cast<size_t>(nslab) * pl.Rs +
+    const int tok = kReduceThreads / (pl.Rs / 8);
+    const int nq = (tok + 31) / 32;
+    const size_t smem = sizeof(float) * (static_cast<size_t>(nq) * nslab * pl.Rs +
                                          static_cast<size_t>(tok) * (pl.Rs + 1));
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -626,20 +558,37 @@ cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int 
         if (e != cudaSuccess) return e;
     }
     const unsigned grid = static_cast<unsigned>(pl.tiles_max * (kTileTokens / tok));
-    return launch_k(reduce_kernel, grid, kReduceThreads, smem, st,
-        ws_ptr<float>(ws, pl.o_logits), ws_ptr<float>(ws, pl.o_lse), seq_off,
-        ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
-        pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.scale2, wave == 0 ? 1 : 0,
-        wave == pl.waves - 1 ? 1 : 0, &ws_ptr<WsHeader>(ws, 0)->bad_input);
+    return launch_k(reduce_kernel, grid, kReduceThreads, smem, st, ws_ptr<uint16_t>(ws, pl.o_logits),
+                    ws_ptr<float>(ws, pl.o_lmax), ws_ptr<float>(ws, pl.o_lse), seq_off,
+                    ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
+                    pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.tiles_max,
+                    wave == 0 ? 1 : 0, wave == pl.waves - 1 ? 1 : 0, &ws_ptr<WsHeader>(ws, 0)->bad_input);
+}
+
+PoolArgs pool_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, const float* imp,
+                   float* tok, void* ws) {
+    PoolArgs a;
+    a.imp = imp;
+    a.tok = tok;
+    a.rpart = ws_ptr<float2>(ws, pl.o_rpart);
+    a.csum = ws_ptr<float2>(ws, pl.o_csum);
+    a.seq_off = seq_off;
+    a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
+    a.chunk_off = ws_ptr<int32_t>(ws, pl.o_chunk_off);
+    a.B = pl.B;
+    a.W = p->pool_w;
+    a.C = pl.C;
+    a.bf_n = p->boost_first_n;
+    a.bl_n = p->boost_last_n;
+    a.bf_mult = p->boost_first_mult;
+    a.bl_mult = p->boost_last_mult;
+    return a;
 }
 
 cudaError_t launch_pool_sums(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                              const float* imp, float* tok, void* ws, cudaStream_t st) {
     return launch_k(pool_sums_kernel, static_cast<unsigned>(pl.tiles_max), kPoolThreads, 0, st,
-        imp, tok, ws_ptr<float2>(ws, pl.o_rpart), ws_ptr<float2>(ws, pl.o_csum), seq_off,
-        ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<int32_t>(ws, pl.o_chunk_off), pl.B, p->pool_w,
-        pl.C, p->boost_first_n, p->boost_first_mult, p->boost_last_n, p->boost_last_mult,
-        &ws_ptr<WsHeader>(ws, 0)->bad_input);
+                    pool_args(pl, p, seq_off, imp, tok, ws), &ws_ptr<WsHeader>(ws, 0)->bad_input);
 }
 
 cudaError_t launch_pool(const Plan& pl, const sp_params* p, const int32_t* seq_off,
