@@ -36,7 +36,10 @@ N_COPIES = 4
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the logits kernel from one ncu capture
 # (profiles/logits_tc_draft2b.md), valid while the kernel source hash matches.
-TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+# DRAM bytes (read + write) of one logits-kernel launch on this workload, from
+# an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
+# only while the kernel sources are the ones that were measured.
+TRAFFIC = {"source_sha1": "ab108530b11887b1a0723e662f82f69765fd40fe", "bytes_per_launch": 213695744}
 
 
 def parse():
@@ -66,10 +69,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+LOGITS_SOURCES = ("sp_logits_tc.cu", "sp_logits_phase.cuh", "sp_ptx.cuh", "sp_device.cuh")
+
+
 def kernel_sha1():
-    p = os.path.join(ROOT, "speculative_prefill_token_gb300", "csrc", "sp_logits_tc.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+    """Digest of the sources that define the logits kernel (the recorded
+    DRAM traffic is only reported while they are unchanged)."""
+    h = hashlib.sha1()
+    for name in LOGITS_SOURCES:
+        with open(os.path.join(ROOT, "speculative_prefill_token_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class RawEvents:
