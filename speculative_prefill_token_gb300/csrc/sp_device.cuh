@@ -152,6 +152,33 @@ __device__ __forceinline__ void stats_flush(RowStats<NH>& st, float2* sm, int qw
     stats_reset(st);
 }
 
+// Reduce per-lane running row statistics of one 128-thread warpgroup (4
+// warps, warp qw; lane r holds the (max, sum of exp2(y - max)) pair of row
+// hh * 32 + r over its warp's tokens) to one pair per row, write rows < R to
+// out[r] and reset the pairs. sm is a [4][64] float2 scratch, bar_id a named
+// barrier of the warpgroup.
+template <int NH>
+__device__ __forceinline__ void flush_rows(float2 (&run)[NH], float2* sm, int qw, int bar_id, float2* out,
+                                           int R) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) sm[qw * 64 + hh * 32 + lane] = run[hh];
+    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+    if (qw == 0) {
+        for (int r = lane; r < R; r += 32) {
+            float2 acc = sm[r];
+            acc = merge_partial(acc, sm[64 + r]);
+            acc = merge_partial(acc, sm[128 + r]);
+            acc = merge_partial(acc, sm[192 + r]);
+            out[r] = acc;
+        }
+        __threadfence();
+    }
+    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) run[hh] = make_float2(-INFINITY, 0.0f);
+}
+
 // Work split of the logits kernels: CTA c of C owns flattened items
 // [floor(W*c/C), floor(W*(c+1)/C)). owner(w) = the CTA owning item w.
 __device__ __forceinline__ int64_t split_start(int64_t W, int64_t C, int64_t c) { return (W * c) / C; }

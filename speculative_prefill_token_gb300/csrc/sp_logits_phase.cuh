@@ -19,13 +19,15 @@
 //               (slab, prompt) into one of two buffers;
 //   warp 9      tcgen05.mma issuer (one thread) and TMEM owner;
 //   warps 0-7   two epilogue warpgroups; warpgroup e drains TMEM accumulator
-//               e (tiles alternate), stages the tile's logits in swizzled
-//               shared memory for one TMA store into the scratch (one
-//               128-token slot per tile), and keeps per-thread running
-//               softmax statistics (row max reference, sum of exp2) that it
-//               reduces across threads once per (slab, prompt) segment; the
-//               last contribution to a segment merges its records into the
-//               segment's log2 normaliser.
+//               e (tiles alternate). Per tile, each warp (32 tokens) takes
+//               the row maxima M of the scaled logits (butterfly), stages the
+//               tile's logits as 16-bit M - y in shared memory for one TMA
+//               store into the scratch (one 128-token slot per tile), and
+//               sums exp2(y - M) per row (butterfly); lane r merges the pair
+//               into its running softmax statistics of row r. Once per (slab,
+//               prompt) segment the four warps' pairs are merged into a
+//               record; the last contribution to a segment merges its
+//               records into the segment's log2 normaliser.
 // Every mbarrier wait is bounded; a wait that gives up records
 // SP_ERR_TIMEOUT in the workspace status word, and the CTA then drains its
 // own copies, stores and MMAs in flight before it leaves the phase.
@@ -100,26 +102,49 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
 }
 
 struct Item {
-    int slab;      // local slab index in [0, nslab)
-    int b;         // prompt
-    int64_t tile;  // flattened tile index of the slab (scratch slot)
-    int64_t tok0;  // first global token of the tile
-    int nvalid;    // tokens of the tile inside the prompt
+    int slab;    // local slab index in [0, nslab)
+    int b;       // prompt
+    int tile;    // flattened tile index of the slab (scratch slot)
+    int tok0;    // first global token of the tile (token counts fit 31 bits)
+    int nvalid;  // tokens of the tile inside the prompt
 };
 
-__device__ __forceinline__ Item decode(const TcArgs& a, int64_t w, int64_t T) {
+// Walks a CTA's contiguous range of work items. Consecutive items are
+// consecutive tiles of one prompt except at prompt and slab boundaries, so
+// only those re-read the offsets; every other step is arithmetic.
+struct ItemCursor {
     Item it;
-    it.slab = static_cast<int>(w / T);
-    it.tile = w - static_cast<int64_t>(it.slab) * T;
-    it.b = search_base(a.tile_base, a.B, it.tile);
-    const int64_t i = it.tile - a.tile_base[it.b];
-    const int64_t start = a.seq_off[it.b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[it.b + 1]) - start;
-    it.tok0 = start + i * kTileTokens;
-    const int64_t rem = n - i * kTileTokens;
-    it.nvalid = static_cast<int>(rem < kTileTokens ? rem : kTileTokens);
-    return it;
-}
+    int base_b;  // first tile of the current prompt
+    int next_b;  // first tile of the next prompt
+    int start, n;
+
+    __device__ __forceinline__ void set(const TcArgs& a, int64_t w, int64_t T) {
+        it.slab = static_cast<int>(w / T);
+        it.tile = static_cast<int>(w - static_cast<int64_t>(it.slab) * T);
+        it.b = search_base(a.tile_base, a.B, it.tile);
+        base_b = a.tile_base[it.b];
+        next_b = a.tile_base[it.b + 1];
+        start = a.seq_off[it.b];
+        n = a.seq_off[it.b + 1] - start;
+        place();
+    }
+    __device__ __forceinline__ void place() {
+        const int i = it.tile - base_b;
+        it.tok0 = start + i * kTileTokens;
+        const int rem = n - i * kTileTokens;
+        it.nvalid = rem < kTileTokens ? rem : kTileTokens;
+    }
+    // Moves to item w, the successor of the current one.
+    __device__ __forceinline__ void next(const TcArgs& a, int64_t w, int64_t T) {
+        const int tile = it.tile + 1;
+        if (tile < next_b && tile < T) {
+            it.tile = tile;
+            place();
+        } else {
+            set(a, w, T);
+        }
+    }
+};
 
 __device__ __forceinline__ void record_timeout(const TcArgs& a, volatile int* abort_flag) {
     *abort_flag = 1;
@@ -251,8 +276,11 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             bool issued[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
             bool ok = true;
+            ItemCursor cur;
             for (int64_t w = w_begin; w < w_end && ok; ++w) {
-                const Item it = decode(a, w, T);
+                if (w == w_begin) cur.set(a, w, T);
+                else cur.next(a, w, T);
+                const Item& it = cur.it;
                 const int slab = a.slab0 + it.slab;
                 const int layer = slab / a.Hk, g = slab - layer * a.Hk;
                 const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
@@ -279,7 +307,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                     }
                     mbar_arrive_expect_tx(bar_full + 8 * stage, kKBlockBytes);
                     tma_load_4d(k_ring + stage * kKBlockBytes, tmap_k, bar_full + 8 * stage,
-                                kb * 64, static_cast<int>(it.tok0), g, layer, pol);
+                                kb * 64, it.tok0, g, layer, pol);
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == a.stages) {
@@ -307,8 +335,11 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             int qb = 0;
             bool ok = true;
             bool any_mma = false;
+            ItemCursor cur;
             for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
-                const Item it = decode(a, w, T);
+                if (w == w_begin) cur.set(a, w, T);
+                else cur.next(a, w, T);
+                const Item& it = cur.it;
                 const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
                 if (key != prev_key) {
                     if (qn > 0) tc_commit(bar_qempty + 8 * ((qn - 1) & 1));
@@ -371,19 +402,24 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
         float2* st_sm = stats + e * 4 * 64;
         volatile int* seg_flag = reinterpret_cast<volatile int*>(smem + L.seg_flag) + e;
         const int tl = qw * 32 + lane;   // token row of the tile
-        RowStats<NH> rs;
-        stats_reset(rs);
+        // running softmax statistics of row hh * 32 + lane over this warp's
+        // tokens of the current segment: (reference max, sum of exp2(y - max))
+        float2 run[NH];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) run[hh] = make_float2(-INFINITY, 0.0f);
         int64_t cur_key = -1;
         bool stores = false;
         bool ok = true;
         int64_t j = 0;
+        ItemCursor cur;
         for (int64_t w = w_begin; w < w_end; ++w, ++j) {
-            const Item it = decode(a, w, T);
+            if (w == w_begin) cur.set(a, w, T);
+            else cur.next(a, w, T);
+            const Item& it = cur.it;
             const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
             if (key != cur_key) {
                 if (cur_key >= 0) {
-                    stats_flush<NH>(rs, st_sm, qw, bar_id,
-                                    a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
+                    flush_rows<NH>(run, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
                     segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
                                  a.R, a.Rs, st_sm, seg_flag, qw, bar_id);
                 }
@@ -412,8 +448,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                 for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
                     if (hh * 32 + r >= a.Nmma) v[hh][r] = 0.0f;
             const bool valid = tl < it.nvalid;
-            if (valid) stats_add<NH>(rs, v, a.scale2);
-            // row maxima of the scaled logits over the warp quarter's valid tokens
+            // row maxima M of the scaled logits over the warp quarter's valid tokens
             float m_own[NH];
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh) {
@@ -431,7 +466,8 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             tc_fence_before();
             mbar_arrive(bar_tempty + 8 * acc);
 
-            // stage the quantised logits and store the tile with TMA
+            // quantised row against M, and exp2(y - M) of the valid tokens for
+            // the quarter's softmax partial
             if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
             asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
 #pragma unroll
@@ -441,18 +477,23 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                 for (int r = 0; r < 32; r += 2) {
                     const float M0 = __shfl_sync(0xffffffffu, m_own[hh], r);
                     const float M1 = __shfl_sync(0xffffffffu, m_own[hh], r + 1);
-                    pk[r / 2] = quant_logit(M0, v[hh][r] * a.scale2) |
-                                (quant_logit(M1, v[hh][r + 1] * a.scale2) << 16);
+                    const float y0 = v[hh][r] * a.scale2, y1 = v[hh][r + 1] * a.scale2;
+                    pk[r / 2] = quant_logit(M0, y0) | (quant_logit(M1, y1) << 16);
+                    v[hh][r] = valid ? exp2f(y0 - M0) : 0.0f;
+                    v[hh][r + 1] = valid ? exp2f(y1 - M1) : 0.0f;
                 }
                 uint4* row = reinterpret_cast<uint4*>(out_buf + hh * kStageOutBytes + tl * 64);
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
                     row[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                // lane r: this tile's (M, sum) of row hh * 32 + r, merged into the running pair
+                const float z = warp_rows_reduce<false>(v[hh]);
+                run[hh] = merge_partial(run[hh], make_float2(m_own[hh], z));
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
             if (qw == 0 && lane == 0) {
-                const int y = static_cast<int>(it.tile * kTileTokens);
+                const int y = it.tile * kTileTokens;
 #pragma unroll
                 for (int hh = 0; hh < NH; ++hh)
                     tma_store_3d(tmap_s, out_addr + hh * kStageOutBytes, hh * 32, y, it.slab);
@@ -461,8 +502,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             }
         }
         if (ok && cur_key >= 0) {
-            stats_flush<NH>(rs, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs,
-                            a.R);
+            flush_rows<NH>(run, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
             segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
                          a.Rs, st_sm, seg_flag, qw, bar_id);
         }
