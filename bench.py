@@ -12,6 +12,10 @@ seeded synthetic inputs already resident in HBM. Prints one JSON line.
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path has no cross-GPU exchange); the reported value is the tokens all
 ranks scored divided by the slowest rank's time.
+
+`value` is the single-stream rate (one call after another on one stream).
+`pipelined` reports, beside it, the rate with --pipeline-streams calls in
+flight on as many streams, each with its own workspace and outputs.
 """
 
 import argparse
@@ -50,6 +54,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pipeline-streams", type=int, default=3,
+                    help="streams of the extra pipelined-throughput measurement (0: skip)")
     return ap.parse_args()
 
 
@@ -333,6 +339,41 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = q_np.nbytes + k_np.nbytes + off_host.numel() * 4
+
+    # pipelined throughput (reported beside the headline, which stays the
+    # single-stream number): S calls in flight on S streams, each with its
+    # own workspace and outputs, as a server scoring a stream of requests
+    # would run them; one call's latency-bound selection overlaps the next
+    # call's key stream
+    pipelined = None
+    S = args.pipeline_streams
+    if S > 1:
+        p_streams = [torch.cuda.Stream(device=dev) for _ in range(S)]
+        p_ws = [sp.make_workspace(shape, params, dev) for _ in range(S)]
+        p_out = [sp.alloc_outputs(qs[0], ks[0], params, intermediates=False) for _ in range(S)]
+
+        def p_step(i):
+            j = i % S
+            sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, params, out=p_out[j], ws=p_ws[j],
+                                 stream=p_streams[j])
+
+        for i in range(max(args.warmup, S)):
+            p_step(i)
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for ps in p_streams:
+            ps.wait_stream(stream)
+        for i in range(args.steps):
+            p_step(i)
+        for ps in p_streams:
+            stream.wait_stream(ps)
+        p1.record(stream)
+        torch.cuda.synchronize()
+        p_ms = p0.elapsed_time(p1)
+        p_ok = all(sp.device_status(x) == 0 for x in p_ws)
+        pipelined = {"streams": S, "value": world * ntot * args.steps / (p_ms / 1e3), "unit": UNIT,
+                     "ms_per_step": p_ms / args.steps, "device_status_ok": p_ok}
     d2h = 2 * ntot * 4 + koff_host.numel() * 4 + 4
 
     # max over ranks of the timed region
@@ -371,6 +412,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": world * ntot / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
+        "pipelined": pipelined,
         "kept_tokens": n_kept, "device_status": status,
     }
     if not args.no_cpu_baseline:

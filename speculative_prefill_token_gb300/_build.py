@@ -28,6 +28,7 @@ def _nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    files.append(os.path.abspath(__file__))  # a changed source list rebuilds too
     return files
 
 

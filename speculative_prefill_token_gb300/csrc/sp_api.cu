@@ -216,7 +216,7 @@ int sp_kernels_per_call(const sp_shape* shape, const sp_params* params, int32_t*
     const int rc = make_plan(shape, params, &pl);
     if (rc != SP_OK) return rc;
     if (!n_kernels) return SP_ERR_INVALID_ARG;
-    // prep, (logits, reduce) per wave, then pool sums, rank, gather or
+    // prep, (logits, importance) per wave, then pool sums, rank, gather or
     // pool, chunk, select, gather scan, gather write
     *n_kernels = 1 + 2 * pl.waves + (fused_post_ok(params) ? 3 : 5);
     return SP_OK;

@@ -421,4 +421,11 @@ __device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int64
     g.sync();
 }
 
+// Host-side argument builders (sp_stages.cu, sp_post.cu).
+PoolArgs pool_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, const float* imp,
+                   float* tok, void* ws);
+PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, float* chunk_score,
+                   uint8_t* keep, int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off,
+                   int32_t* n_kept, void* ws);
+
 }  // namespace sp

@@ -32,7 +32,7 @@ __device__ __forceinline__ void set_status(WsHeader* h, int code) { atomicCAS(&h
 // One CTA: validates seq_off (0 = first, non-decreasing, last = Ntot) and
 // writes the per-prompt bases of logits tiles, chunks and post blocks.
 // A user-provided chunk_off (standalone select/gather) must match.
-constexpr int kPrepThreads = 1024;
+constexpr int kPrepThreads = 256;  // small enough to share an SM with the logits kernel
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_off, int B,
                                                             int64_t Ntot, int C, int64_t Tb,

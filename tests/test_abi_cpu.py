@@ -75,7 +75,7 @@ def test_workspace_size_valid(lib):
 
 
 def test_kernels_per_call(lib):
-    # one wave of 12 slabs: prep, logits, reduce, pool sums, rank, gather
+    # one wave of 12 slabs: prep, logits, importance, pool sums, rank, gather
     assert sp.kernels_per_call(_shape(), sp.SelectionParams(mode="fixed", keep_p=0.15)) == 6
     # a pool window wider than the fused kernel's halo takes the staged path
     # (pool, chunk, select, gather scan instead of pool sums + post)
