@@ -14,6 +14,7 @@ from .specprefill_oracle import (  # noqa: F401
     chunk_offsets,
     decode_bf16,
     finish_selection,
+    gather_rows,
     fixed_count,
     min_max_normalize,
     rank_order,

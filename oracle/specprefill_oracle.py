@@ -31,6 +31,10 @@ plain numpy float64 (inputs are bf16 bit patterns decoded exactly):
    item 4)
 12. kept-token list with original position IDs                (guide §How It
    Works / Sparse Prefill)
+13. rows of the kept tokens gathered from a token-major cache
+   tensor, in kept-list order, for the target's sparse prefill (same
+   section: only the kept tokens are prefilled; listing of the sparse pass
+   adds kept[i] with its position to the target batch)
 
 Readings where the pages are silent (each also listed in the design notes):
 softmax over the prompt keys only; kv head = h // G; the pool divides by the
@@ -331,3 +335,21 @@ def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
     if keep_step_max:
         out["step_max"] = steps
     return out
+
+
+# ---------------------------------------------------------------------------
+# 13. sparse-prefill consumer: the kept tokens' rows of a cache tensor
+
+
+def gather_rows(cache: np.ndarray, kept_idx: Sequence[int]) -> np.ndarray:
+    """Rows of the kept tokens of a token-major cache tensor.
+
+    cache: [Ly, Ntot, Hk, d] (any dtype; bf16 bit patterns pass through
+    unchanged); kept_idx: packed token indices from the selection.
+    Returns [Ly, len(kept_idx), Hk, d] with row i = cache[:, kept_idx[i]]
+    ("SpecPrefill — Implementation Guide", §How It Works / Sparse Prefill:
+    the target prefills only the kept tokens, each with its original
+    position).
+    """
+    idx = np.asarray(kept_idx, dtype=np.int64)
+    return np.asarray(cache)[:, idx]

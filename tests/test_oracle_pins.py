@@ -283,3 +283,28 @@ def test_bf16_decode_exact():
     # bf16 keeps 8 significant bits: these are all representable except 1e-3
     np.testing.assert_array_equal(dec[[0, 1, 2, 3, 5]], vals[[0, 1, 2, 3, 5]].astype(np.float64))
     assert abs(dec[4] - 1e-3) <= 1e-3 * 2.0 ** -8
+
+
+# --- sparse-prefill consumer: rows of the kept tokens -------------------------------
+
+
+def test_gather_rows_brute_force_and_invariants():
+    rng = np.random.default_rng(77)
+    ly, ntot, hk, d = 3, 40, 2, 8
+    cache = rng.integers(0, 1 << 16, size=(ly, ntot, hk, d), dtype=np.uint16)
+    kept = [0, 3, 4, 5, 17, 39]
+    out = oracle.gather_rows(cache, kept)
+    assert out.shape == (ly, len(kept), hk, d) and out.dtype == cache.dtype
+    # element by element with plain loops
+    for layer in range(ly):
+        for i, t in enumerate(kept):
+            for g in range(hk):
+                for x in range(d):
+                    assert out[layer, i, g, x] == cache[layer, t, g, x]
+    # the identity list returns the cache; a permutation and its inverse cancel
+    assert np.array_equal(oracle.gather_rows(cache, range(ntot)), cache)
+    perm = rng.permutation(ntot)
+    back = oracle.gather_rows(oracle.gather_rows(cache, perm), np.argsort(perm))
+    assert np.array_equal(back, cache)
+    # an empty list gives no rows
+    assert oracle.gather_rows(cache, []).shape == (ly, 0, hk, d)
