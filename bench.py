@@ -38,12 +38,10 @@ METRIC = "prompt tokens scored+selected/sec at N=32K; HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
 N_COPIES = 4
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes per launch of the logits kernel from one ncu capture
-# (profiles/logits_tc_draft2b.md), valid while the kernel source hash matches.
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "ab108530b11887b1a0723e662f82f69765fd40fe", "bytes_per_launch": 213695744}
+TRAFFIC = {"source_sha1": "2093f60dcee70b3a7bfedd3d0864ea5b3b82a7c8", "bytes_per_launch": 202496256}
 
 
 def parse():
@@ -376,6 +374,35 @@ def run_ours(args, rank, world, local):
                      "ms_per_step": p_ms / args.steps, "device_status_ok": p_ok}
     d2h = 2 * ntot * 4 + koff_host.numel() * 4 + 4
 
+    # sparse-prefill consumer, reported beside the headline: the kept
+    # tokens' ids and their K and V rows (two 201 MB draft-cache tensors)
+    # gathered on the device from the scoring call's kept list
+    kb = [x.view(torch.bfloat16).view(shape.n_layers, ntot, shape.n_kv_heads, shape.head_dim)
+          for x in ks]
+    ids = torch.arange(ntot, dtype=torch.int32, device=dev)
+    tok_out = torch.empty(ntot, dtype=torch.int32, device=dev)
+    rows_out = [torch.empty_like(kb[0]) for _ in range(2)]
+
+    def c_step(i):
+        sp.gather_tokens(ids, out.kept_idx, out.n_kept, out=tok_out, stream=stream)
+        for j in range(2):
+            sp.gather_rows(kb[(2 * i + j) % N_COPIES], out.kept_idx, out.n_kept, out=rows_out[j],
+                           stream=stream)
+
+    for i in range(args.warmup):
+        c_step(i)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(args.steps):
+        c_step(i)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    c_ms = c0.elapsed_time(c1) / args.steps
+    c_bytes = 2 * 2 * n_kept * shape.n_layers * shape.n_kv_heads * shape.head_dim * 2 + n_kept * 12
+    ref_rows = kb[0][:, out.kept_idx[:n_kept].long()]
+    c_ok = bool(torch.equal(rows_out[0][:, :n_kept], ref_rows))   # every copy holds the same keys
+
     # max over ranks of the timed region
     times = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -413,6 +440,10 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "pipelined": pipelined,
+        "consumer": {"what": "kept token ids + kept K and V rows (gather_tokens, 2x gather_rows)",
+                     "ms_per_step": c_ms, "bytes_per_step": c_bytes,
+                     "gbs": c_bytes / (c_ms / 1e3) / 1e9, "frac": c_bytes / (c_ms / 1e3) / 1e9 / peak,
+                     "kernels_per_step": 3, "rows_match_torch_index": c_ok},
         "kept_tokens": n_kept, "device_status": status,
     }
     if not args.no_cpu_baseline:

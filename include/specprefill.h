@@ -198,6 +198,37 @@ int sp_gather_kept(const sp_shape* shape, const sp_params* params, const int32_t
                    int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws,
                    size_t ws_bytes, sp_stream_t stream);
 
+/* Sparse-prefill consumer: the rows of the kept tokens of a token-major
+ * cache tensor ("SpecPrefill — Implementation Guide", §How It Works / Sparse
+ * Prefill: the target prefills only the kept tokens, each at its original
+ * position), so that keys or values built from the draft can be handed to
+ * the target compactly.
+ * - src (device, bf16 bits): [Ly][Ntot][Hk][d] with the k_stride_* strides
+ *   of `shape` (d contiguous); only Ly, Ntot, Hk, d and those strides of
+ *   `shape` are used.
+ * - kept_idx (device, int32): packed token indices, e.g. from
+ *   sp_specprefill_score; n_kept (device, one int32): how many of them to
+ *   gather. Both are read on the device, so no host synchronisation is
+ *   needed between the selection and this call.
+ * - dst (device, bf16 bits): [Ly][dst_rows][Hk][d], dense; row i of layer l
+ *   receives src[l][kept_idx[i]]. dst_rows must be at least Ntot (the
+ *   largest possible kept count); rows past n_kept are left untouched.
+ * - An index outside [0, Ntot) gives a zero row; n_kept is clamped to
+ *   [0, Ntot].
+ * Returns SP_ERR_INVALID_ARG for a bad shape, a null pointer, a pointer that
+ * is not 16-byte aligned or dst_rows < Ntot. */
+int sp_gather_rows(const sp_shape* shape, const int32_t* kept_idx, const int32_t* n_kept,
+                   const uint16_t* src, uint16_t* dst, int64_t dst_rows, sp_stream_t stream);
+
+/* Kept token ids for the target's batch (same section): out[i] =
+ * token_ids[kept_idx[i]] for i < *n_kept (n_kept read on the device and
+ * clamped to [0, n_tokens_total]); an index outside [0, n_tokens_total)
+ * gives -1. token_ids holds the packed prompts' ids, n_tokens_total of them;
+ * out must hold n_tokens_total entries. All pointers are device pointers.
+ * Returns SP_ERR_INVALID_ARG for a null pointer or a bad size. */
+int sp_gather_tokens(const int32_t* token_ids, int64_t n_tokens_total, const int32_t* kept_idx,
+                     const int32_t* n_kept, int32_t* out, sp_stream_t stream);
+
 /* The whole path in one call. imp, tok_score, chunk_score, chunk_off and
  * chunk_keep are optional outputs (nullable; kept in the workspace when
  * null); kept_idx, kept_pos, kept_off and n_kept are required. `prof` is

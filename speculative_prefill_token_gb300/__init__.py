@@ -31,6 +31,8 @@ __all__ = [
     "pool_chunk_noalloc",
     "select",
     "gather_kept",
+    "gather_rows",
+    "gather_tokens",
     "specprefill_score",
     "device_status",
     "STATUS",
@@ -132,6 +134,8 @@ def load(path: Optional[str] = None):
         "sp_gather_kept": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
         "sp_specprefill_score": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                  _P, ctypes.POINTER(_Profile)],
+        "sp_gather_rows": [sp, _P, _P, _P, _P, ctypes.c_int64, _P],
+        "sp_gather_tokens": [_P, ctypes.c_int64, _P, _P, _P, _P],
         "sp_get_device_status": [_P, _SZ, _P, i32, ctypes.POINTER(ctypes.c_int32)],
     }
     for name, args in sigs.items():
@@ -317,6 +321,46 @@ def gather_kept(chunk_keep, chunk_off, seq_off, n_tokens_total: int, params: Sel
                                 kept_pos.data_ptr(), kept_off.data_ptr(), n_kept.data_ptr(),
                                 *_ws_args(ws), _stream(stream)), "sp_gather_kept")
     return kept_idx, kept_pos, kept_off, n_kept
+
+
+def gather_rows(cache, kept_idx, n_kept, out=None, stream=None):
+    """Rows of the kept tokens of a token-major bf16 cache tensor
+    ``[Ly][Ntot][Hk][d]`` (any strides, d contiguous), packed into ``out``
+    (dense ``[Ly][R][Hk][d]``, R >= Ntot, allocated with R = Ntot when
+    omitted): out[l, i] = cache[l, kept_idx[i]] for i < n_kept. Rows past
+    n_kept are left untouched."""
+    import torch
+    if cache.dtype != torch.bfloat16 or cache.dim() != 4 or cache.stride(-1) != 1:
+        raise ValueError("cache must be a bf16 [Ly][Ntot][Hk][d] tensor with d contiguous")
+    ly, ntot, hk, d = cache.shape
+    if out is None:
+        out = torch.empty(ly, ntot, hk, d, dtype=cache.dtype, device=cache.device)
+    if (out.dtype != cache.dtype or out.dim() != 4 or not out.is_contiguous()
+            or out.shape[0] != ly or out.shape[2:] != cache.shape[2:]):
+        raise ValueError("out must be a dense bf16 [Ly][R][Hk][d] tensor")
+    shape = _Shape(1, int(ly), int(hk), int(hk), int(d), 1, int(ntot), 0,
+                   cache.stride(0), cache.stride(1), cache.stride(2), d, d, d, d)
+    _check(lib().sp_gather_rows(ctypes.byref(shape), kept_idx.data_ptr(), n_kept.data_ptr(),
+                                cache.data_ptr(), out.data_ptr(), int(out.shape[1]),
+                                _stream(stream)), "sp_gather_rows")
+    return out
+
+
+def gather_tokens(token_ids, kept_idx, n_kept, out=None, stream=None):
+    """Kept token ids for the target's batch: out[i] = token_ids[kept_idx[i]]
+    for i < n_kept (int32, device)."""
+    import torch
+    n = token_ids.numel()
+    if token_ids.dtype != torch.int32 or not token_ids.is_contiguous():
+        raise ValueError("token_ids must be a contiguous int32 tensor")
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=token_ids.device)
+    if out.dtype != torch.int32 or out.numel() < n or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int32 tensor of at least len(token_ids)")
+    _check(lib().sp_gather_tokens(token_ids.data_ptr(), int(n), kept_idx.data_ptr(),
+                                  n_kept.data_ptr(), out.data_ptr(), _stream(stream)),
+           "sp_gather_tokens")
+    return out
 
 
 @dataclass

@@ -338,6 +338,34 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
                                          kept_off, n_kept, ws, st));
 }
 
+int sp_gather_rows(const sp_shape* shape, const int32_t* kept_idx, const int32_t* n_kept,
+                   const uint16_t* src, uint16_t* dst, int64_t dst_rows, sp_stream_t stream) {
+    if (!shape || !kept_idx || !n_kept || !src || !dst) return SP_ERR_INVALID_ARG;
+    const sp_shape* s = shape;
+    if (s->n_layers < 1 || s->n_kv_heads < 1 || s->head_dim < 8 || s->head_dim % 8 != 0 ||
+        s->n_tokens_total < 1 || s->n_tokens_total > (int64_t(1) << 30) ||
+        dst_rows < s->n_tokens_total)
+        return SP_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return SP_ERR_INVALID_ARG;
+    const int64_t st[3] = {s->k_stride_layer, s->k_stride_token, s->k_stride_head};
+    const int64_t ext[3] = {s->n_layers, s->n_tokens_total, s->n_kv_heads};
+    for (int i = 0; i < 3; ++i) {
+        if (ext[i] <= 1) continue;
+        if (st[i] < s->head_dim || st[i] % 8 != 0) return SP_ERR_INVALID_ARG;
+    }
+    return to_status(launch_gather_rows(s, kept_idx, n_kept, src, dst, dst_rows,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sp_gather_tokens(const int32_t* token_ids, int64_t n_tokens_total, const int32_t* kept_idx,
+                     const int32_t* n_kept, int32_t* out, sp_stream_t stream) {
+    if (!token_ids || !kept_idx || !n_kept || !out || n_tokens_total < 1 ||
+        n_tokens_total > (int64_t(1) << 30))
+        return SP_ERR_INVALID_ARG;
+    return to_status(launch_gather_tokens(token_ids, kept_idx, n_kept, out, n_tokens_total,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int sp_get_device_status(void* ws, size_t ws_bytes, sp_stream_t stream, int clear,
                          int32_t* status_host) {
     if (!ws || ws_bytes < sizeof(WsHeader) || !status_host) return SP_ERR_INVALID_ARG;
@@ -363,8 +391,8 @@ const char* sp_status_string(int status) {
 }
 
 const char* sp_build_info(void) {
-    return "specprefill sm_103a: tcgen05/TMA logits kernel, fp32 softmax partials, "
-           "bitonic per-prompt selection";
+    return "specprefill sm_103a: tcgen05/TMA logits kernel, 16-bit fixed-point logits scratch, "
+           "slice-parallel chunk ranking, kept-row gathers";
 }
 
 }  // extern "C"

@@ -120,6 +120,14 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
                         float* chunk_score, uint8_t* keep, int32_t* kept_idx, int32_t* kept_pos,
                         int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st);
 
+// Sparse-prefill consumer gathers (sp_rows.cu): kept rows of a token-major
+// bf16 cache tensor, and kept token ids.
+cudaError_t launch_gather_rows(const sp_shape* s, const int32_t* kept_idx, const int32_t* n_kept,
+                               const uint16_t* src, uint16_t* dst, int64_t dst_rows,
+                               cudaStream_t st);
+cudaError_t launch_gather_tokens(const int32_t* ids, const int32_t* kept_idx, const int32_t* n_kept,
+                                 int32_t* out, int64_t ntot, cudaStream_t st);
+
 // Launch with programmatic stream serialisation: the kernel may be
 // scheduled while its predecessor in the stream is still running and waits
 // for it in grid_dep_wait() (every kernel of this library does so before

@@ -130,3 +130,37 @@ def test_workspace_checks(lib):
     assert rc == 3
     rc = lib.sp_workspace_init(ctypes.addressof(buf) | 1, 512, None)
     assert rc == 3
+
+
+def test_gather_rows_and_tokens_validate_on_the_host(lib):
+    """Bad sizes, strides, alignment and null pointers are refused before any
+    launch; the pointers below are never dereferenced."""
+    a = ctypes.c_void_p(4096)
+    s = _shape(n_tokens_total=1024)
+    ok_rows = 1024
+
+    def rows(shape, src=a, dst=a, dst_rows=ok_rows, idx=a, nk=a):
+        return lib.sp_gather_rows(ctypes.byref(shape) if shape is not None else None, idx, nk,
+                                  src, dst, dst_rows, None)
+
+    assert rows(None) == 1
+    assert rows(s, idx=None) == 1
+    assert rows(s, nk=None) == 1
+    assert rows(s, src=None) == 1
+    assert rows(s, dst_rows=1023) == 1                      # fewer rows than tokens
+    assert rows(s, src=ctypes.c_void_p(4096 + 8)) == 1      # src not 16-byte aligned
+    assert rows(s, dst=ctypes.c_void_p(4096 + 2)) == 1
+    bad = _shape(n_tokens_total=1024, head_dim=60)           # d not a whole number of vectors
+    assert rows(bad) == 1
+    bad = _shape(n_tokens_total=1024)
+    bad.k_stride_token = 2 * 256 + 4                         # token stride not 16-byte multiple
+    assert rows(bad) == 1
+    bad = _shape(n_tokens_total=1024)
+    bad.k_stride_head = 128                                   # heads overlap
+    assert rows(bad) == 1
+    bad = _shape(n_tokens_total=0)
+    assert rows(bad, dst_rows=0) == 1
+    assert lib.sp_gather_tokens(None, 16, a, a, a, None) == 1
+    assert lib.sp_gather_tokens(a, 0, a, a, a, None) == 1
+    assert lib.sp_gather_tokens(a, 16, a, a, None, None) == 1
+    assert lib.sp_gather_tokens(a, (1 << 30) + 1, a, a, a, None) == 1
