@@ -9,6 +9,7 @@ invariants); no function here is left unpinned.
 
 from .specprefill_oracle import (  # noqa: F401
     attention_rows,
+    auto_window,
     avg_pool,
     chunk_means,
     chunk_offsets,
@@ -16,13 +17,23 @@ from .specprefill_oracle import (  # noqa: F401
     finish_selection,
     gather_rows,
     fixed_count,
+    importance,
+    listing_cap,
+    listing_eff_min,
+    listing_forced_tokens,
+    listing_keep_count,
+    merge_windows,
     min_max_normalize,
     rank_order,
     run,
     select_fixed,
+    score_from_importance,
     select_from_chunk_scores,
+    select_listing,
     select_mass,
+    select_prompt,
     step_importance,
     structural_boost,
     token_importance,
+    window_plan,
 )

@@ -36,6 +36,21 @@ plain numpy float64 (inputs are bf16 bit patterns decoded exactly):
    section: only the kept tokens are prefilled; listing of the sparse pass
    adds kept[i] with its position to the target batch)
 
+Reference-compatibility variants (the pages' own tool, for A/B comparison):
+14. listing selection rule: k = max(1, ceil(nc * p)) with the product in
+   float32, every chunk scoring at least the k-th score kept (ties can keep
+   more than k), tokens {0, 1, 2, 3, n-2, n-1} forced, a fill up to
+   eff_min = min(min_tok, max(4, n // 10)) tokens from the unselected chunks
+   in ascending order, everything kept when p >= 1 or n <= eff_min, and a
+   strided cap to max_keep tokens that keeps the last one  (guide v2 listing
+   `select_chunks` and the cap after it in `main`)
+15. sliding-window scoring: windows of `window` tokens every `stride`
+   tokens, each contributing its first `stride` scores (the last window all
+   of its own), averaged per token; the window size comes from the draft's
+   context size                                               (guide v3.1,
+   §Sliding Window Loop and §Bug Fixes in v3.1; guide v2 listing `main`,
+   window sizing)
+
 Readings where the pages are silent (each also listed in the design notes):
 softmax over the prompt keys only; kv head = h // G; the pool divides by the
 number of in-range tokens and never crosses a prompt boundary; normalisation
@@ -228,6 +243,143 @@ def finish_selection(sel: np.ndarray, n: int, chunk: int, force_bos: bool,
 
 
 # ---------------------------------------------------------------------------
+# 14. the listing's selection rule (reference-compatibility mode)
+
+
+def listing_keep_count(nc: int, keep_p: float) -> int:
+    """k = max(1, ceil(nc * p)) where nc * p is an int times a float32, so
+    the product is rounded to float32 before the ceiling (5 * 0.4f gives
+    2.0, not 2.0000000298)."""
+    prod = np.float32(nc) * np.float32(keep_p)
+    return max(1, int(math.ceil(float(prod))))
+
+
+def listing_eff_min(n: int, min_tok: int) -> int:
+    """Smallest kept-token count: min(min_tok, max(4, n // 10))."""
+    return min(int(min_tok), max(4, n // 10))
+
+
+def listing_forced_tokens(n: int) -> List[int]:
+    """Tokens 0-3 and, when the prompt has more than four, the last two."""
+    forced = [t for t in (0, 1, 2, 3) if t < n]
+    if n > 4:
+        forced += [n - 2, n - 1]
+    return sorted(set(forced))
+
+
+def listing_cap(kept: Sequence[int], max_keep: int) -> List[int]:
+    """Keep every step-th entry (step = len // max_keep) up to max_keep
+    entries, the last entry replaced by the list's last token; max_keep <= 0
+    disables the cap."""
+    kept = list(kept)
+    if max_keep <= 0 or len(kept) <= max_keep:
+        return kept
+    step = len(kept) // max_keep
+    capped = []
+    i = 0
+    while i < len(kept) and len(capped) < max_keep:
+        capped.append(kept[i])
+        i += step
+    capped[-1] = kept[-1]
+    return capped
+
+
+def select_listing(cs: np.ndarray, n: int, *, chunk: int, mode: str, keep_p: float,
+                   mass: float, min_tok: int, max_keep: int) -> Selection:
+    """Steps 9-12 under the listing's rule. Fixed mode keeps every chunk whose
+    score is at least the k-th largest; mass mode keeps the ranking prefix of
+    step 10. Then the forced tokens, the fill from unselected chunks (chunk
+    order, token order) up to eff_min, and the cap. chunk_keep has bit 0 for
+    the chunks the ranking (or the keep-everything case) selected."""
+    nc = cs.shape[0]
+    if n == 0:
+        return Selection(chunk_keep=np.zeros(0, dtype=np.uint8), kept_tokens=np.zeros(0, dtype=np.int64))
+    eff_min = listing_eff_min(n, min_tok)
+    if (mode == "fixed" and as_f32(keep_p) >= 1.0) or n <= eff_min:
+        sel = np.ones(nc, dtype=bool)
+    elif mode == "fixed":
+        kc = listing_keep_count(nc, keep_p)
+        ordered = sorted((float(v) for v in cs), reverse=True)
+        th = ordered[kc - 1] if kc <= nc else -math.inf
+        sel = np.array([float(v) >= th for v in cs], dtype=bool)
+    elif mode == "mass":
+        sel = select_mass(cs, mass)
+    else:
+        raise ValueError(mode)
+    kept = set()
+    for c in range(nc):
+        if sel[c]:
+            kept.update(range(c * chunk, min((c + 1) * chunk, n)))
+    kept.update(listing_forced_tokens(n))
+    if len(kept) < eff_min:
+        for c in range(nc):
+            if len(kept) >= eff_min:
+                break
+            if sel[c]:
+                continue
+            for t in range(c * chunk, min((c + 1) * chunk, n)):
+                if len(kept) >= eff_min:
+                    break
+                kept.add(t)
+    toks = listing_cap(sorted(kept), max_keep)
+    return Selection(chunk_keep=sel.astype(np.uint8), kept_tokens=np.array(toks, dtype=np.int64))
+
+
+# ---------------------------------------------------------------------------
+# 15. sliding-window scoring (reference-compatibility mode)
+
+
+def auto_window(spec_ctx: int, window: int = 0):
+    """(window, stride) for a draft context of spec_ctx tokens: a requested
+    window <= 0 becomes min(spec_ctx - 512, 500 MiB / (spec_ctx * 32)); the
+    result is clamped to [512, spec_ctx - 128] (upper bound last) and the
+    stride is half of it."""
+    max_safe = (500 * 1024 * 1024) // (spec_ctx * 32)
+    if window <= 0:
+        window = min(spec_ctx - 512, max_safe)
+    window = max(window, 512)
+    window = min(window, spec_ctx - 128)
+    return window, window // 2
+
+
+def window_plan(n: int, window: int, stride: int):
+    """Windows of the fixed loop: (start, end, kept) per window, where the
+    window scores tokens [start, end) and contributes its first `kept`
+    scores; the loop stops after the first window that reaches the end of
+    the prompt or whose next start would."""
+    if stride < 1 or window < stride:
+        raise ValueError("need 1 <= stride <= window")
+    plan = []
+    pos = 0
+    while pos < n:
+        end = min(pos + window, n)
+        last = end >= n or pos + stride >= n
+        plan.append((pos, end, (end - pos) if last else stride))
+        if last:
+            break
+        pos += stride
+    return plan
+
+
+def merge_windows(window_imps: Sequence[np.ndarray], n: int, window: int, stride: int) -> np.ndarray:
+    """Per-token average of the window contributions; a token no window
+    scored gets 1.0."""
+    plan = window_plan(n, window, stride)
+    if len(window_imps) != len(plan):
+        raise ValueError("one importance vector per window")
+    acc = np.zeros(n, dtype=np.float64)
+    cnt = np.zeros(n, dtype=np.int64)
+    for (start, end, kept), imp in zip(plan, window_imps):
+        imp = np.asarray(imp, dtype=np.float64)
+        if imp.shape[0] != end - start:
+            raise ValueError("window importance has the wrong length")
+        for i in range(kept):
+            acc[start + i] += imp[i]
+            cnt[start + i] += 1
+    return np.where(cnt > 0, acc / np.maximum(cnt, 1), 1.0)
+
+
+# ---------------------------------------------------------------------------
 # whole path
 
 
@@ -242,8 +394,14 @@ def score_prompt(imp: np.ndarray, *, pool_w: int, chunk: int, normalize: bool,
 
 
 def select_prompt(cs: np.ndarray, n: int, *, chunk: int, mode: str, keep_p: float,
-                  mass: float, force_bos: bool, force_last_chunk: bool) -> Selection:
-    """Steps 9-12 for one prompt."""
+                  mass: float, force_bos: bool, force_last_chunk: bool, rule: str = "exact",
+                  min_tok: int = 128, max_keep: int = 0) -> Selection:
+    """Steps 9-12 for one prompt (rule "listing": step 14 instead)."""
+    if rule == "listing":
+        return select_listing(cs, n, chunk=chunk, mode=mode, keep_p=keep_p, mass=mass,
+                              min_tok=min_tok, max_keep=max_keep)
+    if rule != "exact":
+        raise ValueError(rule)
     if cs.shape[0] == 0:
         sel = np.zeros(0, dtype=bool)
     elif mode == "fixed":
@@ -264,7 +422,8 @@ def chunk_offsets(seq_off: np.ndarray, chunk: int) -> np.ndarray:
 
 def select_from_chunk_scores(chunk_score: np.ndarray, seq_off: np.ndarray, *, chunk: int,
                              mode: str, keep_p: float, mass: float, force_bos: bool,
-                             force_last_chunk: bool, **_unused) -> Dict[str, np.ndarray]:
+                             force_last_chunk: bool, rule: str = "exact", min_tok: int = 128,
+                             max_keep: int = 0, **_unused) -> Dict[str, np.ndarray]:
     """Steps 9-12 over a packed batch of given chunk scores."""
     seq_off = np.asarray(seq_off, dtype=np.int64)
     coff = chunk_offsets(seq_off, chunk)
@@ -273,7 +432,8 @@ def select_from_chunk_scores(chunk_score: np.ndarray, seq_off: np.ndarray, *, ch
         n = int(seq_off[b + 1] - seq_off[b])
         cs = np.asarray(chunk_score[coff[b]:coff[b + 1]], dtype=np.float64)
         s = select_prompt(cs, n, chunk=chunk, mode=mode, keep_p=keep_p, mass=mass,
-                          force_bos=force_bos, force_last_chunk=force_last_chunk)
+                          force_bos=force_bos, force_last_chunk=force_last_chunk, rule=rule,
+                          min_tok=min_tok, max_keep=max_keep)
         keep.append(s.chunk_keep)
         idx.append(s.kept_tokens + seq_off[b])
         pos.append(s.kept_tokens)
@@ -287,51 +447,78 @@ def select_from_chunk_scores(chunk_score: np.ndarray, seq_off: np.ndarray, *, ch
     }
 
 
-def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
-        pool_w: int = 13, chunk: int = 32, mode: str = "fixed", keep_p: float = 0.30,
-        mass: float = 0.85, normalize: bool = True, boost_first_mult: float = 1.5,
-        boost_first_n: int = 64, boost_last_mult: float = 1.3, boost_last_n: int = 128,
-        force_bos: bool = True, force_last_chunk: bool = True,
-        scale: Optional[float] = None, keep_step_max: bool = False) -> Dict[str, np.ndarray]:
-    """The whole path over a packed batch.
-
-    q_bits: [B, Ly, L, Hq, d] bf16 bits; k_bits: [Ly, Ntot, Hk, d] bf16 bits;
-    seq_off: [B+1] prompt offsets into the token axis of k.
-    Returns float64 imp / tok_score / final_score (per token), chunk_score and
-    chunk_keep (per chunk), and the kept lists (packed index, position,
-    per-prompt offsets).
-    """
+def score_from_importance(imp: np.ndarray, seq_off: Sequence[int], *, pool_w: int = 13,
+                          chunk: int = 32, mode: str = "fixed", keep_p: float = 0.30,
+                          mass: float = 0.85, normalize: bool = True,
+                          boost_first_mult: float = 1.5, boost_first_n: int = 64,
+                          boost_last_mult: float = 1.3, boost_last_n: int = 128,
+                          force_bos: bool = True, force_last_chunk: bool = True,
+                          rule: str = "exact", min_tok: int = 128,
+                          max_keep: int = 0) -> Dict[str, np.ndarray]:
+    """Steps 5-12 over a packed batch of per-token importance vectors."""
     seq_off = np.asarray(seq_off, dtype=np.int64)
-    n_kv_heads = k_bits.shape[2]
-    imps, toks, finals, chunks, steps = [], [], [], [], []
+    imp = np.asarray(imp, dtype=np.float64)
+    toks, finals, chunks = [], [], []
     for b in range(len(seq_off) - 1):
-        start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
-        if n == 0:
-            for lst in (imps, toks, finals, chunks):
+        start, end = int(seq_off[b]), int(seq_off[b + 1])
+        if end == start:
+            for lst in (toks, finals, chunks):
                 lst.append(np.zeros(0))
-            if keep_step_max:
-                steps.append(np.zeros((q_bits.shape[2], 0)))
             continue
-        a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale)
-        imp = token_importance(a)
-        sc = score_prompt(imp, pool_w=pool_w, chunk=chunk, normalize=normalize,
+        sc = score_prompt(imp[start:end], pool_w=pool_w, chunk=chunk, normalize=normalize,
                           boost_first_mult=boost_first_mult, boost_first_n=boost_first_n,
                           boost_last_mult=boost_last_mult, boost_last_n=boost_last_n)
-        imps.append(imp)
         toks.append(sc["tok_score"])
         finals.append(sc["final_score"])
         chunks.append(sc["chunk_score"])
-        if keep_step_max:
-            steps.append(a)
     out = {
-        "imp": np.concatenate(imps),
+        "imp": imp,
         "tok_score": np.concatenate(toks),
         "final_score": np.concatenate(finals),
         "chunk_score": np.concatenate(chunks),
     }
     out.update(select_from_chunk_scores(out["chunk_score"], seq_off, chunk=chunk, mode=mode,
                                         keep_p=keep_p, mass=mass, force_bos=force_bos,
-                                        force_last_chunk=force_last_chunk))
+                                        force_last_chunk=force_last_chunk, rule=rule,
+                                        min_tok=min_tok, max_keep=max_keep))
+    return out
+
+
+def importance(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
+               scale: Optional[float] = None, keep_step_max: bool = False):
+    """Steps 1-4 over a packed batch: imp per token (and, on request, the
+    per-step maxima A[l, t] of each prompt)."""
+    seq_off = np.asarray(seq_off, dtype=np.int64)
+    n_kv_heads = k_bits.shape[2]
+    imps, steps = [], []
+    for b in range(len(seq_off) - 1):
+        start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
+        if n == 0:
+            imps.append(np.zeros(0))
+            steps.append(np.zeros((q_bits.shape[2], 0)))
+            continue
+        a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale)
+        imps.append(token_importance(a))
+        steps.append(a)
+    imp = np.concatenate(imps)
+    return (imp, steps) if keep_step_max else imp
+
+
+def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
+        scale: Optional[float] = None, keep_step_max: bool = False, **kw) -> Dict[str, np.ndarray]:
+    """The whole path over a packed batch.
+
+    q_bits: [B, Ly, L, Hq, d] bf16 bits; k_bits: [Ly, Ntot, Hk, d] bf16 bits;
+    seq_off: [B+1] prompt offsets into the token axis of k; the selection
+    keywords are those of score_from_importance (defaults: W = 13, C = 32,
+    fixed p = 0.30, mass 0.85, normalise, boost 1.5 x 64 / 1.3 x 128, BOS and
+    final chunk forced, the exact rule).
+    Returns float64 imp / tok_score / final_score (per token), chunk_score and
+    chunk_keep (per chunk), and the kept lists (packed index, position,
+    per-prompt offsets).
+    """
+    imp, steps = importance(q_bits, k_bits, seq_off, scale=scale, keep_step_max=True)
+    out = score_from_importance(imp, seq_off, **kw)
     if keep_step_max:
         out["step_max"] = steps
     return out

@@ -93,6 +93,45 @@ def _normalize_no_shift(x):
     return x / (hi - lo)  # mistake: the minimum is not subtracted
 
 
+def _keep_count_float64(nc, keep_p):
+    return max(1, int(math.ceil(nc * so.as_f32(keep_p))))  # mistake: float64 product
+
+
+def _forced_without_tail(n):
+    return [t for t in (0, 1, 2, 3) if t < n]  # mistake: n-2 and n-1 dropped
+
+
+def _eff_min_wrong_divisor(n, min_tok):
+    return min(int(min_tok), max(4, n // 100))  # mistake: n / 100
+
+
+def _cap_without_last(kept, max_keep):
+    kept = list(kept)
+    if max_keep <= 0 or len(kept) <= max_keep:
+        return kept
+    step = len(kept) // max_keep
+    return kept[::step][:max_keep]  # mistake: the last token is not put back
+
+
+def _plan_without_break(n, window, stride):
+    plan, pos = [], 0
+    while pos < n:  # mistake: the loop runs on after the window that reaches the end
+        end = min(pos + window, n)
+        last = end >= n
+        plan.append((pos, end, (end - pos) if last else stride))
+        pos += stride
+    return plan
+
+
+def _auto_window_clamp_order(spec_ctx, window=0):
+    max_safe = (500 * 1024 * 1024) // (spec_ctx * 32)
+    if window <= 0:
+        window = min(spec_ctx - 512, max_safe)
+    window = min(window, spec_ctx - 128)
+    window = max(window, 512)  # mistake: the lower bound applied last
+    return window, window // 2
+
+
 def _run_pins(names):
     failures = 0
     for name in names:
@@ -125,6 +164,16 @@ MUTANTS = [
     ("chunk_means", _chunk_means_full_divisor, ["test_oracle_matches_bruteforce"]),
     ("min_max_normalize", _normalize_no_shift, ["test_normalize_closed_form",
                                                "test_oracle_matches_bruteforce"]),
+    ("listing_keep_count", _keep_count_float64, ["test_listing_keep_count_rounds_the_product_in_float32"]),
+    ("listing_forced_tokens", _forced_without_tail, ["test_listing_forced_tokens_and_eff_min",
+                                                     "test_listing_ties_keep_every_chunk_at_the_threshold"]),
+    ("listing_eff_min", _eff_min_wrong_divisor, ["test_listing_forced_tokens_and_eff_min",
+                                                 "test_listing_fill_up_to_eff_min"]),
+    ("listing_cap", _cap_without_last, ["test_listing_cap_hand_worked",
+                                        "test_listing_keep_all_cases_and_cap"]),
+    ("window_plan", _plan_without_break, ["test_window_plan_matches_the_guides_examples",
+                                          "test_window_plan_covers_every_token_once"]),
+    ("auto_window", _auto_window_clamp_order, ["test_auto_window_closed_forms"]),
 ]
 
 

@@ -308,3 +308,191 @@ def test_gather_rows_brute_force_and_invariants():
     assert np.array_equal(back, cache)
     # an empty list gives no rows
     assert oracle.gather_rows(cache, []).shape == (ly, 0, hk, d)
+
+
+# ---------------------------------------------------------------- listing rule
+
+
+def test_listing_keep_count_rounds_the_product_in_float32():
+    # 0.4f = 0.4000000059604645; 5 * 0.4f = 2.0000000298 in exact arithmetic,
+    # which rounds to 2.0 in float32: the listing keeps 2 chunks, the exact
+    # rule (float64 product of the float32 p) keeps 3
+    assert oracle.listing_keep_count(5, 0.4) == 2
+    assert oracle.fixed_count(5, 0.4) == 3
+    # 16 * 0.3f = 4.8000002 -> 5; 1024 * 0.15f = 153.6 -> 154; tiny p -> 1
+    assert oracle.listing_keep_count(16, 0.3) == 5
+    assert oracle.listing_keep_count(1024, 0.15) == 154
+    assert oracle.listing_keep_count(10, 0.01) == 1
+    assert oracle.listing_keep_count(7, 1.0) == 7
+
+
+def test_listing_forced_tokens_and_eff_min():
+    assert oracle.listing_forced_tokens(1) == [0]
+    assert oracle.listing_forced_tokens(4) == [0, 1, 2, 3]
+    assert oracle.listing_forced_tokens(5) == [0, 1, 2, 3, 4]
+    assert oracle.listing_forced_tokens(100) == [0, 1, 2, 3, 98, 99]
+    assert oracle.listing_eff_min(400, 128) == 40
+    assert oracle.listing_eff_min(30, 128) == 4
+    assert oracle.listing_eff_min(5000, 128) == 128
+    assert oracle.listing_eff_min(5000, 8) == 8
+
+
+def test_listing_cap_hand_worked():
+    ten = list(range(10))
+    assert oracle.listing_cap(ten, 4) == [0, 2, 4, 9]     # step 2, last replaced
+    assert oracle.listing_cap(ten, 3) == [0, 3, 9]        # step 3
+    assert oracle.listing_cap(ten, 1) == [9]              # step 10
+    assert oracle.listing_cap(ten, 10) == ten
+    assert oracle.listing_cap(ten, 0) == ten              # disabled
+    assert oracle.listing_cap([1, 5, 7, 8, 20, 21, 22], 2) == [1, 22]
+
+
+def _listing(cs, n, chunk, **kw):
+    base = dict(mode="fixed", keep_p=0.3, mass=0.85, min_tok=128, max_keep=0)
+    base.update(kw)
+    return oracle.select_listing(np.asarray(cs, dtype=np.float64), n, chunk=chunk, **base)
+
+
+def test_listing_ties_keep_every_chunk_at_the_threshold():
+    # k = ceil(10 * 0.2f) = 2; the 2nd largest score 0.9 is shared by three
+    # chunks, all kept; eff_min = 10 is met, no fill
+    cs = [0.1, 0.9, 0.3, 0.9, 0.2, 0.5, 0.9, 0.05, 0.4, 0.6]
+    s = _listing(cs, 100, 10, keep_p=0.2)
+    assert s.chunk_keep.tolist() == [0, 1, 0, 1, 0, 0, 1, 0, 0, 0]
+    want = [0, 1, 2, 3] + list(range(10, 20)) + list(range(30, 40)) + list(range(60, 70)) + [98, 99]
+    assert s.kept_tokens.tolist() == want
+    # the exact rule keeps k chunks, ties broken by index
+    ex = oracle.select_prompt(np.asarray(cs), 100, chunk=10, mode="fixed", keep_p=0.15, mass=0.85,
+                              force_bos=False, force_last_chunk=False)
+    assert ex.chunk_keep.tolist() == [0, 1, 0, 1, 0, 0, 0, 0, 0, 0]
+
+
+def test_listing_fill_up_to_eff_min():
+    # n = 400, C = 32: 13 chunks (the last of 16 tokens); eff_min = 40;
+    # k = ceil(13 * 0.05f) = 1 keeps chunk 5 (32 tokens) + 6 forced = 38;
+    # the fill adds tokens 4 and 5 of chunk 0, the first unselected chunk
+    cs = np.linspace(0.1, 0.2, 13)
+    cs[5] = 0.9
+    s = _listing(cs, 400, 32, keep_p=0.05)
+    assert s.chunk_keep.tolist() == [1 if c == 5 else 0 for c in range(13)]
+    assert s.kept_tokens.tolist() == [0, 1, 2, 3, 4, 5] + list(range(160, 192)) + [398, 399]
+    # a smaller min_tok (eff_min 8) needs no fill
+    s = _listing(cs, 400, 32, keep_p=0.05, min_tok=8)
+    assert s.kept_tokens.tolist() == [0, 1, 2, 3] + list(range(160, 192)) + [398, 399]
+    # n = 800: 25 chunks, k = ceil(25 * 0.01f) = 1 keeps chunk 1 (tokens
+    # 32-63) + 6 forced = 38; eff_min = 80 asks for 42 more: tokens 4-31 of
+    # chunk 0 (28), then the selected chunk 1 is skipped and tokens 64-77 of
+    # chunk 2 (14) complete it
+    cs2 = np.linspace(0.1, 0.2, 25)
+    cs2[1] = 0.95
+    s = _listing(cs2, 800, 32, keep_p=0.01, min_tok=80)
+    assert s.kept_tokens.tolist() == list(range(0, 78)) + [798, 799]
+
+
+def test_listing_keep_all_cases_and_cap():
+    cs = [0.3, 0.1, 0.2]
+    assert _listing(cs, 4, 2, keep_p=0.1).kept_tokens.tolist() == [0, 1, 2, 3]  # n <= eff_min
+    s = _listing(cs, 80, 32, keep_p=1.0)
+    assert s.kept_tokens.tolist() == list(range(80)) and s.chunk_keep.tolist() == [1, 1, 1]
+    s = _listing(cs, 80, 32, keep_p=1.0, max_keep=8)       # 80 // 8 = 10
+    assert s.kept_tokens.tolist() == [0, 10, 20, 30, 40, 50, 60, 79]
+
+
+def test_listing_mass_mode_adds_forced_tokens_and_fill():
+    # mass 0.5 of the total 1.0: chunk 2 (0.6) alone reaches it
+    cs = [0.1, 0.1, 0.6, 0.2]
+    s = _listing(cs, 100, 25, mode="mass", mass=0.5, min_tok=12)   # eff_min = 10
+    assert s.chunk_keep.tolist() == [0, 0, 1, 0]
+    assert s.kept_tokens.tolist() == [0, 1, 2, 3] + list(range(50, 75)) + [98, 99]
+
+
+def test_listing_invariants_on_random_prompts():
+    rng = np.random.default_rng(123)
+    for _ in range(200):
+        n = int(rng.integers(1, 700))
+        chunk = int(rng.choice([4, 16, 32]))
+        nc = -(-n // chunk)
+        cs = np.round(rng.random(nc), 1)           # coarse values: many ties
+        kw = dict(keep_p=float(rng.choice([0.05, 0.3, 0.7, 1.0])), min_tok=int(rng.integers(1, 200)),
+                  max_keep=int(rng.choice([0, 5, 50])), mode=str(rng.choice(["fixed", "mass"])))
+        s = _listing(cs, n, chunk, **kw)
+        kt = s.kept_tokens.tolist()
+        assert kt == sorted(set(kt)) and all(0 <= t < n for t in kt)
+        uncapped = _listing(cs, n, chunk, **dict(kw, max_keep=0)).kept_tokens.tolist()
+        assert set(oracle.listing_forced_tokens(n)) <= set(uncapped)
+        assert len(uncapped) >= min(n, oracle.listing_eff_min(n, kw["min_tok"]))
+        sel_tokens = {t for c in range(nc) if s.chunk_keep[c] for t in range(c * chunk, min(n, c * chunk + chunk))}
+        assert sel_tokens <= set(uncapped)
+        if kw["max_keep"] and len(uncapped) > kw["max_keep"]:
+            assert len(kt) == kw["max_keep"] and kt[-1] == uncapped[-1] and set(kt) <= set(uncapped)
+        else:
+            assert kt == uncapped
+        if kw["mode"] == "fixed" and kw["keep_p"] < 1.0 and n > oracle.listing_eff_min(n, kw["min_tok"]):
+            k = oracle.listing_keep_count(nc, kw["keep_p"])
+            # every selected chunk scores at least every unselected one, and at
+            # least k chunks are selected (exactly k when the k-th score is unique)
+            sel = s.chunk_keep.astype(bool)
+            assert sel.sum() >= min(k, nc)
+            if (~sel).any():
+                assert cs[sel].min() > cs[~sel].max()
+
+
+# ---------------------------------------------------------------- sliding windows
+
+
+def test_auto_window_closed_forms():
+    # 500 MiB / (8192 * 32) = 2000 tokens, stride 1000 (the guide's default)
+    assert oracle.auto_window(8192) == (2000, 1000)
+    # 500 MiB / (4096 * 32) = 4000 > 4096 - 512
+    assert oracle.auto_window(4096) == (3584, 1792)
+    assert oracle.auto_window(8192, 300) == (512, 256)      # raised to 512
+    assert oracle.auto_window(600) == (472, 236)            # lowered to spec_ctx - 128 last
+    assert oracle.auto_window(8192, 5000) == (5000, 2500)
+
+
+def test_window_plan_matches_the_guides_examples():
+    # 10,000 tokens, window 2000 / stride 1000: windows start every 1000
+    # tokens and each keeps its first 1000 scores; the window starting at
+    # 8000 already reaches the end and is the last (the fixed loop drops the
+    # redundant window at 9000)
+    plan = oracle.window_plan(10000, 2000, 1000)
+    assert [p[0] for p in plan] == list(range(0, 9000, 1000))
+    assert all(p == (s, s + 2000, 1000) for p, s in zip(plan[:-1], range(0, 8000, 1000)))
+    assert plan[-1] == (8000, 10000, 2000)
+    # a 4.5K prompt takes 4 windows instead of 5
+    plan = oracle.window_plan(4500, 2000, 1000)
+    assert len(plan) == 4 and plan[-1] == (3000, 4500, 1500)
+    assert oracle.window_plan(1500, 2000, 1000) == [(0, 1500, 1500)]
+    assert oracle.window_plan(0, 2000, 1000) == []
+
+
+def test_window_plan_covers_every_token_once():
+    rng = np.random.default_rng(9)
+    for _ in range(300):
+        window = int(rng.integers(2, 300))
+        stride = window // 2
+        n = int(rng.integers(1, 2000))
+        plan = oracle.window_plan(n, window, stride)
+        covered = np.zeros(n, dtype=np.int64)
+        for start, end, kept in plan:
+            assert 0 <= start < end <= n and end - start <= window and 1 <= kept <= end - start
+            covered[start:start + kept] += 1
+        assert (covered == 1).all()
+        # every window but the last is full length
+        assert all(end - start == window for start, end, _ in plan[:-1])
+
+
+def test_merge_windows_places_each_windows_scores():
+    n, window, stride = 4500, 2000, 1000
+    plan = oracle.window_plan(n, window, stride)
+    imps = [np.full(end - start, float(w + 1)) for w, (start, end, _) in enumerate(plan)]
+    merged = oracle.merge_windows(imps, n, window, stride)
+    want = np.concatenate([np.full(1000, 1.0), np.full(1000, 2.0), np.full(1000, 3.0),
+                           np.full(1500, 4.0)])
+    assert np.array_equal(merged, want)
+    # positions inside a window map to the window's own token offsets
+    imps = [np.arange(end - start, dtype=np.float64) + 10000 * w for w, (start, end, _) in enumerate(plan)]
+    merged = oracle.merge_windows(imps, n, window, stride)
+    for t in (0, 999, 1000, 2500, 2999, 3000, 4499):
+        w = min(t // stride, len(plan) - 1)
+        assert merged[t] == 10000 * w + (t - plan[w][0])
