@@ -68,6 +68,27 @@ typedef enum sp_status {
 
 enum { SP_MODE_FIXED = 0, SP_MODE_MASS = 1 };
 
+/* Selection rule.
+ * SP_RULE_EXACT: exactly k chunks in fixed mode (ties broken by ascending
+ *   chunk index), token 0 and the final chunk forced (force_bos,
+ *   force_last_chunk); the SpecPrefill scoring contract.
+ * SP_RULE_LISTING: the rule of the pages' own tool ("SpecPrefill —
+ *   Implementation Guide", v2 listing `select_chunks` and the cap in `main`):
+ *   k = max(1, ceil(nc * p)) with the product rounded to float32, every
+ *   chunk scoring at least the k-th largest score kept (ties can keep more
+ *   than k), tokens {0, 1, 2, 3, n-2, n-1} forced (the last two when
+ *   n > 4; force_bos and force_last_chunk are ignored), then a fill of the
+ *   smallest unselected tokens up to eff_min = min(min_tok, max(4, n / 10))
+ *   tokens, everything kept when p >= 1 (fixed mode) or n <= eff_min, and
+ *   finally, when max_keep > 0 and more than max_keep tokens are kept, every
+ *   step-th kept token (step = count / max_keep) up to max_keep of them with
+ *   the last one replaced by the prompt's last kept token. Mass mode keeps
+ *   its ranking prefix and then applies the forced tokens, the fill and the
+ *   cap. Only sp_specprefill_score and sp_select_from_importance take this
+ *   rule, and only with pool_w / 2 <= 64 and chunk dividing 128
+ *   (SP_ERR_UNSUPPORTED otherwise). */
+enum { SP_RULE_EXACT = 0, SP_RULE_LISTING = 1 };
+
 /* Shapes and strides. Strides are in elements; the head_dim axis is
  * contiguous (stride 1).
  * K: bf16 keys of layer l, global token t, KV head g at
@@ -106,6 +127,9 @@ typedef struct sp_params {
     int32_t force_last_chunk;  /* 1: every prompt's final chunk is kept */
     float scale;               /* logit scale; 0 selects 1/sqrt(head_dim) */
     int32_t spin_limit;        /* polls before a device wait gives up; <= 0 selects the default */
+    int32_t rule;              /* SP_RULE_EXACT (0) or SP_RULE_LISTING */
+    int32_t min_tok;           /* SP_RULE_LISTING: >= 0 (128), bound of eff_min */
+    int32_t max_keep;          /* SP_RULE_LISTING: >= 0 (2000 in the pages' tool); 0 = no cap */
 } sp_params;
 
 /* Optional profiling hook: when non-null, `logits_start`/`logits_stop` are
@@ -182,7 +206,9 @@ int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* params,
                           sp_stream_t stream);
 
 /* Chunk selection per prompt. chunk_keep (device, one byte per chunk):
- * bit 0 = chosen by the ranking, bit 1 = forced final chunk. */
+ * bit 0 = chosen by the ranking, bit 1 = forced final chunk.
+ * SP_RULE_LISTING is not a chunk-level rule: SP_ERR_UNSUPPORTED (likewise
+ * for sp_gather_kept). */
 int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
               const int32_t* chunk_off, const float* chunk_score, uint8_t* chunk_keep,
               void* ws, size_t ws_bytes, sp_stream_t stream);
@@ -228,6 +254,53 @@ int sp_gather_rows(const sp_shape* shape, const int32_t* kept_idx, const int32_t
  * Returns SP_ERR_INVALID_ARG for a null pointer or a bad size. */
 int sp_gather_tokens(const int32_t* token_ids, int64_t n_tokens_total, const int32_t* kept_idx,
                      const int32_t* n_kept, int32_t* out, sp_stream_t stream);
+
+/* Sliding-window scoring of the pages' tool ("SpecPrefill — Implementation
+ * Guide", v3.1 §Sliding Window Loop and §Bug Fixes in v3.1): a prompt longer
+ * than the draft's context is scored in windows of `window` tokens starting
+ * every `stride` tokens, each window on its own (its own keys and lookahead
+ * queries); window w contributes the scores of its first `stride` tokens,
+ * the last window (the first one that reaches the end of the prompt) all of
+ * its own, so every token is scored by exactly one window.
+ *
+ * sp_auto_window (host only): the guide's sizing for a draft context of
+ * spec_ctx tokens (v2 listing `main`): a requested window <= 0 becomes
+ * min(spec_ctx - 512, 500 MiB / (spec_ctx * 32)), the result is raised to
+ * at least 512 and then lowered to at most spec_ctx - 128, and the stride is
+ * half of it. SP_ERR_INVALID_ARG when spec_ctx < 130 (the window would be
+ * below 2) or an output pointer is null.
+ *
+ * sp_window_plan (host only): the windows of a prompt of n tokens, in scoring
+ * order: window w covers tokens [start[w], end[w]) and contributes its first
+ * kept[w] scores. Writes *n_windows; the arrays (host, `capacity` entries
+ * each, nullable when capacity is 0) receive min(capacity, *n_windows)
+ * windows. SP_ERR_INVALID_ARG unless 1 <= stride <= window and n >= 0.
+ *
+ * sp_merge_windows (device): out[t] for t < n (device, n floats) from the
+ * per-window importance vectors packed back to back in window order
+ * (imp_windows, device, sum of the window lengths: every window but the
+ * last has `window` tokens), i.e. out[t] = imp_windows[w * window + t -
+ * w * stride] with w = min(t / stride, last window). Feed the window batch
+ * to sp_attn_importance as a batch of prompts (one per window), merge, then
+ * select with sp_select_from_importance. */
+int sp_auto_window(int32_t spec_ctx, int32_t window_request, int32_t* window, int32_t* stride);
+int sp_window_plan(int64_t n, int32_t window, int32_t stride, int32_t* start, int32_t* end,
+                   int32_t* kept, int32_t capacity, int32_t* n_windows);
+int sp_merge_windows(int64_t n, int32_t window, int32_t stride, const float* imp_windows,
+                     float* out, sp_stream_t stream);
+
+/* Pooling, normalisation, boost, chunk scores, selection and the kept
+ * lists from a given per-token importance imp (device, Ntot floats): the
+ * part of sp_specprefill_score after the importance, for importance that
+ * comes from elsewhere (merged windows, another scorer). `shape` needs only
+ * n_seqs and n_tokens_total to be meaningful (the attention dimensions must
+ * still pass the checks; sp_workspace_size with the same shape gives the
+ * workspace). Outputs as for sp_specprefill_score. */
+int sp_select_from_importance(const sp_shape* shape, const sp_params* params,
+                              const int32_t* seq_off, const float* imp, float* tok_score,
+                              float* chunk_score, int32_t* chunk_off, uint8_t* chunk_keep,
+                              int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off,
+                              int32_t* n_kept, void* ws, size_t ws_bytes, sp_stream_t stream);
 
 /* The whole path in one call. imp, tok_score, chunk_score, chunk_off and
  * chunk_keep are optional outputs (nullable; kept in the workspace when

@@ -33,6 +33,10 @@ __all__ = [
     "gather_kept",
     "gather_rows",
     "gather_tokens",
+    "select_from_importance",
+    "auto_window",
+    "window_plan",
+    "merge_windows",
     "specprefill_score",
     "device_status",
     "STATUS",
@@ -44,6 +48,7 @@ LIB_PATH = os.path.join(_HERE, "libspecprefill.so")
 STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_ERR_WORKSPACE",
           4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_DEVICE"}
 MODES = {"fixed": 0, "mass": 1}
+RULES = {"exact": 0, "listing": 1}
 
 
 class SpecPrefillError(RuntimeError):
@@ -70,7 +75,8 @@ class _Params(ctypes.Structure):
                 ("boost_first_n", ctypes.c_int32), ("boost_last_mult", ctypes.c_float),
                 ("boost_last_n", ctypes.c_int32), ("force_bos", ctypes.c_int32),
                 ("force_last_chunk", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("spin_limit", ctypes.c_int32)]
+                ("spin_limit", ctypes.c_int32), ("rule", ctypes.c_int32),
+                ("min_tok", ctypes.c_int32), ("max_keep", ctypes.c_int32)]
 
 
 class _Profile(ctypes.Structure):
@@ -80,7 +86,10 @@ class _Profile(ctypes.Structure):
 @dataclass
 class SelectionParams:
     """Selection settings; defaults are the pages' (W=13, C=32, mass 0.85,
-    boost x1.5 first 64 / x1.3 last 128, BOS and final chunk kept)."""
+    boost x1.5 first 64 / x1.3 last 128, BOS and final chunk kept).
+    rule "listing" selects like the pages' own tool (ties at the threshold,
+    tokens {0,1,2,3,n-2,n-1}, fill to min(min_tok, max(4, n/10)), cap to
+    max_keep tokens when max_keep > 0)."""
     pool_w: int = 13
     chunk: int = 32
     mode: str = "mass"
@@ -95,13 +104,17 @@ class SelectionParams:
     force_last_chunk: bool = True
     scale: float = 0.0
     spin_limit: int = 0
+    rule: str = "exact"
+    min_tok: int = 128
+    max_keep: int = 0
 
     def _c(self) -> _Params:
         return _Params(int(self.pool_w), int(self.chunk), MODES[self.mode], float(self.keep_p),
                        float(self.mass), int(bool(self.normalize)), float(self.boost_first_mult),
                        int(self.boost_first_n), float(self.boost_last_mult), int(self.boost_last_n),
                        int(bool(self.force_bos)), int(bool(self.force_last_chunk)),
-                       float(self.scale), int(self.spin_limit))
+                       float(self.scale), int(self.spin_limit), RULES[self.rule],
+                       int(self.min_tok), int(self.max_keep))
 
 
 _lib = None
@@ -135,6 +148,10 @@ def load(path: Optional[str] = None):
         "sp_specprefill_score": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                  _P, ctypes.POINTER(_Profile)],
         "sp_gather_rows": [sp, _P, _P, _P, _P, ctypes.c_int64, _P],
+        "sp_select_from_importance": [sp, pp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+        "sp_auto_window": [i32, i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+        "sp_window_plan": [ctypes.c_int64, i32, i32, _P, _P, _P, i32, ctypes.POINTER(ctypes.c_int32)],
+        "sp_merge_windows": [ctypes.c_int64, i32, i32, _P, _P, _P],
         "sp_gather_tokens": [_P, ctypes.c_int64, _P, _P, _P, _P],
         "sp_get_device_status": [_P, _SZ, _P, i32, ctypes.POINTER(ctypes.c_int32)],
     }
@@ -416,6 +433,76 @@ def specprefill_score(q, k, seq_off, params: SelectionParams, out: Optional[Scor
         _ptr(out.chunk_off), _ptr(out.chunk_keep), out.kept_idx.data_ptr(),
         out.kept_pos.data_ptr(), out.kept_off.data_ptr(), out.n_kept.data_ptr(), *_ws_args(ws),
         _stream(stream), prof), "sp_specprefill_score")
+    return out
+
+
+def select_from_importance(imp, seq_off, params: SelectionParams, out: Optional[ScoreOutputs] = None,
+                           ws=None, stream=None) -> ScoreOutputs:
+    """Pooling, normalisation, boost, chunk scores, selection and kept lists
+    from a given per-token importance (float32, device). ``out.imp`` is the
+    given ``imp``."""
+    import torch
+    n_seqs = seq_off.numel() - 1
+    ntot = imp.numel()
+    shape = token_shape(n_seqs, ntot)
+    dev = imp.device
+    if out is None:
+        nch = max_chunks(shape, params)
+        out = ScoreOutputs(kept_idx=torch.empty(ntot, dtype=torch.int32, device=dev),
+                           kept_pos=torch.empty(ntot, dtype=torch.int32, device=dev),
+                           kept_off=torch.empty(n_seqs + 1, dtype=torch.int32, device=dev),
+                           n_kept=torch.empty(1, dtype=torch.int32, device=dev),
+                           tok_score=torch.empty(ntot, dtype=torch.float32, device=dev),
+                           chunk_score=torch.empty(nch, dtype=torch.float32, device=dev),
+                           chunk_off=torch.empty(n_seqs + 1, dtype=torch.int32, device=dev),
+                           chunk_keep=torch.empty(nch, dtype=torch.uint8, device=dev))
+    out.imp = imp
+    if ws is None:
+        ws = make_workspace(shape, params, dev)
+    _check(lib().sp_select_from_importance(
+        ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(), imp.data_ptr(),
+        _ptr(out.tok_score), _ptr(out.chunk_score), _ptr(out.chunk_off), _ptr(out.chunk_keep),
+        out.kept_idx.data_ptr(), out.kept_pos.data_ptr(), out.kept_off.data_ptr(),
+        out.n_kept.data_ptr(), *_ws_args(ws), _stream(stream)), "sp_select_from_importance")
+    return out
+
+
+def auto_window(spec_ctx: int, window: int = 0):
+    """(window, stride) of the sliding-window scoring for a draft context of
+    spec_ctx tokens (host computation)."""
+    w, st = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().sp_auto_window(int(spec_ctx), int(window), ctypes.byref(w), ctypes.byref(st)),
+           "sp_auto_window")
+    return int(w.value), int(st.value)
+
+
+def window_plan(n: int, window: int, stride: int):
+    """[(start, end, kept)] of the sliding-window scoring of an n-token prompt
+    (host computation)."""
+    cnt = ctypes.c_int32()
+    _check(lib().sp_window_plan(int(n), int(window), int(stride), None, None, None, 0,
+                                ctypes.byref(cnt)), "sp_window_plan")
+    m = int(cnt.value)
+    arr = [(ctypes.c_int32 * max(m, 1))() for _ in range(3)]
+    _check(lib().sp_window_plan(int(n), int(window), int(stride), *[ctypes.addressof(a) for a in arr],
+                                m, ctypes.byref(cnt)), "sp_window_plan")
+    return [(arr[0][i], arr[1][i], arr[2][i]) for i in range(m)]
+
+
+def merge_windows(imp_windows, n: int, window: int, stride: int, out=None, stream=None):
+    """Per-token importance of an n-token prompt from its windows' importance
+    vectors packed back to back (float32, device)."""
+    import torch
+    if imp_windows.dtype != torch.float32 or not imp_windows.is_contiguous():
+        raise ValueError("imp_windows must be a contiguous float32 tensor")
+    plan = window_plan(n, window, stride)
+    need = sum(e - s for s, e, _ in plan)
+    if imp_windows.numel() < need:
+        raise ValueError(f"imp_windows holds {imp_windows.numel()} scores, the windows need {need}")
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=imp_windows.device)
+    _check(lib().sp_merge_windows(int(n), int(window), int(stride), imp_windows.data_ptr(),
+                                  out.data_ptr(), _stream(stream)), "sp_merge_windows")
     return out
 
 

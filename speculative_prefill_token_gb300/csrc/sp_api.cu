@@ -61,6 +61,8 @@ int check_params(const sp_params* p) {
     if ((p->normalize != 0 && p->normalize != 1) || (p->force_bos != 0 && p->force_bos != 1) ||
         (p->force_last_chunk != 0 && p->force_last_chunk != 1))
         return SP_ERR_INVALID_ARG;
+    if ((p->rule != SP_RULE_EXACT && p->rule != SP_RULE_LISTING) || p->min_tok < 0 || p->max_keep < 0)
+        return SP_ERR_INVALID_ARG;
     return SP_OK;
 }
 
@@ -132,7 +134,10 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_pblk_base = take(B1 * 4);
     P.o_slice_base = take(B1 * 4);
     P.o_scount = take(static_cast<size_t>(P.slices_max) * 4);
-    P.o_segcnt = take(static_cast<size_t>(P.slabs_per_wave) * P.B * 4);
+    // per-segment record counters, then the listing rule's per-prompt
+    // kept counts: one range, zeroed by the prep kernel on every call
+    P.o_segcnt = take((static_cast<size_t>(P.slabs_per_wave) + 1) * P.B * 4);
+    P.o_lcount = P.o_segcnt + static_cast<size_t>(P.slabs_per_wave) * P.B * 4;
     P.o_logits = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * kTileTokens * P.Rs * 2);
     P.o_lmax = take(static_cast<size_t>(P.slabs_per_wave) * P.tiles_max * 4 * P.Rs * 4);
     P.o_part = take(static_cast<size_t>(P.rec_slots) * P.Rs * 8);
@@ -193,6 +198,34 @@ int attn_importance(const sp_shape* shape, const sp_params* params, const int32_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_prep(pl, seq_off, ws, nullptr, st) != cudaSuccess) return SP_ERR_CUDA;
     return importance_waves(pl, shape, seq_off, q, k, imp, ws, st, simt, nullptr);
+}
+
+// Steps after the importance: pool (+ normalise, boost, chunk sums), chunk
+// scores and selection, kept lists. The fused post path when the pool halo
+// and chunk size allow it (required by the listing rule), else the staged
+// kernels.
+int select_tail(const Plan& pl, const sp_params* params, const int32_t* seq_off, const float* imp,
+                float* tok_score, float* chunk_score, uint8_t* chunk_keep, int32_t* kept_idx,
+                int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st) {
+    float* tok_p = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
+    float* cs_p = chunk_score ? chunk_score : ws_ptr<float>(ws, pl.o_cscore);
+    uint8_t* keep_p = chunk_keep ? chunk_keep : ws_ptr<uint8_t>(ws, pl.o_ckeep);
+    const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
+    if (fused_post_ok(params)) {
+        if (launch_pool_sums(pl, params, seq_off, imp, tok_p, ws, st) != cudaSuccess)
+            return SP_ERR_CUDA;
+        return to_status(launch_post(pl, params, seq_off, cs_p, keep_p, kept_idx, kept_pos, kept_off,
+                                     n_kept, ws, st));
+    }
+    if (launch_pool(pl, params, seq_off, imp, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_select(pl, params, seq_off, coff, cs_p, keep_p, ws, false, nullptr, nullptr, st) !=
+        cudaSuccess)
+        return SP_ERR_CUDA;
+    if (launch_gather_scan(pl, params, seq_off, coff, keep_p, ws, kept_off, n_kept, st) != cudaSuccess)
+        return SP_ERR_CUDA;
+    return to_status(launch_gather_write(pl, params, seq_off, coff, keep_p, kept_idx, kept_pos,
+                                         kept_off, n_kept, ws, st));
 }
 
 }  // namespace
@@ -271,6 +304,7 @@ int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq
     int rc = make_plan(shape, params, &pl);
     if (rc != SP_OK) return rc;
     if (!seq_off || !chunk_off || !chunk_score || !chunk_keep) return SP_ERR_INVALID_ARG;
+    if (params->rule != SP_RULE_EXACT) return SP_ERR_UNSUPPORTED;
     if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_prep_check(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
@@ -287,6 +321,7 @@ int sp_gather_kept(const sp_shape* shape, const sp_params* params, const int32_t
     if (rc != SP_OK) return rc;
     if (!seq_off || !chunk_off || !chunk_keep || !kept_idx || !kept_pos || !kept_off || !n_kept)
         return SP_ERR_INVALID_ARG;
+    if (params->rule != SP_RULE_EXACT) return SP_ERR_UNSUPPORTED;
     if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
@@ -309,33 +344,74 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
     if (!seq_off || !q || !k || !kept_idx || !kept_pos || !kept_off || !n_kept || !aligned16(q) ||
         !aligned16(k))
         return SP_ERR_INVALID_ARG;
+    if (params->rule != SP_RULE_EXACT && !fused_post_ok(params)) return SP_ERR_UNSUPPORTED;
     if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* imp_p = imp ? imp : ws_ptr<float>(ws, pl.o_imp);
-    float* tok_p = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
-    float* cs_p = chunk_score ? chunk_score : ws_ptr<float>(ws, pl.o_cscore);
-    uint8_t* keep_p = chunk_keep ? chunk_keep : ws_ptr<uint8_t>(ws, pl.o_ckeep);
-    const int32_t* coff = ws_ptr<int32_t>(ws, pl.o_chunk_off);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
     if ((rc = importance_waves(pl, shape, seq_off, q, k, imp_p, ws, st, false, prof)) != SP_OK)
         return rc;
-    if (fused_post_ok(params)) {
-        if (launch_pool_sums(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess)
-            return SP_ERR_CUDA;
-        return to_status(launch_post(pl, params, seq_off, cs_p, keep_p, kept_idx, kept_pos, kept_off,
-                                     n_kept, ws, st));
-    } else {
-        if (launch_pool(pl, params, seq_off, imp_p, tok_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-        if (launch_chunk(pl, params, seq_off, tok_p, cs_p, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-        if (launch_select(pl, params, seq_off, coff, cs_p, keep_p, ws, false, nullptr, nullptr, st) !=
-            cudaSuccess)
-            return SP_ERR_CUDA;
-        if (launch_gather_scan(pl, params, seq_off, coff, keep_p, ws, kept_off, n_kept, st) !=
-            cudaSuccess)
-            return SP_ERR_CUDA;
+    return select_tail(pl, params, seq_off, imp_p, tok_score, chunk_score, chunk_keep, kept_idx,
+                       kept_pos, kept_off, n_kept, ws, st);
+}
+
+int sp_select_from_importance(const sp_shape* shape, const sp_params* params,
+                              const int32_t* seq_off, const float* imp, float* tok_score,
+                              float* chunk_score, int32_t* chunk_off, uint8_t* chunk_keep,
+                              int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off,
+                              int32_t* n_kept, void* ws, size_t ws_bytes, sp_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(shape, params, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !imp || !kept_idx || !kept_pos || !kept_off || !n_kept) return SP_ERR_INVALID_ARG;
+    if (params->rule != SP_RULE_EXACT && !fused_post_ok(params)) return SP_ERR_UNSUPPORTED;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    return select_tail(pl, params, seq_off, imp, tok_score, chunk_score, chunk_keep, kept_idx,
+                       kept_pos, kept_off, n_kept, ws, st);
+}
+
+int sp_auto_window(int32_t spec_ctx, int32_t window_request, int32_t* window, int32_t* stride) {
+    if (!window || !stride || spec_ctx < 130) return SP_ERR_INVALID_ARG;
+    const int64_t max_safe = (int64_t(500) * 1024 * 1024) / (static_cast<int64_t>(spec_ctx) * 32);
+    int64_t w = window_request;
+    if (w <= 0) w = std::min<int64_t>(spec_ctx - 512, max_safe);
+    w = std::max<int64_t>(w, 512);
+    w = std::min<int64_t>(w, spec_ctx - 128);
+    *window = static_cast<int32_t>(w);
+    *stride = static_cast<int32_t>(w / 2);
+    return SP_OK;
+}
+
+int sp_window_plan(int64_t n, int32_t window, int32_t stride, int32_t* start, int32_t* end,
+                   int32_t* kept, int32_t capacity, int32_t* n_windows) {
+    if (!n_windows || n < 0 || n > (int64_t(1) << 30) || stride < 1 || window < stride ||
+        capacity < 0 || (capacity > 0 && (!start || !end || !kept)))
+        return SP_ERR_INVALID_ARG;
+    int32_t w = 0;
+    for (int64_t pos = 0; pos < n; pos += stride) {
+        const int64_t e = std::min<int64_t>(pos + window, n);
+        const bool last = e >= n || pos + stride >= n;
+        if (w < capacity) {
+            start[w] = static_cast<int32_t>(pos);
+            end[w] = static_cast<int32_t>(e);
+            kept[w] = static_cast<int32_t>(last ? e - pos : stride);
+        }
+        ++w;
+        if (last) break;
     }
-    return to_status(launch_gather_write(pl, params, seq_off, coff, keep_p, kept_idx, kept_pos,
-                                         kept_off, n_kept, ws, st));
+    *n_windows = w;
+    return SP_OK;
+}
+
+int sp_merge_windows(int64_t n, int32_t window, int32_t stride, const float* imp_windows,
+                     float* out, sp_stream_t stream) {
+    if (!imp_windows || !out || n < 0 || n > (int64_t(1) << 30) || stride < 1 || window < stride)
+        return SP_ERR_INVALID_ARG;
+    if (n == 0) return SP_OK;
+    return to_status(launch_merge_windows(n, window, stride, imp_windows, out,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int sp_gather_rows(const sp_shape* shape, const int32_t* kept_idx, const int32_t* n_kept,

@@ -48,7 +48,7 @@ struct Plan {
     // workspace offsets (bytes)
     size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_lmax, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
-        o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_kept_off, o_nkept, total;
+        o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_lcount, o_kept_off, o_nkept, total;
 };
 
 int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
@@ -56,7 +56,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
 // ------------------------------------------------------------ launchers
 // Each returns cudaSuccess or the launch error.
 
-// Per-call offsets and checks; also zeroes the per-segment record counters.
+// Per-call offsets and checks; also zeroes the per-segment record counters
+// and the per-prompt kept counts of the listing rule (one range).
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
                         cudaStream_t st);
 
@@ -125,6 +126,8 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
 cudaError_t launch_gather_rows(const sp_shape* s, const int32_t* kept_idx, const int32_t* n_kept,
                                const uint16_t* src, uint16_t* dst, int64_t dst_rows,
                                cudaStream_t st);
+cudaError_t launch_merge_windows(int64_t n, int window, int stride, const float* imp_windows,
+                                 float* out, cudaStream_t st);
 cudaError_t launch_gather_tokens(const int32_t* ids, const int32_t* kept_idx, const int32_t* n_kept,
                                  int32_t* out, int64_t ntot, cudaStream_t st);
 

@@ -64,8 +64,9 @@ extern "C" int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* par
     int rc = make_plan(shape, params, &pl);
     if (rc != SP_OK) return rc;
     if (!seq_off || !imp || !tok_score || !chunk_score || !chunk_off) return SP_ERR_INVALID_ARG;
-    // scratch layout inside the fixed array: header, three offset tables,
-    // per-block (min, max) of the pooled scores
+    // scratch layout inside the fixed array: header, the four offset tables
+    // and the counters the prep kernel writes, per-block (min, max) of the
+    // pooled scores
     size_t off = sizeof(WsHeader);
     const size_t tables = (static_cast<size_t>(pl.B) + 1) * sizeof(int32_t);
     pl.o_tile_base = off;
@@ -74,6 +75,11 @@ extern "C" int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* par
     off = align256(off + tables);
     pl.o_pblk_base = off;
     off = align256(off + tables);
+    pl.o_slice_base = off;
+    off = align256(off + tables);
+    pl.o_segcnt = off;
+    pl.o_lcount = off + static_cast<size_t>(pl.slabs_per_wave) * pl.B * sizeof(int32_t);
+    off = align256(off + (static_cast<size_t>(pl.slabs_per_wave) + 1) * pl.B * sizeof(int32_t));
     pl.o_ppart = off;
     off = align256(off + static_cast<size_t>(pl.pblk_max) * 2 * sizeof(float));
     if (off > kStaticScratchBytes) return SP_ERR_UNSUPPORTED;  // batch too large for the fixed scratch

@@ -157,8 +157,10 @@ struct PostArgs {
     int32_t* kept_pos;
     int32_t* kept_off;
     int32_t* n_kept;
+    int32_t* lcount;            // listing rule: kept tokens per prompt before the fill
     WsHeader* hdr;
     int B, C, mode, normalize, force_bos, force_last;
+    int rule, min_tok, max_keep;
     float keep_p, mass;
 };
 
@@ -266,6 +268,7 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         }
     }
     const bool is_mass = a.mode == SP_MODE_MASS;
+    const bool listing = a.rule == SP_RULE_LISTING;
     if (is_mass) {
         for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
         if (lane == 0) sh.red_mx[warp] = smax;
@@ -291,9 +294,13 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
             sh.need = mass_threshold(tot, a.mass);
         }
     } else if (t == 0) {
-        sh.need = fixed_keep_count(nc, a.keep_p);
+        sh.need = listing ? listing_keep_count(nc, a.keep_p) : fixed_keep_count(nc, a.keep_p);
         sh.all = 0;
     }
+    // the listing keeps every token when p >= 1 (fixed mode) or the prompt
+    // is no longer than its smallest kept count
+    if (listing && t == 0 && ((!is_mass && a.keep_p >= 1.0f) || n <= listing_eff_min(n, a.min_tok)))
+        sh.all = 1;
     g.sync();
     const uint64_t need = sh.need;
     const bool all = sh.all != 0;
@@ -302,22 +309,26 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
     // warp w ranks chunks c_lo + w + kRankWarps * q of the slice: the count
     // (fixed) or fixed-point mass (mass mode) of the chunks ordered before
     // it. The order key (descending score, ascending index) is one 64-bit
-    // integer so that the comparison is branch-free.
+    // integer so that the comparison is branch-free. The listing rule's
+    // fixed mode counts only chunks with a strictly larger score (the index
+    // half of the key is masked off), so every chunk tied with the k-th
+    // score is kept.
+    const uint64_t kmask = (listing && !is_mass) ? 0xffffffff00000000ull : ~0ull;
     int64_t ci[kWarpChunks];
     uint64_t ki[kWarpChunks];
     uint64_t acc[kWarpChunks];
 #pragma unroll
     for (int q = 0; q < kWarpChunks; ++q) {
         ci[q] = c_lo + warp + kRankWarps * q;
-        ki[q] = ci[q] < c_hi ? (static_cast<uint64_t>(score_desc_key(cs_s[ci[q]])) << 32) |
-                                   static_cast<uint32_t>(ci[q])
+        ki[q] = ci[q] < c_hi ? ((static_cast<uint64_t>(score_desc_key(cs_s[ci[q]])) << 32) |
+                                static_cast<uint32_t>(ci[q])) & kmask
                              : 0u;
         acc[q] = 0;
     }
     if (!all) {
         for (int j = lane; j < static_cast<int>(nc); j += 32) {
             const float sj = cs_s[j];
-            const uint64_t kj = (static_cast<uint64_t>(score_desc_key(sj)) << 32) | static_cast<uint32_t>(j);
+            const uint64_t kj = ((static_cast<uint64_t>(score_desc_key(sj)) << 32) | static_cast<uint32_t>(j)) & kmask;
             const uint64_t wj = is_mass ? fixed_point(sj, S) : 1u;
 #pragma unroll
             for (int q = 0; q < kWarpChunks; ++q) acc[q] += kj < ki[q] ? wj : 0u;
@@ -334,10 +345,11 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
             if (c >= c_hi) continue;
             // fixed: fewer than k chunks before it; mass: mass before it below the threshold
             uint8_t f = (all || acc[q] < need) ? 1 : 0;
-            if (a.force_last && c == nc - 1) f |= 2;
+            if (!listing && a.force_last && c == nc - 1) f |= 2;
             a.keep[coff + c] = f;
-            my_cnt += static_cast<int32_t>(f ? chunk_tokens(n, a.C, c)
-                                             : ((c == 0 && a.force_bos && n > 0) ? 1 : 0));
+            int64_t extra = (c == 0 && a.force_bos && n > 0) ? 1 : 0;  // BOS of an unselected chunk 0
+            if (listing) extra = listing_forced_in(c * a.C, c * a.C + chunk_tokens(n, a.C, c), n);
+            my_cnt += static_cast<int32_t>(f ? chunk_tokens(n, a.C, c) : extra);
         }
         sh.warp_cnt[warp] = my_cnt;
     }
@@ -346,6 +358,7 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         int32_t tot = 0;
         for (int w = 0; w < kRankWarps; ++w) tot += sh.warp_cnt[w];
         a.scount[s] = tot;
+        if (listing) atomicAdd(a.lcount + b, tot);
     }
     g.sync();  // shared memory may be reused for the next slice
 }

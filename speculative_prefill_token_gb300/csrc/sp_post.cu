@@ -38,6 +38,7 @@
 #include "sp_device.cuh"
 #include "sp_internal.h"
 #include "sp_phases.cuh"
+#include "sp_select.cuh"
 
 namespace sp {
 namespace {
@@ -65,6 +66,121 @@ __global__ void __launch_bounds__(kRankThreads) gather_kernel(const PostArgs a) 
     gather_slice(a, s, S, threadIdx.x, GroupBar{1, kRankThreads}, sh);
 }
 
+// Listing rule: the final kept count of prompt b from its count before the
+// fill (the rank kernel's per-prompt sum): the fill up to eff_min, limited
+// to the tokens the prompt has, then the cap.
+__device__ __forceinline__ int64_t listing_final_count(const PostArgs& a, int b) {
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - a.seq_off[b];
+    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - a.chunk_off[b];
+    if (nc == 0 || nc > kMaxPromptChunks) return 0;  // nothing kept (the latter reported by the rank)
+    const int64_t k0 = __ldcg(a.lcount + b);
+    const int64_t fill = min64(max64(0, listing_eff_min(n, a.min_tok) - k0), n - k0);
+    const int64_t k = k0 + fill;
+    return (a.max_keep > 0 && k > a.max_keep) ? a.max_keep : k;
+}
+
+// Listing rule gather, one CTA per prompt plus one for the totals. The
+// prompt's kept list before the cap is: the tokens of its selected chunks
+// and its forced tokens ("kept0"), plus the first `fill` of the remaining
+// tokens ("spare") in token order. A kept0 token's position in that list is
+// the number of kept0 tokens before it plus min(fill, spare tokens before
+// it); a spare token is kept when fewer than `fill` spare tokens precede it.
+// With the cap (count k > max_keep = M, step = k / M), position p goes to
+// slot p / step when p % step == 0 and p / step < M - 1, and position k - 1
+// to slot M - 1; other positions are dropped. Each thread walks a
+// contiguous range of chunks after a block scan of the per-range counts.
+__global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const PostArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if (a.hdr->bad_input) return;
+    __shared__ int64_t red[kRankWarps];
+    __shared__ int64_t wk[kRankWarps], wu[kRankWarps];
+    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    // output offset: final counts of all earlier prompts
+    int64_t part = 0;
+    for (int bb = t; bb < b; bb += kRankThreads) part += listing_final_count(a, bb);
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red[warp] = part;
+    __syncthreads();
+    int64_t P = 0;
+    for (int w = 0; w < kRankWarps; ++w) P += red[w];
+    if (b == a.B) {
+        if (t == 0) {
+            a.kept_off[a.B] = static_cast<int32_t>(P);
+            *a.n_kept = static_cast<int32_t>(P);
+        }
+        return;
+    }
+    if (t == 0) a.kept_off[b] = static_cast<int32_t>(P);
+    const int64_t start = a.seq_off[b];
+    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
+    const int64_t coff = a.chunk_off[b];
+    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
+    if (nc == 0 || nc > kMaxPromptChunks) return;
+    const int64_t k0 = __ldcg(a.lcount + b);
+    const int64_t fill = min64(max64(0, listing_eff_min(n, a.min_tok) - k0), n - k0);
+    const int64_t k = k0 + fill;
+    const int64_t M = (a.max_keep > 0 && k > a.max_keep) ? a.max_keep : 0;
+    const int64_t step = M > 0 ? k / M : 1;
+    // this thread's chunks and their kept0 / spare token counts
+    const int64_t per = (nc + kRankThreads - 1) / kRankThreads;
+    const int64_t c0 = min64(nc, t * per), c1 = min64(nc, c0 + per);
+    int64_t nk = 0, nu = 0;
+    for (int64_t c = c0; c < c1; ++c) {
+        const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
+        if (__ldcg(a.keep + coff + c) & 1) {
+            nk += a1 - a0;
+        } else {
+            const int64_t f = listing_forced_in(a0, a1, n);
+            nk += f;
+            nu += a1 - a0 - f;
+        }
+    }
+    // block exclusive scans of both counts
+    int64_t ik = nk, iu = nu;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t vk = __shfl_up_sync(0xffffffffu, ik, o);
+        const int64_t vu = __shfl_up_sync(0xffffffffu, iu, o);
+        if (lane >= o) {
+            ik += vk;
+            iu += vu;
+        }
+    }
+    if (lane == 31) {
+        wk[warp] = ik;
+        wu[warp] = iu;
+    }
+    __syncthreads();
+    int64_t kb = ik - nk, ub = iu - nu;
+    for (int w = 0; w < warp; ++w) {
+        kb += wk[w];
+        ub += wu[w];
+    }
+    for (int64_t c = c0; c < c1; ++c) {
+        const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
+        const bool sel = (__ldcg(a.keep + coff + c) & 1) != 0;
+        for (int64_t tt = a0; tt < a1; ++tt) {
+            int64_t p = -1;
+            if (sel || listing_forced(tt, n)) {
+                p = kb + min64(fill, ub);
+                ++kb;
+            } else {
+                if (ub < fill) p = kb + ub;
+                ++ub;
+            }
+            if (p < 0) continue;
+            int64_t slot = p;
+            if (M > 0) {
+                if (p == k - 1) slot = M - 1;
+                else if (p % step == 0 && p / step < M - 1) slot = p / step;
+                else continue;
+            }
+            a.kept_idx[P + slot] = static_cast<int32_t>(start + tt);
+            a.kept_pos[P + slot] = static_cast<int32_t>(tt);
+        }
+    }
+}
+
 }  // namespace
 
 PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, float* chunk_score,
@@ -84,6 +200,7 @@ PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, f
     a.kept_pos = kept_pos;
     a.kept_off = kept_off;
     a.n_kept = n_kept;
+    a.lcount = ws_ptr<int32_t>(ws, pl.o_lcount);
     a.hdr = ws_ptr<WsHeader>(ws, 0);
     a.B = pl.B;
     a.C = pl.C;
@@ -93,6 +210,9 @@ PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, f
     a.force_last = p->force_last_chunk;
     a.keep_p = p->keep_p;
     a.mass = p->mass;
+    a.rule = p->rule;
+    a.min_tok = p->min_tok;
+    a.max_keep = p->max_keep;
     return a;
 }
 
@@ -110,6 +230,8 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
     }
     const cudaError_t e = launch_k(rank_kernel, static_cast<unsigned>(pl.slices_max), kRankThreads, smem, st, a);
     if (e != cudaSuccess) return e;
+    if (p->rule == SP_RULE_LISTING)
+        return launch_k(listing_gather_kernel, static_cast<unsigned>(pl.B + 1), kRankThreads, 0, st, a);
     return launch_k(gather_kernel, static_cast<unsigned>(pl.slices_max + 1), kRankThreads, 0, st, a);
 }
 

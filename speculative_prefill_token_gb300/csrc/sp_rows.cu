@@ -7,7 +7,10 @@
 //  - gather_rows: the kept tokens' rows of a token-major cache tensor
 //    (keys or values built from the draft), packed densely.
 //
-// Both are HBM-bound copies. gather_rows gives every (layer, kept row) to
+// The sliding-window scoring of the pages' tool merges per-window
+// importance the same way (merge_windows_kernel).
+//
+// All are HBM-bound copies. gather_rows gives every (layer, kept row) to
 // one warp, which issues all of its 16-byte streaming loads for up to 4
 // vectors per lane before the stores, so that one warp keeps a whole row
 // of a typical cache in flight; a grid of 8 CTAs per SM strides over the
@@ -90,6 +93,26 @@ __global__ void __launch_bounds__(kRowsThreads)
     }
 }
 
+// Sliding-window merge ("SpecPrefill — Implementation Guide", v3.1
+// §Sliding Window Loop): window w starts at w * stride; every window but the
+// last contributes its first `stride` scores and the last window (the first
+// whose end w * stride + window reaches n) all of its own, so token t takes
+// the score of window min(t / stride, last) at offset t - w * stride. The
+// windows' vectors are packed back to back and every window before the last
+// has `window` tokens.
+__global__ void __launch_bounds__(kRowsThreads)
+    merge_windows_kernel(const float* imp_windows, float* out, int64_t n, int64_t window,
+                         int64_t stride) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t last = n > window ? (n - window + stride - 1) / stride : 0;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kRowsThreads + threadIdx.x; t < n;
+         t += static_cast<int64_t>(gridDim.x) * kRowsThreads) {
+        const int64_t w = min(t / stride, last);
+        out[t] = imp_windows[w * window + (t - w * stride)];
+    }
+}
+
 int sm_count() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -117,6 +140,15 @@ cudaError_t launch_gather_rows(const sp_shape* s, const int32_t* kept_idx, const
     a.ks_head = s->k_stride_head;
     return launch_k(gather_rows_kernel, static_cast<unsigned>(kRowsCtasPerSm * sm_count()),
                     kRowsThreads, 0, st, a);
+}
+
+cudaError_t launch_merge_windows(int64_t n, int window, int stride, const float* imp_windows,
+                                 float* out, cudaStream_t st) {
+    int64_t blocks = (n + kRowsThreads - 1) / kRowsThreads;
+    const int64_t cap = static_cast<int64_t>(kRowsCtasPerSm) * sm_count();
+    if (blocks > cap) blocks = cap;
+    return launch_k(merge_windows_kernel, static_cast<unsigned>(blocks), kRowsThreads, 0, st,
+                    imp_windows, out, n, static_cast<int64_t>(window), static_cast<int64_t>(stride));
 }
 
 cudaError_t launch_gather_tokens(const int32_t* ids, const int32_t* kept_idx, const int32_t* n_kept,

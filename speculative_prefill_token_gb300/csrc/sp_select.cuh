@@ -54,6 +54,35 @@ __device__ __forceinline__ uint64_t fixed_keep_count(int64_t nc, float keep_p) {
     return static_cast<uint64_t>(k > nc ? nc : k);
 }
 
+// Listing rule ("SpecPrefill — Implementation Guide", v2 listing
+// `select_chunks`): k = max(1, ceil(nc * p)) where the product of the chunk
+// count and the float32 p is itself a float32 (5 * 0.4f is 2, not 3); at
+// most nc.
+__device__ __forceinline__ uint64_t listing_keep_count(int64_t nc, float keep_p) {
+    const float kk = ceilf(__fmul_rn(static_cast<float>(nc), keep_p));
+    const int64_t k = kk < 1.0f ? 1 : static_cast<int64_t>(kk);
+    return static_cast<uint64_t>(k > nc ? nc : k);
+}
+
+// Listing rule: the smallest kept-token count of an n-token prompt,
+// min(min_tok, max(4, n / 10)).
+__device__ __forceinline__ int64_t listing_eff_min(int64_t n, int min_tok) {
+    return min64(static_cast<int64_t>(min_tok), max64(4, n / 10));
+}
+
+// Listing rule: is token t of an n-token prompt one of the forced tokens
+// {0, 1, 2, 3} and, when n > 4, {n - 2, n - 1}?
+__device__ __forceinline__ bool listing_forced(int64_t t, int64_t n) {
+    return t < 4 || (n > 4 && t >= n - 2);
+}
+
+// Listing rule: forced tokens in [a0, a1) of an n-token prompt.
+__device__ __forceinline__ int64_t listing_forced_in(int64_t a0, int64_t a1, int64_t n) {
+    const int64_t head = max64(0, min64(a1, min64(4, n)) - a0);
+    const int64_t tail = n > 4 ? max64(0, min64(a1, n) - max64(a0, max64(4, n - 2))) : 0;
+    return head + tail;
+}
+
 // Mass mode: the power-of-two scale S of the fixed-point scores, from the
 // prompt's largest score, so that the sum of nc scores stays below 2^52.
 __device__ __forceinline__ int mass_scale(int64_t nc, float smax) {

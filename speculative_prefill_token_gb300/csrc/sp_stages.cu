@@ -531,7 +531,7 @@ cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), chunk_off_out,
         nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
-        static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B,
         ws_ptr<WsHeader>(ws, 0));
 }
 
@@ -542,7 +542,7 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), nullptr,
         chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
-        static_cast<int64_t>(pl.slabs_per_wave) * pl.B,
+        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B,
         ws_ptr<WsHeader>(ws, 0));
 }
 

@@ -100,7 +100,7 @@ def test_bad_shapes_rejected(lib, kw, code):
 @pytest.mark.parametrize("kw", [
     dict(pool_w=12), dict(pool_w=0), dict(chunk=0), dict(mode="fixed", keep_p=0.0),
     dict(mode="fixed", keep_p=1.5), dict(mode="mass", mass=0.0), dict(boost_first_mult=0.0),
-    dict(boost_last_n=-1), dict(scale=-1.0),
+    dict(boost_last_n=-1), dict(scale=-1.0), dict(min_tok=-1), dict(max_keep=-1),
 ])
 def test_bad_params_rejected(lib, kw):
     rc, _ = _ws(_shape(), sp.SelectionParams(**kw))
@@ -164,3 +164,57 @@ def test_gather_rows_and_tokens_validate_on_the_host(lib):
     assert lib.sp_gather_tokens(a, 0, a, a, a, None) == 1
     assert lib.sp_gather_tokens(a, 16, a, a, None, None) == 1
     assert lib.sp_gather_tokens(a, (1 << 30) + 1, a, a, a, None) == 1
+
+
+def test_listing_rule_validation(lib):
+    s = _shape()
+    bad = sp.SelectionParams()._c()
+    bad.rule = 2
+    n = ctypes.c_size_t()
+    assert lib.sp_workspace_size(ctypes.byref(s), ctypes.byref(bad), ctypes.byref(n)) == 1
+    a = ctypes.c_void_p(4096)
+    listing = sp.SelectionParams(rule="listing", mode="fixed", keep_p=0.3)._c()
+    # chunk-level stage entry points do not take the token-level listing rule
+    assert lib.sp_select(ctypes.byref(s), ctypes.byref(listing), a, a, a, a, a, 1 << 30, None) == 2
+    assert lib.sp_gather_kept(ctypes.byref(s), ctypes.byref(listing), a, a, a, a, a, a, a, a,
+                              1 << 30, None) == 2
+    # the listing rule runs on the fused post path only (chunk dividing 128)
+    odd = sp.SelectionParams(rule="listing", chunk=48)._c()
+    assert lib.sp_specprefill_score(ctypes.byref(s), ctypes.byref(odd), a, a, a, None, None, None,
+                                    None, None, a, a, a, a, a, 1 << 30, None, None) == 2
+    assert lib.sp_select_from_importance(ctypes.byref(s), ctypes.byref(odd), a, a, None, None, None,
+                                         None, a, a, a, a, a, 1 << 30, None) == 2
+    # same kernel count as the exact rule (its own gather kernel)
+    assert sp.kernels_per_call(s, sp.SelectionParams(rule="listing", mode="fixed")) == 6
+
+
+def test_auto_window_matches_the_oracle(lib):
+    import oracle
+    for spec_ctx in (130, 200, 600, 640, 1024, 2048, 4096, 8192, 16384, 32768, 131072):
+        for req in (0, -5, 100, 512, 1000, 3000, 100000):
+            assert sp.auto_window(spec_ctx, req) == oracle.auto_window(spec_ctx, req), (spec_ctx, req)
+    w = ctypes.c_int32()
+    assert lib.sp_auto_window(129, 0, ctypes.byref(w), ctypes.byref(w)) == 1
+    assert lib.sp_auto_window(8192, 0, None, ctypes.byref(w)) == 1
+
+
+def test_window_plan_matches_the_oracle(lib):
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(4)
+    cases = [(10000, 2000, 1000), (4500, 2000, 1000), (1500, 2000, 1000), (0, 2000, 1000),
+             (2000, 2000, 1000), (2001, 2000, 1000), (7, 3, 1)]
+    cases += [(int(rng.integers(0, 5000)), int(w), int(w) // 2) for w in rng.integers(2, 900, 40)]
+    for n, window, stride in cases:
+        assert sp.window_plan(n, window, stride) == oracle.window_plan(n, window, stride), (n, window)
+    # a short buffer receives the first windows, the count is the full one
+    cnt = ctypes.c_int32()
+    arr = [(ctypes.c_int32 * 2)() for _ in range(3)]
+    assert lib.sp_window_plan(10000, 2000, 1000, *[ctypes.addressof(x) for x in arr], 2,
+                              ctypes.byref(cnt)) == 0
+    assert cnt.value == 9 and list(arr[0]) == [0, 1000] and list(arr[2]) == [1000, 1000]
+    for bad in ((100, 10, 0), (100, 10, 11), (-1, 10, 5)):
+        assert lib.sp_window_plan(*bad, None, None, None, 0, ctypes.byref(cnt)) == 1
+    assert lib.sp_window_plan(100, 10, 5, None, None, None, 4, ctypes.byref(cnt)) == 1
+    assert lib.sp_merge_windows(100, 10, 0, ctypes.c_void_p(4096), ctypes.c_void_p(4096), None) == 1
+    assert lib.sp_merge_windows(100, 10, 5, None, ctypes.c_void_p(4096), None) == 1
