@@ -15,7 +15,10 @@ ranks scored divided by the slowest rank's time.
 
 `value` is the single-stream rate (one call after another on one stream).
 `pipelined` reports, beside it, the rate with --pipeline-streams calls in
-flight on as many streams, each with its own workspace and outputs.
+flight on as many streams, each with its own workspace and outputs;
+`listing_rule` the rate of the same calls under the pages' own selection
+rule (reference-compatibility mode); `consumer` the bandwidth of the
+sparse-prefill gathers (kept token ids, kept K and V rows).
 """
 
 import argparse
@@ -374,6 +377,29 @@ def run_ours(args, rank, world, local):
                      "ms_per_step": p_ms / args.steps, "device_status_ok": p_ok}
     d2h = 2 * ntot * 4 + koff_host.numel() * 4 + 4
 
+    # reference-compatibility rule (the pages' own selection: threshold
+    # ties, six forced tokens, eff_min fill, 2000-token cap), reported beside
+    # the headline: the same calls with the listing rule
+    l_params = sp.SelectionParams(**dict(w.selection_kwargs(), rule="listing", min_tok=128,
+                                         max_keep=2000))
+    l_ws = sp.make_workspace(shape, l_params, dev)
+    l_out = sp.alloc_outputs(qs[0], ks[0], l_params, intermediates=False)
+    for i in range(args.warmup):
+        sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, l_params, out=l_out, ws=l_ws,
+                             stream=stream)
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for i in range(args.steps):
+        sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, l_params, out=l_out, ws=l_ws,
+                             stream=stream)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    l_ms = l0.elapsed_time(l1) / args.steps
+    listing = {"what": "listing rule, min_tok 128, max_keep 2000", "ms_per_step": l_ms,
+               "value": world * ntot / (l_ms / 1e3), "unit": UNIT,
+               "kept_tokens": int(l_out.n_kept.item()), "device_status": sp.device_status(l_ws)}
+
     # sparse-prefill consumer, reported beside the headline: the kept
     # tokens' ids and their K and V rows (two 201 MB draft-cache tensors)
     # gathered on the device from the scoring call's kept list
@@ -440,6 +466,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "pipelined": pipelined,
+        "listing_rule": listing,
         "consumer": {"what": "kept token ids + kept K and V rows (gather_tokens, 2x gather_rows)",
                      "ms_per_step": c_ms, "bytes_per_step": c_bytes,
                      "gbs": c_bytes / (c_ms / 1e3) / 1e9, "frac": c_bytes / (c_ms / 1e3) / 1e9 / peak,

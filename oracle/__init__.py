@@ -24,6 +24,7 @@ from .specprefill_oracle import (  # noqa: F401
     listing_keep_count,
     merge_windows,
     min_max_normalize,
+    pool_rows,
     rank_order,
     run,
     select_fixed,

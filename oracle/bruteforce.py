@@ -11,7 +11,9 @@ Definitions followed (same pages as the oracle):
 * importance = mean over lookahead steps of (max over layers and heads of
   the softmax row), "SpecPrefill — Implementation Guide" §How It Works /
   Token Importance;
-* W-wide centred average pool, PR "Speculative prefill" §Approach item 3;
+* W-wide centred average pool, PR "Speculative prefill" §Approach item 3,
+  either on the per-token importance or (pool_at = "head") on every softmax
+  row before the max over heads and layers;
 * min-max normalisation, guide v3.1 §v3.1 Optimizations item 5;
 * structural boost, guide v3 §v3 Improvements item 2;
 * chunk mean and ranking, guide §Chunk Selection; cumulative mass, guide v3
@@ -33,7 +35,7 @@ def f32(x: float) -> float:
     return struct.unpack("<f", struct.pack("<f", float(x)))[0]
 
 
-def _prompt_importance(q, k, start: int, n: int, scale: float) -> List[float]:
+def _prompt_importance(q, k, start: int, n: int, scale: float, row_pool: int = 1) -> List[float]:
     n_layers, n_steps, n_q_heads, d = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
     n_kv_heads = len(k[0][0])
     group = n_q_heads // n_kv_heads
@@ -50,10 +52,12 @@ def _prompt_importance(q, k, start: int, n: int, scale: float) -> List[float]:
                 top = max(logits)
                 ex = [math.exp(x - top) for x in logits]
                 z = math.fsum(ex)
+                row = [ex[t] / z for t in range(n)]
+                if row_pool > 1:
+                    row = _pool(row, row_pool)
                 for t in range(n):
-                    p = ex[t] / z
-                    if p > best[s][t]:
-                        best[s][t] = p
+                    if row[t] > best[s][t]:
+                        best[s][t] = row[t]
     return [math.fsum(best[s][t] for s in range(n_steps)) / n_steps for t in range(n)]
 
 
@@ -100,7 +104,8 @@ def _select(cs: List[float], mode: str, keep_p: float, mass: float) -> List[int]
 def run_bruteforce(q, k, seq_off, *, pool_w=13, chunk=32, mode="fixed", keep_p=0.30,
                    mass=0.85, normalize=True, boost_first_mult=1.5, boost_first_n=64,
                    boost_last_mult=1.3, boost_last_n=128, force_bos=True,
-                   force_last_chunk=True, scale=None, select=True) -> Dict[str, list]:
+                   force_last_chunk=True, scale=None, select=True,
+                   pool_at="token") -> Dict[str, list]:
     """Same outputs as the oracle's ``run`` (lists instead of arrays).
 
     q: nested [B][Ly][L][Hq][d] bf16 bits; k: nested [Ly][Ntot][Hk][d] bf16 bits.
@@ -115,8 +120,8 @@ def run_bruteforce(q, k, seq_off, *, pool_w=13, chunk=32, mode="fixed", keep_p=0
            "chunk_keep": [], "kept_idx": [], "kept_pos": [], "kept_off": [0]}
     for b in range(len(seq_off) - 1):
         start, n = seq_off[b], seq_off[b + 1] - seq_off[b]
-        imp = _prompt_importance(q[b], k, start, n, scale)
-        x = _pool(imp, pool_w)
+        imp = _prompt_importance(q[b], k, start, n, scale, pool_w if pool_at == "head" else 1)
+        x = _pool(imp, pool_w if pool_at == "token" else 1)
         y = list(x)
         if normalize:
             lo, hi = min(y), max(y)

@@ -36,6 +36,12 @@ plain numpy float64 (inputs are bf16 bit patterns decoded exactly):
    section: only the kept tokens are prefilled; listing of the sparse pass
    adds kept[i] with its position to the target batch)
 
+Per-head pooling variant (the PR's other reading of where the smoothing
+sits, §Approach item 3: "smoothed ... max-reduced across heads/layers"):
+5'. with pool_at = "head", every softmax row p[layer, step, head, :] is
+   pooled (the same centred in-range mean, width W) before the max of
+   step 3; step 5 is then the identity.
+
 Reference-compatibility variants (the pages' own tool, for A/B comparison):
 14. listing selection rule: k = max(1, ceil(nc * p)) with the product in
    float32, every chunk scoring at least the k-th score kept (ties can keep
@@ -110,15 +116,37 @@ def attention_rows(q_bits: np.ndarray, k_bits: np.ndarray, start: int, n: int,
     return e / e.sum(axis=-1, keepdims=True)                                     # step 2
 
 
+def pool_rows(p: np.ndarray, width: int) -> np.ndarray:
+    """Centred in-range mean of odd ``width`` along the last axis of every
+    row (step 5'): the sum over the window offsets -W/2 .. W/2 of the row
+    shifted by that offset (positions outside [0, n) add nothing), divided
+    by the number of in-range positions."""
+    n = p.shape[-1]
+    half = width // 2
+    acc = np.zeros_like(p, dtype=np.float64)
+    cnt = np.zeros(n, dtype=np.float64)
+    for o in range(-half, half + 1):
+        lo, hi = max(0, -o), min(n, n - o)     # t with t + o in [0, n)
+        if lo >= hi:
+            continue
+        acc[..., lo:hi] += p[..., lo + o:hi + o]
+        cnt[lo:hi] += 1.0
+    return acc / cnt
+
+
 def step_importance(q_bits: np.ndarray, k_bits: np.ndarray, start: int, n: int,
-                    n_kv_heads: int, scale: Optional[float] = None) -> np.ndarray:
-    """A[l, t] = max over layers and query heads of p (step 3), shape [L, n]."""
+                    n_kv_heads: int, scale: Optional[float] = None,
+                    head_pool_w: int = 1) -> np.ndarray:
+    """A[l, t] = max over layers and query heads of p (step 3), shape [L, n];
+    with head_pool_w > 1 each row is pooled first (step 5')."""
     n_layers, n_steps, n_q_heads, _ = q_bits.shape
     group = n_q_heads // n_kv_heads
     a = np.full((n_steps, n), -np.inf)
     for layer in range(n_layers):
         for g in range(n_kv_heads):
             p = attention_rows(q_bits, k_bits, start, n, layer, g, group, scale)
+            if head_pool_w > 1:
+                p = pool_rows(p, head_pool_w)
             a = np.maximum(a, p.max(axis=1))
     return a
 
@@ -453,9 +481,14 @@ def score_from_importance(imp: np.ndarray, seq_off: Sequence[int], *, pool_w: in
                           boost_first_mult: float = 1.5, boost_first_n: int = 64,
                           boost_last_mult: float = 1.3, boost_last_n: int = 128,
                           force_bos: bool = True, force_last_chunk: bool = True,
-                          rule: str = "exact", min_tok: int = 128,
-                          max_keep: int = 0) -> Dict[str, np.ndarray]:
-    """Steps 5-12 over a packed batch of per-token importance vectors."""
+                          rule: str = "exact", min_tok: int = 128, max_keep: int = 0,
+                          pool_at: str = "token") -> Dict[str, np.ndarray]:
+    """Steps 5-12 over a packed batch of per-token importance vectors (with
+    pool_at = "head" the importance is already pooled: no step 5)."""
+    if pool_at not in ("token", "head"):
+        raise ValueError(pool_at)
+    if pool_at == "head":
+        pool_w = 1
     seq_off = np.asarray(seq_off, dtype=np.int64)
     imp = np.asarray(imp, dtype=np.float64)
     toks, finals, chunks = [], [], []
@@ -485,9 +518,14 @@ def score_from_importance(imp: np.ndarray, seq_off: Sequence[int], *, pool_w: in
 
 
 def importance(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
-               scale: Optional[float] = None, keep_step_max: bool = False):
+               scale: Optional[float] = None, keep_step_max: bool = False,
+               pool_at: str = "token", pool_w: int = 13):
     """Steps 1-4 over a packed batch: imp per token (and, on request, the
-    per-step maxima A[l, t] of each prompt)."""
+    per-step maxima A[l, t] of each prompt); pool_at = "head" pools every
+    softmax row with width pool_w before the max (step 5')."""
+    if pool_at not in ("token", "head"):
+        raise ValueError(pool_at)
+    head_pool_w = pool_w if pool_at == "head" else 1
     seq_off = np.asarray(seq_off, dtype=np.int64)
     n_kv_heads = k_bits.shape[2]
     imps, steps = [], []
@@ -497,7 +535,7 @@ def importance(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *
             imps.append(np.zeros(0))
             steps.append(np.zeros((q_bits.shape[2], 0)))
             continue
-        a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale)
+        a = step_importance(q_bits[b], k_bits, start, n, n_kv_heads, scale, head_pool_w)
         imps.append(token_importance(a))
         steps.append(a)
     imp = np.concatenate(imps)
@@ -517,7 +555,8 @@ def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
     chunk_keep (per chunk), and the kept lists (packed index, position,
     per-prompt offsets).
     """
-    imp, steps = importance(q_bits, k_bits, seq_off, scale=scale, keep_step_max=True)
+    imp, steps = importance(q_bits, k_bits, seq_off, scale=scale, keep_step_max=True,
+                            pool_at=kw.get("pool_at", "token"), pool_w=kw.get("pool_w", 13))
     out = score_from_importance(imp, seq_off, **kw)
     if keep_step_max:
         out["step_max"] = steps

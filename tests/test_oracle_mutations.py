@@ -132,12 +132,27 @@ def _auto_window_clamp_order(spec_ctx, window=0):
     return window, window // 2
 
 
+def _pool_rows_fixed_divisor(p, width):
+    half = width // 2
+    n = p.shape[-1]
+    padded = np.concatenate([np.zeros(p.shape[:-1] + (half,)), p, np.zeros(p.shape[:-1] + (half,))], axis=-1)
+    return sum(padded[..., o:o + n] for o in range(width)) / width  # mistake: zero padding counted
+
+
+_STEP_IMPORTANCE = so.step_importance  # the unmutated step, for the mutant that wraps it
+
+
+def _step_importance_pool_after_max(q_bits, k_bits, start, n, n_kv_heads, scale=None, head_pool_w=1):
+    a = _STEP_IMPORTANCE(q_bits, k_bits, start, n, n_kv_heads, scale, 1)
+    return so.pool_rows(a, head_pool_w) if head_pool_w > 1 else a  # mistake: pooled after the max
+
+
 def _run_pins(names):
     failures = 0
     for name in names:
         fn = getattr(pins, name)
         try:
-            if name == "test_oracle_matches_bruteforce":
+            if name in ("test_oracle_matches_bruteforce", "test_head_pooling_matches_bruteforce"):
                 for i in range(len(pins.TINY_CASES)):
                     fn(i)
             elif name == "test_selection_matches_subset_enumeration":
@@ -174,6 +189,9 @@ MUTANTS = [
     ("window_plan", _plan_without_break, ["test_window_plan_matches_the_guides_examples",
                                           "test_window_plan_covers_every_token_once"]),
     ("auto_window", _auto_window_clamp_order, ["test_auto_window_closed_forms"]),
+    ("pool_rows", _pool_rows_fixed_divisor, ["test_head_pooling_matches_bruteforce",
+                                             "test_pool_rows_against_convolution"]),
+    ("step_importance", _step_importance_pool_after_max, ["test_head_pooling_matches_bruteforce"]),
 ]
 
 

@@ -496,3 +496,66 @@ def test_merge_windows_places_each_windows_scores():
     for t in (0, 999, 1000, 2500, 2999, 3000, 4499):
         w = min(t // stride, len(plan) - 1)
         assert merged[t] == 10000 * w + (t - plan[w][0])
+
+
+# ---------------------------------------------------------------- per-head pooling
+
+
+@pytest.mark.parametrize("i", range(len(TINY_CASES)))
+def test_head_pooling_matches_bruteforce(i):
+    q, k, off, params = _case(i)
+    params = dict(params, pool_at="head")
+    got = oracle.run(q, k, off, **params)
+    want = bruteforce.run_bruteforce(q, k, off, **params)
+    for key in ("imp", "tok_score", "final_score", "chunk_score"):
+        np.testing.assert_allclose(got[key], want[key], rtol=1e-12, atol=1e-15, err_msg=key)
+    for key in ("chunk_keep", "kept_idx", "kept_pos", "kept_off"):
+        np.testing.assert_array_equal(np.asarray(got[key]), np.asarray(want[key]), err_msg=key)
+    # the pooled importance is the score: step 5 is the identity
+    np.testing.assert_array_equal(got["tok_score"], got["imp"])
+
+
+def test_pool_rows_against_convolution():
+    rng = np.random.default_rng(12)
+    p = rng.random((3, 2, 50))
+    for w in (1, 3, 13):
+        got = oracle.pool_rows(p, w)
+        h = w // 2
+        for idx in np.ndindex(3, 2):
+            row = p[idx]
+            np.testing.assert_allclose(got[idx][h:50 - h], np.convolve(row, np.ones(w) / w, "valid"),
+                                       rtol=1e-13)
+            # edges: mean over the in-range part of the window
+            np.testing.assert_allclose(got[idx][0], row[:h + 1].mean(), rtol=1e-13)
+            np.testing.assert_allclose(got[idx][-1], row[-h - 1:].mean(), rtol=1e-13)
+    # one window wider than the row: every output is the row mean
+    np.testing.assert_allclose(oracle.pool_rows(p[:, :, :5], 13), np.broadcast_to(
+        p[:, :, :5].mean(axis=-1, keepdims=True), (3, 2, 5)), rtol=1e-13)
+
+
+def test_head_pooling_equals_token_pooling_when_rows_coincide():
+    """With every (layer, head) row of a step equal, pooling commutes with
+    the max and, being linear, with the mean over steps: both placements
+    give the same scores."""
+    rng = np.random.default_rng(3)
+    ly, hq, hk, d, steps, n = 3, 4, 2, 16, 3, 90
+    qs = rng.standard_normal((steps, d)).astype(np.float32) * 2.0
+    k1 = rng.standard_normal((n, d)).astype(np.float32)
+    q = np.broadcast_to(qs[None, None, :, None, :], (1, ly, steps, hq, d)).copy()
+    k = np.broadcast_to(k1[None, :, None, :], (ly, n, hk, d)).copy()
+    q, k = bf16_bits_from_f32(q), bf16_bits_from_f32(k)
+    off = np.array([0, n])
+    kw = dict(pool_w=13, chunk=8, mode="fixed", keep_p=0.3)
+    tok = oracle.run(q, k, off, **kw)
+    head = oracle.run(q, k, off, pool_at="head", **kw)
+    np.testing.assert_allclose(head["imp"], tok["tok_score"], rtol=1e-12)
+    np.testing.assert_allclose(head["chunk_score"], tok["chunk_score"], rtol=1e-12)
+
+
+def test_head_pooling_with_width_one_is_the_default_path():
+    q, k, off, params = _case(1)
+    params = dict(params, pool_w=1)
+    a = oracle.run(q, k, off, **params)
+    b = oracle.run(q, k, off, pool_at="head", **params)
+    for key in ("imp", "tok_score", "chunk_score", "kept_idx"):
+        np.testing.assert_array_equal(a[key], b[key])
