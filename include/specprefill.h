@@ -89,6 +89,17 @@ enum { SP_MODE_FIXED = 0, SP_MODE_MASS = 1 };
  *   (SP_ERR_UNSUPPORTED otherwise). */
 enum { SP_RULE_EXACT = 0, SP_RULE_LISTING = 1 };
 
+/* Where the W-wide average pool applies (llama.cpp PR "Speculative
+ * prefill", §Approach item 3, lists the smoothing together with the max over
+ * heads and layers without fixing the order).
+ * SP_POOL_TOKEN: on the per-token importance, after the mean over the
+ *   lookahead steps (the scoring contract).
+ * SP_POOL_HEAD: on every attention row (layer, step, query head) before the
+ *   max over heads and layers; the later pooling step is then the identity
+ *   (sp_pool_chunk and the fused call treat pool_w as 1 after it). Requires
+ *   pool_w / 2 <= 64 (SP_ERR_UNSUPPORTED otherwise). */
+enum { SP_POOL_TOKEN = 0, SP_POOL_HEAD = 1 };
+
 /* Shapes and strides. Strides are in elements; the head_dim axis is
  * contiguous (stride 1).
  * K: bf16 keys of layer l, global token t, KV head g at
@@ -130,6 +141,7 @@ typedef struct sp_params {
     int32_t rule;              /* SP_RULE_EXACT (0) or SP_RULE_LISTING */
     int32_t min_tok;           /* SP_RULE_LISTING: >= 0 (128), bound of eff_min */
     int32_t max_keep;          /* SP_RULE_LISTING: >= 0 (2000 in the pages' tool); 0 = no cap */
+    int32_t pool_at;           /* SP_POOL_TOKEN (0) or SP_POOL_HEAD */
 } sp_params;
 
 /* Optional profiling hook: when non-null, `logits_start`/`logits_stop` are

@@ -49,6 +49,7 @@ STATUS = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED", 3: "SP_E
           4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT", 6: "SP_ERR_DEVICE"}
 MODES = {"fixed": 0, "mass": 1}
 RULES = {"exact": 0, "listing": 1}
+POOL_AT = {"token": 0, "head": 1}
 
 
 class SpecPrefillError(RuntimeError):
@@ -76,7 +77,8 @@ class _Params(ctypes.Structure):
                 ("boost_last_n", ctypes.c_int32), ("force_bos", ctypes.c_int32),
                 ("force_last_chunk", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("spin_limit", ctypes.c_int32), ("rule", ctypes.c_int32),
-                ("min_tok", ctypes.c_int32), ("max_keep", ctypes.c_int32)]
+                ("min_tok", ctypes.c_int32), ("max_keep", ctypes.c_int32),
+                ("pool_at", ctypes.c_int32)]
 
 
 class _Profile(ctypes.Structure):
@@ -89,7 +91,9 @@ class SelectionParams:
     boost x1.5 first 64 / x1.3 last 128, BOS and final chunk kept).
     rule "listing" selects like the pages' own tool (ties at the threshold,
     tokens {0,1,2,3,n-2,n-1}, fill to min(min_tok, max(4, n/10)), cap to
-    max_keep tokens when max_keep > 0)."""
+    max_keep tokens when max_keep > 0). pool_at "head" pools every attention
+    row before the max over heads and layers instead of the per-token
+    importance."""
     pool_w: int = 13
     chunk: int = 32
     mode: str = "mass"
@@ -107,6 +111,7 @@ class SelectionParams:
     rule: str = "exact"
     min_tok: int = 128
     max_keep: int = 0
+    pool_at: str = "token"
 
     def _c(self) -> _Params:
         return _Params(int(self.pool_w), int(self.chunk), MODES[self.mode], float(self.keep_p),
@@ -114,7 +119,7 @@ class SelectionParams:
                        int(self.boost_first_n), float(self.boost_last_mult), int(self.boost_last_n),
                        int(bool(self.force_bos)), int(bool(self.force_last_chunk)),
                        float(self.scale), int(self.spin_limit), RULES[self.rule],
-                       int(self.min_tok), int(self.max_keep))
+                       int(self.min_tok), int(self.max_keep), POOL_AT[self.pool_at])
 
 
 _lib = None

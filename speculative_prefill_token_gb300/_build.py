@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecprefill.so")
 SOURCES = ["sp_api.cu", "sp_stages.cu", "sp_logits_tc.cu", "sp_logits_simt.cu", "sp_noalloc.cu", "sp_post.cu",
-           "sp_rows.cu"]
+           "sp_rows.cu", "sp_head_pool.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

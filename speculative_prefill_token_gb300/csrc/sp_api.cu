@@ -63,7 +63,16 @@ int check_params(const sp_params* p) {
         return SP_ERR_INVALID_ARG;
     if ((p->rule != SP_RULE_EXACT && p->rule != SP_RULE_LISTING) || p->min_tok < 0 || p->max_keep < 0)
         return SP_ERR_INVALID_ARG;
+    if (p->pool_at != SP_POOL_TOKEN && p->pool_at != SP_POOL_HEAD) return SP_ERR_INVALID_ARG;
+    if (p->pool_at == SP_POOL_HEAD && p->pool_w / 2 > 64) return SP_ERR_UNSUPPORTED;
     return SP_OK;
+}
+
+// The fused post path is available for the parameters the steps after the
+// importance see.
+bool post_fused(const sp_params* p) {
+    const sp_params q = post_params(p);
+    return fused_post_ok(&q);
 }
 
 int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
@@ -121,6 +130,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
                                           : static_cast<double>(1.0f / std::sqrt(static_cast<float>(P.d)));
     P.scale2 = static_cast<float>(scale * 1.4426950408889634);
     P.spin = p->spin_limit > 0 ? p->spin_limit : kDefaultSpin;
+    P.head_h = (p->pool_at == SP_POOL_HEAD && p->pool_w > 1) ? p->pool_w / 2 : 0;
 
     size_t off = sizeof(WsHeader);
     auto take = [&](size_t bytes) {
@@ -207,6 +217,8 @@ int attn_importance(const sp_shape* shape, const sp_params* params, const int32_
 int select_tail(const Plan& pl, const sp_params* params, const int32_t* seq_off, const float* imp,
                 float* tok_score, float* chunk_score, uint8_t* chunk_keep, int32_t* kept_idx,
                 int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st) {
+    const sp_params pp = post_params(params);
+    params = &pp;
     float* tok_p = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
     float* cs_p = chunk_score ? chunk_score : ws_ptr<float>(ws, pl.o_cscore);
     uint8_t* keep_p = chunk_keep ? chunk_keep : ws_ptr<uint8_t>(ws, pl.o_ckeep);
@@ -251,7 +263,7 @@ int sp_kernels_per_call(const sp_shape* shape, const sp_params* params, int32_t*
     if (!n_kernels) return SP_ERR_INVALID_ARG;
     // prep, (logits, importance) per wave, then pool sums, rank, gather or
     // pool, chunk, select, gather scan, gather write
-    *n_kernels = 1 + 2 * pl.waves + (fused_post_ok(params) ? 3 : 5);
+    *n_kernels = 1 + 2 * pl.waves + (post_fused(params) ? 3 : 5);
     return SP_OK;
 }
 
@@ -293,8 +305,9 @@ int sp_pool_chunk(const sp_shape* shape, const sp_params* params, const int32_t*
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* tok = tok_score ? tok_score : ws_ptr<float>(ws, pl.o_tok);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
-    if (launch_pool(pl, params, seq_off, imp, tok, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-    return to_status(launch_chunk(pl, params, seq_off, tok, chunk_score, ws, st));
+    const sp_params pp = post_params(params);
+    if (launch_pool(pl, &pp, seq_off, imp, tok, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    return to_status(launch_chunk(pl, &pp, seq_off, tok, chunk_score, ws, st));
 }
 
 int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
@@ -344,7 +357,7 @@ int sp_specprefill_score(const sp_shape* shape, const sp_params* params, const i
     if (!seq_off || !q || !k || !kept_idx || !kept_pos || !kept_off || !n_kept || !aligned16(q) ||
         !aligned16(k))
         return SP_ERR_INVALID_ARG;
-    if (params->rule != SP_RULE_EXACT && !fused_post_ok(params)) return SP_ERR_UNSUPPORTED;
+    if (params->rule != SP_RULE_EXACT && !post_fused(params)) return SP_ERR_UNSUPPORTED;
     if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* imp_p = imp ? imp : ws_ptr<float>(ws, pl.o_imp);
@@ -364,7 +377,7 @@ int sp_select_from_importance(const sp_shape* shape, const sp_params* params,
     int rc = make_plan(shape, params, &pl);
     if (rc != SP_OK) return rc;
     if (!seq_off || !imp || !kept_idx || !kept_pos || !kept_off || !n_kept) return SP_ERR_INVALID_ARG;
-    if (params->rule != SP_RULE_EXACT && !fused_post_ok(params)) return SP_ERR_UNSUPPORTED;
+    if (params->rule != SP_RULE_EXACT && !post_fused(params)) return SP_ERR_UNSUPPORTED;
     if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;

@@ -45,6 +45,7 @@ struct Plan {
     int slabs_per_wave, waves;
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
+    int head_h;           // per-head pooling: half window (0 = pool the per-token importance)
     // workspace offsets (bytes)
     size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_lmax, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
@@ -71,8 +72,20 @@ cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* s
 
 
 // Softmax, max over heads/layers of the wave; the last wave writes imp.
+// With per-head pooling (pl.head_h > 0) every row is pooled before the max
+// (sp_head_pool.cu).
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
                           float* imp, cudaStream_t st);
+cudaError_t launch_reduce_head_pool(const Plan& pl, const int32_t* seq_off, void* ws, int nslab,
+                                    int wave, float* imp, cudaStream_t st);
+
+// The selection parameters of the steps after the importance: with
+// per-head pooling the pool has already been applied (width 1 afterwards).
+inline sp_params post_params(const sp_params* p) {
+    sp_params q = *p;
+    if (q.pool_at == SP_POOL_HEAD) q.pool_w = 1;
+    return q;
+}
 
 // Fused-path pooling: pooled scores, per-tile min / max and per-chunk sums
 // (requires fused_post_ok: the pool halo fits and chunks never straddle a

@@ -89,8 +89,9 @@ extern "C" int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* par
     // the previous call's status word, input flag and counter must not leak in
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return SP_ERR_CUDA;
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
-    if (launch_pool(pl, params, seq_off, imp, tok_score, ws, st) != cudaSuccess) return SP_ERR_CUDA;
-    if (launch_chunk(pl, params, seq_off, tok_score, chunk_score, ws, st) != cudaSuccess)
+    const sp_params pp = post_params(params);
+    if (launch_pool(pl, &pp, seq_off, imp, tok_score, ws, st) != cudaSuccess) return SP_ERR_CUDA;
+    if (launch_chunk(pl, &pp, seq_off, tok_score, chunk_score, ws, st) != cudaSuccess)
         return SP_ERR_CUDA;
     if (status_out &&
         cudaMemcpyAsync(status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

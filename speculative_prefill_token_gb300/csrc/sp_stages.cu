@@ -548,6 +548,7 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
 
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,
                           float* imp, cudaStream_t st) {
+    if (pl.head_h > 0) return launch_reduce_head_pool(pl, seq_off, ws, nslab, wave, imp, st);
     const int tok = kReduceThreads / (pl.Rs / 8);
     const int nq = (tok + 31) / 32;
     const size_t smem = sizeof(float) * (static_cast<size_t>(nq) * nslab * pl.Rs +

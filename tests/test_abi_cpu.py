@@ -218,3 +218,21 @@ def test_window_plan_matches_the_oracle(lib):
     assert lib.sp_window_plan(100, 10, 5, None, None, None, 4, ctypes.byref(cnt)) == 1
     assert lib.sp_merge_windows(100, 10, 0, ctypes.c_void_p(4096), ctypes.c_void_p(4096), None) == 1
     assert lib.sp_merge_windows(100, 10, 5, None, ctypes.c_void_p(4096), None) == 1
+
+
+def test_pool_at_validation(lib):
+    s = _shape()
+    bad = sp.SelectionParams()._c()
+    bad.pool_at = 2
+    n = ctypes.c_size_t()
+    assert lib.sp_workspace_size(ctypes.byref(s), ctypes.byref(bad), ctypes.byref(n)) == 1
+    # per-head pooling keeps its halo in shared memory: half window <= 64
+    rc, _ = _ws(s, sp.SelectionParams(pool_at="head", pool_w=131))
+    assert rc == 2
+    rc, _ = _ws(s, sp.SelectionParams(pool_at="head", pool_w=129))
+    assert rc == 0
+    # the pool is applied before the max, so the post path sees width 1: its
+    # fused kernels only need the chunk to divide 128
+    assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="head", pool_w=129, chunk=48)) == 8
+    assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="head", pool_w=129)) == 6
+    assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="token", pool_w=131)) == 8
