@@ -49,7 +49,7 @@ struct Plan {
     // workspace offsets (bytes)
     size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_lmax, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
-        o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_lcount, o_kept_off, o_nkept, total;
+        o_ppart, o_cscore, o_ckeep, o_ckoff, o_pcount, o_lcount, o_ucount, o_kept_off, o_nkept, total;
 };
 
 int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);

@@ -158,6 +158,7 @@ struct PostArgs {
     int32_t* kept_off;
     int32_t* n_kept;
     int32_t* lcount;            // listing rule: kept tokens per prompt before the fill
+    int32_t* ucount;            // listing rule: unselected, unforced tokens per slice
     WsHeader* hdr;
     int B, C, mode, normalize, force_bos, force_last;
     int rule, min_tok, max_keep;
@@ -170,7 +171,7 @@ struct RankShared {
     float mn, mx;
     unsigned long long need;
     int all, S;
-    int32_t warp_cnt[kRankWarps];
+    int32_t warp_cnt[kRankWarps], warp_spare[kRankWarps];
     int64_t red[kRankWarps];
     int64_t base[kSliceChunks];
 };
@@ -202,6 +203,7 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         if (t == 0) {
             atomicCAS(&a.hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
             a.scount[s] = 0;
+            a.ucount[s] = 0;
         }
         return;
     }
@@ -338,7 +340,7 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
             for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
     }
     if (lane == 0) {
-        int32_t my_cnt = 0;
+        int32_t my_cnt = 0, my_spare = 0;
 #pragma unroll
         for (int q = 0; q < kWarpChunks; ++q) {
             const int64_t c = ci[q];
@@ -350,15 +352,22 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
             int64_t extra = (c == 0 && a.force_bos && n > 0) ? 1 : 0;  // BOS of an unselected chunk 0
             if (listing) extra = listing_forced_in(c * a.C, c * a.C + chunk_tokens(n, a.C, c), n);
             my_cnt += static_cast<int32_t>(f ? chunk_tokens(n, a.C, c) : extra);
+            if (!f) my_spare += static_cast<int32_t>(chunk_tokens(n, a.C, c) - extra);
         }
         sh.warp_cnt[warp] = my_cnt;
+        sh.warp_spare[warp] = my_spare;
     }
     g.sync();
     if (t == 0) {
         int32_t tot = 0;
         for (int w = 0; w < kRankWarps; ++w) tot += sh.warp_cnt[w];
         a.scount[s] = tot;
-        if (listing) atomicAdd(a.lcount + b, tot);
+        if (listing) {
+            int32_t spare = 0;
+            for (int w = 0; w < kRankWarps; ++w) spare += sh.warp_spare[w];
+            a.ucount[s] = spare;
+            atomicAdd(a.lcount + b, tot);
+        }
     }
     g.sync();  // shared memory may be reused for the next slice
 }

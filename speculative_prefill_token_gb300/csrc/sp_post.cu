@@ -79,104 +79,133 @@ __device__ __forceinline__ int64_t listing_final_count(const PostArgs& a, int b)
     return (a.max_keep > 0 && k > a.max_keep) ? a.max_keep : k;
 }
 
-// Listing rule gather, one CTA per prompt plus one for the totals. The
-// prompt's kept list before the cap is: the tokens of its selected chunks
-// and its forced tokens ("kept0"), plus the first `fill` of the remaining
-// tokens ("spare") in token order. A kept0 token's position in that list is
-// the number of kept0 tokens before it plus min(fill, spare tokens before
-// it); a spare token is kept when fewer than `fill` spare tokens precede it.
-// With the cap (count k > max_keep = M, step = k / M), position p goes to
-// slot p / step when p % step == 0 and p / step < M - 1, and position k - 1
-// to slot M - 1; other positions are dropped. Each thread walks a
-// contiguous range of chunks after a block scan of the per-range counts.
+// Listing rule gather, one CTA per slice of kSliceChunks chunks plus one
+// for the totals. The prompt's kept list before the cap is: the tokens of
+// its selected chunks and its forced tokens ("kept0"), plus the first
+// `fill` of the remaining tokens ("spare") in token order. A kept0 token's
+// position in that list is the number of kept0 tokens before it plus
+// min(fill, spare tokens before it); a spare token is kept when fewer than
+// `fill` spare tokens precede it. With the cap (count k > max_keep = M,
+// step = k / M), position p goes to slot p / step when p % step == 0 and
+// p / step < M - 1, and position k - 1 to slot M - 1; other positions are
+// dropped. The counts before the slice come from the rank kernel's
+// per-slice kept0 (scount) and spare (ucount) counts, those before each
+// chunk from a scan over the slice's chunks, those before each token from
+// warp ballots.
 __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const PostArgs a) {
     grid_dep_wait();
     grid_dep_launch();
     if (a.hdr->bad_input) return;
-    __shared__ int64_t red[kRankWarps];
-    __shared__ int64_t wk[kRankWarps], wu[kRankWarps];
-    const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    // output offset: final counts of all earlier prompts
-    int64_t part = 0;
-    for (int bb = t; bb < b; bb += kRankThreads) part += listing_final_count(a, bb);
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) red[warp] = part;
+    __shared__ int64_t red[3][kRankWarps];
+    __shared__ int64_t base_k[kSliceChunks], base_u[kSliceChunks];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t S = a.slice_base[a.B];
+    const int64_t s = blockIdx.x;
+    if (s > S) return;
+    const int b = s == S ? a.B : search_base(a.slice_base, a.B, s);
+    const int64_t sb = s == S ? S : a.slice_base[b];
+    // output offset of prompt b (final counts of all earlier prompts) and
+    // the kept0 / spare tokens of the prompt's slices before this one
+    int64_t part[3] = {0, 0, 0};
+    for (int bb = t; bb < b; bb += kRankThreads) part[0] += listing_final_count(a, bb);
+    for (int64_t i = sb + t; i < s; i += kRankThreads) {
+        part[1] += __ldcg(a.scount + i);
+        part[2] += __ldcg(a.ucount + i);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        for (int o = 16; o > 0; o >>= 1) part[j] += __shfl_xor_sync(0xffffffffu, part[j], o);
+        if (lane == 0) red[j][warp] = part[j];
+    }
     __syncthreads();
-    int64_t P = 0;
-    for (int w = 0; w < kRankWarps; ++w) P += red[w];
-    if (b == a.B) {
+    int64_t P = 0, kb0 = 0, ub0 = 0;
+    for (int w = 0; w < kRankWarps; ++w) {
+        P += red[0][w];
+        kb0 += red[1][w];
+        ub0 += red[2][w];
+    }
+    if (s == S) {
         if (t == 0) {
+            for (int bb = a.B - 1; bb >= 0 && a.slice_base[bb] == S; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
             a.kept_off[a.B] = static_cast<int32_t>(P);
             *a.n_kept = static_cast<int32_t>(P);
         }
         return;
     }
-    if (t == 0) a.kept_off[b] = static_cast<int32_t>(P);
+    if (t == 0 && s == sb) {
+        // first slice of prompt b: its offset, and that of empty prompts before it
+        for (int bb = b; bb >= 0 && a.slice_base[bb] == s; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
+    }
     const int64_t start = a.seq_off[b];
     const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
     const int64_t coff = a.chunk_off[b];
     const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
-    if (nc == 0 || nc > kMaxPromptChunks) return;
+    if (nc > kMaxPromptChunks) return;  // reported by the rank kernel; nothing kept
     const int64_t k0 = __ldcg(a.lcount + b);
     const int64_t fill = min64(max64(0, listing_eff_min(n, a.min_tok) - k0), n - k0);
     const int64_t k = k0 + fill;
     const int64_t M = (a.max_keep > 0 && k > a.max_keep) ? a.max_keep : 0;
     const int64_t step = M > 0 ? k / M : 1;
-    // this thread's chunks and their kept0 / spare token counts
-    const int64_t per = (nc + kRankThreads - 1) / kRankThreads;
-    const int64_t c0 = min64(nc, t * per), c1 = min64(nc, c0 + per);
-    int64_t nk = 0, nu = 0;
-    for (int64_t c = c0; c < c1; ++c) {
-        const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
-        if (__ldcg(a.keep + coff + c) & 1) {
-            nk += a1 - a0;
-        } else {
-            const int64_t f = listing_forced_in(a0, a1, n);
-            nk += f;
-            nu += a1 - a0 - f;
+    const int64_t c_lo = (s - sb) * kSliceChunks;
+    // exclusive scans of the slice's per-chunk kept0 / spare counts (lane = chunk)
+    if (warp == 0) {
+        const int64_t c = c_lo + lane;
+        int64_t ck = 0, cu = 0;
+        if (c < nc) {
+            const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
+            if (__ldcg(a.keep + coff + c) & 1) {
+                ck = a1 - a0;
+            } else {
+                ck = listing_forced_in(a0, a1, n);
+                cu = a1 - a0 - ck;
+            }
         }
-    }
-    // block exclusive scans of both counts
-    int64_t ik = nk, iu = nu;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t vk = __shfl_up_sync(0xffffffffu, ik, o);
-        const int64_t vu = __shfl_up_sync(0xffffffffu, iu, o);
-        if (lane >= o) {
-            ik += vk;
-            iu += vu;
+        int64_t ik = ck, iu = cu;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t vk = __shfl_up_sync(0xffffffffu, ik, o);
+            const int64_t vu = __shfl_up_sync(0xffffffffu, iu, o);
+            if (lane >= o) {
+                ik += vk;
+                iu += vu;
+            }
         }
-    }
-    if (lane == 31) {
-        wk[warp] = ik;
-        wu[warp] = iu;
+        base_k[lane] = kb0 + ik - ck;
+        base_u[lane] = ub0 + iu - cu;
     }
     __syncthreads();
-    int64_t kb = ik - nk, ub = iu - nu;
-    for (int w = 0; w < warp; ++w) {
-        kb += wk[w];
-        ub += wu[w];
-    }
-    for (int64_t c = c0; c < c1; ++c) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int q = warp; q < kSliceChunks; q += kRankWarps) {
+        const int64_t c = c_lo + q;
+        if (c >= nc) break;
         const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
         const bool sel = (__ldcg(a.keep + coff + c) & 1) != 0;
-        for (int64_t tt = a0; tt < a1; ++tt) {
+        int64_t kb = base_k[q], ub = base_u[q];
+        for (int64_t g0 = a0; g0 < a1; g0 += 32) {
+            const int64_t tt = g0 + lane;
+            const bool in = tt < a1;
+            const bool kept0 = in && (sel || listing_forced(tt, n));
+            const bool spare = in && !kept0;
+            const unsigned km = __ballot_sync(0xffffffffu, kept0);
+            const unsigned um = __ballot_sync(0xffffffffu, spare);
+            const int64_t kbt = kb + __popc(km & lt), ubt = ub + __popc(um & lt);
             int64_t p = -1;
-            if (sel || listing_forced(tt, n)) {
-                p = kb + min64(fill, ub);
-                ++kb;
-            } else {
-                if (ub < fill) p = kb + ub;
-                ++ub;
+            if (kept0) p = kbt + min64(fill, ubt);
+            else if (spare && ubt < fill) p = kbt + ubt;
+            if (p >= 0) {
+                int64_t slot = p;
+                if (M > 0) {
+                    if (p == k - 1) slot = M - 1;
+                    else if (p % step == 0 && p / step < M - 1) slot = p / step;
+                    else slot = -1;
+                }
+                if (slot >= 0) {
+                    a.kept_idx[P + slot] = static_cast<int32_t>(start + tt);
+                    a.kept_pos[P + slot] = static_cast<int32_t>(tt);
+                }
             }
-            if (p < 0) continue;
-            int64_t slot = p;
-            if (M > 0) {
-                if (p == k - 1) slot = M - 1;
-                else if (p % step == 0 && p / step < M - 1) slot = p / step;
-                else continue;
-            }
-            a.kept_idx[P + slot] = static_cast<int32_t>(start + tt);
-            a.kept_pos[P + slot] = static_cast<int32_t>(tt);
+            kb += __popc(km);
+            ub += __popc(um);
         }
     }
 }
@@ -201,6 +230,7 @@ PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, f
     a.kept_off = kept_off;
     a.n_kept = n_kept;
     a.lcount = ws_ptr<int32_t>(ws, pl.o_lcount);
+    a.ucount = ws_ptr<int32_t>(ws, pl.o_ucount);
     a.hdr = ws_ptr<WsHeader>(ws, 0);
     a.B = pl.B;
     a.C = pl.C;
@@ -231,7 +261,7 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
     const cudaError_t e = launch_k(rank_kernel, static_cast<unsigned>(pl.slices_max), kRankThreads, smem, st, a);
     if (e != cudaSuccess) return e;
     if (p->rule == SP_RULE_LISTING)
-        return launch_k(listing_gather_kernel, static_cast<unsigned>(pl.B + 1), kRankThreads, 0, st, a);
+        return launch_k(listing_gather_kernel, static_cast<unsigned>(pl.slices_max + 1), kRankThreads, 0, st, a);
     return launch_k(gather_kernel, static_cast<unsigned>(pl.slices_max + 1), kRankThreads, 0, st, a);
 }
 
