@@ -17,7 +17,8 @@ ranks scored divided by the slowest rank's time.
 `pipelined` reports, beside it, the rate with --pipeline-streams calls in
 flight on as many streams, each with its own workspace and outputs;
 `listing_rule` the rate of the same calls under the pages' own selection
-rule (reference-compatibility mode); `consumer` the bandwidth of the
+rule (reference-compatibility mode), `head_pool` with the pool applied to
+every attention row before the max; `consumer` the bandwidth of the
 sparse-prefill gathers (kept token ids, kept K and V rows).
 """
 
@@ -377,28 +378,36 @@ def run_ours(args, rank, world, local):
                      "ms_per_step": p_ms / args.steps, "device_status_ok": p_ok}
     d2h = 2 * ntot * 4 + koff_host.numel() * 4 + 4
 
-    # reference-compatibility rule (the pages' own selection: threshold
-    # ties, six forced tokens, eff_min fill, 2000-token cap), reported beside
-    # the headline: the same calls with the listing rule
-    l_params = sp.SelectionParams(**dict(w.selection_kwargs(), rule="listing", min_tok=128,
-                                         max_keep=2000))
-    l_ws = sp.make_workspace(shape, l_params, dev)
-    l_out = sp.alloc_outputs(qs[0], ks[0], l_params, intermediates=False)
-    for i in range(args.warmup):
-        sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, l_params, out=l_out, ws=l_ws,
-                             stream=stream)
-    torch.cuda.synchronize()
-    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(stream)
-    for i in range(args.steps):
-        sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, l_params, out=l_out, ws=l_ws,
-                             stream=stream)
-    l1.record(stream)
-    torch.cuda.synchronize()
-    l_ms = l0.elapsed_time(l1) / args.steps
-    listing = {"what": "listing rule, min_tok 128, max_keep 2000", "ms_per_step": l_ms,
-               "value": world * ntot / (l_ms / 1e3), "unit": UNIT,
-               "kept_tokens": int(l_out.n_kept.item()), "device_status": sp.device_status(l_ws)}
+    # variants of the path, reported beside the headline: the same calls
+    # with the pages' own selection rule (threshold ties, six forced tokens,
+    # eff_min fill, 2000-token cap; reference-compatibility mode) and with
+    # the pool applied to every attention row before the max over heads
+    def time_variant(what, **over):
+        v_params = sp.SelectionParams(**dict(w.selection_kwargs(), **over))
+        v_ws = sp.make_workspace(shape, v_params, dev)
+        v_out = sp.alloc_outputs(qs[0], ks[0], v_params, intermediates=False)
+
+        def v_step(i):
+            sp.specprefill_score(qs[i % N_COPIES], ks[i % N_COPIES], off, v_params, out=v_out,
+                                 ws=v_ws, stream=stream)
+
+        for i in range(args.warmup):
+            v_step(i)
+        torch.cuda.synchronize()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for i in range(args.steps):
+            v_step(i)
+        v1.record(stream)
+        torch.cuda.synchronize()
+        v_ms = v0.elapsed_time(v1) / args.steps
+        return {"what": what, "ms_per_step": v_ms, "value": world * ntot / (v_ms / 1e3), "unit": UNIT,
+                "kernels_per_step": sp.kernels_per_call(shape, v_params),
+                "kept_tokens": int(v_out.n_kept.item()), "device_status": sp.device_status(v_ws)}
+
+    listing = time_variant("listing rule, min_tok 128, max_keep 2000", rule="listing", min_tok=128,
+                           max_keep=2000)
+    head_pool = time_variant("W=13 pool on every attention row before the max", pool_at="head")
 
     # sparse-prefill consumer, reported beside the headline: the kept
     # tokens' ids and their K and V rows (two 201 MB draft-cache tensors)
@@ -467,6 +476,7 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "pipelined": pipelined,
         "listing_rule": listing,
+        "head_pool": head_pool,
         "consumer": {"what": "kept token ids + kept K and V rows (gather_tokens, 2x gather_rows)",
                      "ms_per_step": c_ms, "bytes_per_step": c_bytes,
                      "gbs": c_bytes / (c_ms / 1e3) / 1e9, "frac": c_bytes / (c_ms / 1e3) / 1e9 / peak,
