@@ -18,6 +18,7 @@ from .specprefill_oracle import (  # noqa: F401
     gather_rows,
     fixed_count,
     importance,
+    kv_from_pages,
     listing_cap,
     listing_eff_min,
     listing_forced_tokens,

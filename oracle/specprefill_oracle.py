@@ -57,6 +57,12 @@ Reference-compatibility variants (the pages' own tool, for A/B comparison):
    §Sliding Window Loop and §Bug Fixes in v3.1; guide v2 listing `main`,
    window sizing)
 
+In-situ draft caches: a draft engine keeps K per layer in pools of
+fixed-size blocks with a per-prompt block table (logical block -> physical
+block); kv_from_pages gathers such a cache back into the dense token-major
+[Ly, Ntot, Hk, d] layout the steps above read, so the scores of a paged
+cache are by definition those of its dense gather.
+
 Readings where the pages are silent (each also listed in the design notes):
 softmax over the prompt keys only; kv head = h // G; the pool divides by the
 number of in-range tokens and never crosses a prompt boundary; normalisation
@@ -560,6 +566,34 @@ def run(q_bits: np.ndarray, k_bits: np.ndarray, seq_off: Sequence[int], *,
     out = score_from_importance(imp, seq_off, **kw)
     if keep_step_max:
         out["step_max"] = steps
+    return out
+
+
+# ---------------------------------------------------------------------------
+# in-situ draft caches
+
+
+def kv_from_pages(pools: Sequence[np.ndarray], block_table: np.ndarray, seq_off: Sequence[int],
+                  block_size: int) -> np.ndarray:
+    """Dense token-major keys from per-layer block pools.
+
+    pools: one array per layer, [num_blocks, block_size, Hk, d];
+    block_table: [B, max_blocks] physical block of each logical block of
+    prompt b; logical token t of prompt b sits in block
+    block_table[b, t // block_size] at row t % block_size.
+    Returns [Ly, Ntot, Hk, d] with prompt b at tokens seq_off[b] + t.
+    """
+    seq_off = np.asarray(seq_off, dtype=np.int64)
+    ly = len(pools)
+    _, bs, hk, d = pools[0].shape
+    if bs != block_size:
+        raise ValueError("pool block size differs from block_size")
+    out = np.zeros((ly, int(seq_off[-1]), hk, d), dtype=pools[0].dtype)
+    for layer in range(ly):
+        for b in range(len(seq_off) - 1):
+            start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
+            for t in range(n):
+                out[layer, start + t] = pools[layer][int(block_table[b, t // block_size]), t % block_size]
     return out
 
 

@@ -559,3 +559,47 @@ def test_head_pooling_with_width_one_is_the_default_path():
     b = oracle.run(q, k, off, pool_at="head", **params)
     for key in ("imp", "tok_score", "chunk_score", "kept_idx"):
         np.testing.assert_array_equal(a[key], b[key])
+
+
+# ---------------------------------------------------------------- paged caches
+
+
+def _scatter_pages(k, seq_off, block_size, rng, spare_blocks=3):
+    """Scatter dense [Ly, Ntot, Hk, d] keys into per-layer pools of shuffled
+    blocks (plus unused blocks of noise); returns (pools, block_table)."""
+    ly, _, hk, d = k.shape
+    seq_off = np.asarray(seq_off)
+    nblk = [-(-int(seq_off[b + 1] - seq_off[b]) // block_size) for b in range(len(seq_off) - 1)]
+    total = sum(nblk) + spare_blocks
+    perm = rng.permutation(total)
+    table = np.full((len(nblk), max(max(nblk), 1) + 2), -1, dtype=np.int32)
+    pools = [rng.integers(0, 1 << 16, size=(total, block_size, hk, d), dtype=np.uint16) for _ in range(ly)]
+    used = 0
+    for b, nb in enumerate(nblk):
+        start, n = int(seq_off[b]), int(seq_off[b + 1] - seq_off[b])
+        for j in range(nb):
+            phys = int(perm[used]); used += 1
+            table[b, j] = phys
+            rows = min(block_size, n - j * block_size)
+            for layer in range(ly):
+                pools[layer][phys, :rows] = k[layer, start + j * block_size:start + j * block_size + rows]
+    return pools, table
+
+
+def test_kv_from_pages_round_trip_and_scores():
+    rng = np.random.default_rng(21)
+    q, k, off = random_case(31, [37, 0, 70, 5], 2, 4, 2, 16, 2, q_gain=2.0)
+    for bs in (8, 16, 64):
+        pools, table = _scatter_pages(k, off, bs, rng)
+        dense = oracle.kv_from_pages(pools, table, off, bs)
+        assert np.array_equal(dense, k)
+    # element by element for one token of one prompt
+    pools, table = _scatter_pages(k, off, 16, rng)
+    t, b = 53, 2
+    assert np.array_equal(oracle.kv_from_pages(pools, table, off, 16)[1, off[b] + t],
+                          pools[1][table[b, t // 16], t % 16])
+    # the scores of the paged cache are those of the dense keys
+    kw = dict(pool_w=5, chunk=4, mode="fixed", keep_p=0.3)
+    a = oracle.run(q, k, off, **kw)
+    bb = oracle.run(q, oracle.kv_from_pages(pools, table, off, 16), off, **kw)
+    assert np.array_equal(a["imp"], bb["imp"]) and np.array_equal(a["kept_idx"], bb["kept_idx"])
