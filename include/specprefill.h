@@ -267,6 +267,45 @@ int sp_gather_rows(const sp_shape* shape, const int32_t* kept_idx, const int32_t
 int sp_gather_tokens(const int32_t* token_ids, int64_t n_tokens_total, const int32_t* kept_idx,
                      const int32_t* n_kept, int32_t* out, sp_stream_t stream);
 
+/* Keys read in place from a draft engine's cache (in-situ scoring): one
+ * key pool per layer, as draft engines allocate them, instead of one
+ * [Ly][Ntot][Hk][d] tensor.
+ * - layer_k: host array of n_layers (<= 64) device pointers, 16-byte
+ *   aligned; pool row r, KV head g, element j of layer l at
+ *   layer_k[l][r*k_stride_token + g*k_stride_head + j] (the shape's
+ *   k_stride_token and k_stride_head; k_stride_layer is not used).
+ * - block_table NULL: pool row = packed token index (seq_off[b] + t);
+ *   pool_tokens >= n_tokens_total.
+ * - block_table non-NULL (device, [n_seqs][table_stride] int32): a
+ *   block-paged cache; token t of prompt b is pool row
+ *   block_table[b*table_stride + t/block_size]*block_size + t%block_size.
+ *   block_size is 8, 16, 32 or 64, or a multiple of 128; every prompt's
+ *   blocks must fit in its table row (else the call's device status is
+ *   SP_ERR_DEVICE and nothing is scored); a block id whose rows fall outside
+ *   [0, pool_tokens) sets SP_ERR_DEVICE and reads pool row 0 instead.
+ * - pool_tokens: rows of each layer's pool (num_blocks * block_size), at
+ *   most 2^31 - 1. */
+typedef struct sp_kv_source {
+    const uint16_t* const* layer_k;
+    const int32_t* block_table;
+    int32_t block_size;
+    int32_t table_stride;
+    int64_t pool_tokens;
+} sp_kv_source;
+
+/* sp_attn_importance and sp_specprefill_score with the keys from `kv`
+ * (the tensor-core path; same outputs, same workspace size for the same
+ * shape). */
+int sp_attn_importance_kv(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                          const uint16_t* q, const sp_kv_source* kv, float* imp, void* ws,
+                          size_t ws_bytes, sp_stream_t stream);
+int sp_specprefill_score_kv(const sp_shape* shape, const sp_params* params,
+                            const int32_t* seq_off, const uint16_t* q, const sp_kv_source* kv,
+                            float* imp, float* tok_score, float* chunk_score, int32_t* chunk_off,
+                            uint8_t* chunk_keep, int32_t* kept_idx, int32_t* kept_pos,
+                            int32_t* kept_off, int32_t* n_kept, void* ws, size_t ws_bytes,
+                            sp_stream_t stream);
+
 /* Sliding-window scoring of the pages' tool ("SpecPrefill — Implementation
  * Guide", v3.1 §Sliding Window Loop and §Bug Fixes in v3.1): a prompt longer
  * than the draft's context is scored in windows of `window` tokens starting

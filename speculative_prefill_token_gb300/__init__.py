@@ -34,6 +34,9 @@ __all__ = [
     "gather_rows",
     "gather_tokens",
     "select_from_importance",
+    "kv_source",
+    "specprefill_score_kv",
+    "attn_importance_kv",
     "auto_window",
     "window_plan",
     "merge_windows",
@@ -79,6 +82,12 @@ class _Params(ctypes.Structure):
                 ("spin_limit", ctypes.c_int32), ("rule", ctypes.c_int32),
                 ("min_tok", ctypes.c_int32), ("max_keep", ctypes.c_int32),
                 ("pool_at", ctypes.c_int32)]
+
+
+class _KvSource(ctypes.Structure):
+    _fields_ = [("layer_k", ctypes.POINTER(ctypes.c_void_p)), ("block_table", ctypes.c_void_p),
+                ("block_size", ctypes.c_int32), ("table_stride", ctypes.c_int32),
+                ("pool_tokens", ctypes.c_int64)]
 
 
 class _Profile(ctypes.Structure):
@@ -158,6 +167,9 @@ def load(path: Optional[str] = None):
         "sp_window_plan": [ctypes.c_int64, i32, i32, _P, _P, _P, i32, ctypes.POINTER(ctypes.c_int32)],
         "sp_merge_windows": [ctypes.c_int64, i32, i32, _P, _P, _P],
         "sp_gather_tokens": [_P, ctypes.c_int64, _P, _P, _P, _P],
+        "sp_attn_importance_kv": [sp, pp, _P, _P, ctypes.POINTER(_KvSource), _P, _P, _SZ, _P],
+        "sp_specprefill_score_kv": [sp, pp, _P, _P, ctypes.POINTER(_KvSource), _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _SZ, _P],
         "sp_get_device_status": [_P, _SZ, _P, i32, ctypes.POINTER(ctypes.c_int32)],
     }
     for name, args in sigs.items():
@@ -509,6 +521,105 @@ def merge_windows(imp_windows, n: int, window: int, stride: int, out=None, strea
     _check(lib().sp_merge_windows(int(n), int(window), int(stride), imp_windows.data_ptr(),
                                   out.data_ptr(), _stream(stream)), "sp_merge_windows")
     return out
+
+
+def kv_source(layer_k, block_table=None, block_size: int = 0):
+    """Key source over a draft engine's cache: ``layer_k`` is a list of one
+    bf16 key pool per layer, each [rows, Hk, d] or, block-paged,
+    [num_blocks, block_size, Hk, d] (d contiguous, rows evenly strided);
+    ``block_table`` (int32, device, [B, max_blocks]) maps each prompt's
+    logical blocks to pool blocks. Returns (struct, keep-alive, token stride,
+    head stride, Hk, d)."""
+    import torch
+    k0 = layer_k[0]
+    if k0.dim() == 4:
+        nb, bs, hk, d = k0.shape
+        if k0.stride(0) != bs * k0.stride(1):
+            raise ValueError("blocks of a pool must follow one another with the token stride")
+        rows, st_tok, st_head = nb * bs, k0.stride(1), k0.stride(2)
+        if block_table is not None and block_size not in (0, bs):
+            raise ValueError("block_size differs from the pools' block dimension")
+        block_size = bs if block_table is not None else 0
+    elif k0.dim() == 3:
+        rows, hk, d = k0.shape
+        st_tok, st_head = k0.stride(0), k0.stride(1)
+    else:
+        raise ValueError("each layer pool is [rows, Hk, d] or [blocks, block_size, Hk, d]")
+    for kl in layer_k:
+        if (kl.dtype != torch.bfloat16 or kl.shape != k0.shape or kl.stride() != k0.stride()
+                or kl.stride(-1) != 1):
+            raise ValueError("every layer pool must be bf16 with the first one's shape and strides")
+    ptrs = (ctypes.c_void_p * len(layer_k))(*[kl.data_ptr() for kl in layer_k])
+    table_stride = 0
+    if block_table is not None:
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.stride(1) != 1:
+            raise ValueError("block_table must be an int32 [B, max_blocks] tensor, rows contiguous")
+        table_stride = block_table.stride(0)
+    src = _KvSource(ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)), _ptr(block_table),
+                    int(block_size), int(table_stride), int(rows))
+    return src, ptrs, int(st_tok), int(st_head), int(hk), int(d)
+
+
+def shape_of_kv(q, layer_k, n_tokens_total: int, block_table=None) -> "_Shape":
+    """Shape struct of a draft-cache call: Q as in shape_of, keys from the
+    per-layer pools (their token and head strides)."""
+    _, _, st_tok, st_head, hk, d = kv_source(layer_k, block_table)
+    b, ly, steps, hq, dq = q.shape
+    if dq != d or ly != len(layer_k):
+        raise ValueError("q and the pools disagree on layers or head_dim")
+    return _Shape(int(b), int(ly), int(hq), int(hk), int(d), int(steps), int(n_tokens_total), 0,
+                  st_tok, st_tok, st_head, q.stride(0), q.stride(1), q.stride(2), q.stride(3))
+
+
+def specprefill_score_kv(q, layer_k, seq_off, n_tokens_total: int, params: SelectionParams,
+                         block_table=None, out: Optional[ScoreOutputs] = None, ws=None,
+                         stream=None) -> ScoreOutputs:
+    """The whole path with the keys read in place from per-layer (optionally
+    block-paged) pools; n_tokens_total = seq_off[-1]."""
+    import torch
+    src, keep, *_ = kv_source(layer_k, block_table)
+    shape = shape_of_kv(q, layer_k, n_tokens_total, block_table)
+    dev = q.device
+    if out is None:
+        nb = shape.n_seqs
+        nch = max_chunks(shape, params)
+        out = ScoreOutputs(kept_idx=torch.empty(n_tokens_total, dtype=torch.int32, device=dev),
+                           kept_pos=torch.empty(n_tokens_total, dtype=torch.int32, device=dev),
+                           kept_off=torch.empty(nb + 1, dtype=torch.int32, device=dev),
+                           n_kept=torch.empty(1, dtype=torch.int32, device=dev),
+                           imp=torch.empty(n_tokens_total, dtype=torch.float32, device=dev),
+                           tok_score=torch.empty(n_tokens_total, dtype=torch.float32, device=dev),
+                           chunk_score=torch.empty(nch, dtype=torch.float32, device=dev),
+                           chunk_off=torch.empty(nb + 1, dtype=torch.int32, device=dev),
+                           chunk_keep=torch.empty(nch, dtype=torch.uint8, device=dev))
+    if ws is None:
+        ws = make_workspace(shape, params, dev)
+    _check(lib().sp_specprefill_score_kv(
+        ctypes.byref(shape), ctypes.byref(params._c()), seq_off.data_ptr(), q.data_ptr(),
+        ctypes.byref(src), _ptr(out.imp), _ptr(out.tok_score), _ptr(out.chunk_score),
+        _ptr(out.chunk_off), _ptr(out.chunk_keep), out.kept_idx.data_ptr(), out.kept_pos.data_ptr(),
+        out.kept_off.data_ptr(), out.n_kept.data_ptr(), *_ws_args(ws), _stream(stream)),
+        "sp_specprefill_score_kv")
+    del keep
+    return out
+
+
+def attn_importance_kv(q, layer_k, seq_off, n_tokens_total: int, params: SelectionParams,
+                       block_table=None, imp=None, ws=None, stream=None):
+    """imp[t] for every packed token, keys read in place from the pools."""
+    import torch
+    src, keep, *_ = kv_source(layer_k, block_table)
+    shape = shape_of_kv(q, layer_k, n_tokens_total, block_table)
+    if imp is None:
+        imp = torch.empty(n_tokens_total, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = make_workspace(shape, params, q.device)
+    _check(lib().sp_attn_importance_kv(ctypes.byref(shape), ctypes.byref(params._c()),
+                                       seq_off.data_ptr(), q.data_ptr(), ctypes.byref(src),
+                                       imp.data_ptr(), *_ws_args(ws), _stream(stream)),
+           "sp_attn_importance_kv")
+    del keep
+    return imp
 
 
 def device_status(ws, stream=None, clear: bool = True) -> int:

@@ -173,7 +173,7 @@ namespace {
 
 int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, const uint16_t* q,
                      const uint16_t* k, float* imp, void* ws, cudaStream_t st, bool simt,
-                     const sp_profile* prof) {
+                     const sp_profile* prof, const KvSrc* kv = nullptr) {
     if (prof && prof->logits_start)
         if (cudaEventRecord(reinterpret_cast<cudaEvent_t>(prof->logits_start), st) != cudaSuccess)
             return SP_ERR_CUDA;
@@ -186,7 +186,7 @@ int importance_waves(const Plan& pl, const sp_shape* s, const int32_t* seq_off, 
             e = launch_logits_simt(pl, s, seq_off, q, k, ws, slab0, ns, &grid, st);
         } else {
             grid = logits_tc_grid(pl, ns);
-            e = launch_logits_tc(pl, s, seq_off, q, k, ws, slab0, ns, grid, st);
+            e = launch_logits_tc(pl, s, seq_off, q, k, ws, slab0, ns, grid, st, kv);
         }
         if (e != cudaSuccess) return SP_ERR_CUDA;
         if (w == pl.waves - 1 && prof && prof->logits_stop)
@@ -209,6 +209,38 @@ int attn_importance(const sp_shape* shape, const sp_params* params, const int32_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_prep(pl, seq_off, ws, nullptr, st) != cudaSuccess) return SP_ERR_CUDA;
     return importance_waves(pl, shape, seq_off, q, k, imp, ws, st, simt, nullptr);
+}
+
+// Checks a draft-cache key source, builds the plan (the shape's unused
+// layer stride is replaced) and the device-side descriptor.
+int kv_plan(const sp_shape* shape, const sp_params* params, const sp_kv_source* kv, sp_shape* s2,
+            KvSrc* src, Plan* pl) {
+    if (!shape || !kv || !kv->layer_k) return SP_ERR_INVALID_ARG;
+    *s2 = *shape;
+    s2->k_stride_layer = shape->k_stride_token;  // not used: one pool per layer
+    int rc = make_plan(s2, params, pl);
+    if (rc != SP_OK) return rc;
+    if (pl->Ly > kMaxKvLayers) return SP_ERR_UNSUPPORTED;
+    if (kv->pool_tokens < 1 || kv->pool_tokens > INT32_MAX) return SP_ERR_INVALID_ARG;
+    std::memset(src, 0, sizeof(*src));
+    for (int l = 0; l < pl->Ly; ++l) {
+        if (!kv->layer_k[l] || !aligned16(kv->layer_k[l])) return SP_ERR_INVALID_ARG;
+        src->layer_k[l] = kv->layer_k[l];
+    }
+    src->pool_tokens = kv->pool_tokens;
+    if (kv->block_table) {
+        const int bs = kv->block_size;
+        const bool ok_bs = bs == 8 || bs == 16 || bs == 32 || bs == 64 || (bs >= 128 && bs % 128 == 0);
+        if (!ok_bs || kv->table_stride < 1) return SP_ERR_INVALID_ARG;
+        src->block_table = kv->block_table;
+        src->block_size = bs;
+        src->table_stride = kv->table_stride;
+        pl->kv_block_size = bs;
+        pl->kv_table_stride = kv->table_stride;
+    } else if (kv->pool_tokens < pl->Ntot) {
+        return SP_ERR_INVALID_ARG;
+    }
+    return SP_OK;
 }
 
 // Steps after the importance: pool (+ normalise, boost, chunk sums), chunk
@@ -383,6 +415,44 @@ int sp_select_from_importance(const sp_shape* shape, const sp_params* params,
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
     return select_tail(pl, params, seq_off, imp, tok_score, chunk_score, chunk_keep, kept_idx,
+                       kept_pos, kept_off, n_kept, ws, st);
+}
+
+int sp_attn_importance_kv(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                          const uint16_t* q, const sp_kv_source* kv, float* imp, void* ws,
+                          size_t ws_bytes, sp_stream_t stream) {
+    sp_shape s2;
+    KvSrc src;
+    Plan pl;
+    int rc = kv_plan(shape, params, kv, &s2, &src, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !q || !imp || !aligned16(q)) return SP_ERR_INVALID_ARG;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_prep(pl, seq_off, ws, nullptr, st) != cudaSuccess) return SP_ERR_CUDA;
+    return importance_waves(pl, &s2, seq_off, q, nullptr, imp, ws, st, false, nullptr, &src);
+}
+
+int sp_specprefill_score_kv(const sp_shape* shape, const sp_params* params, const int32_t* seq_off,
+                            const uint16_t* q, const sp_kv_source* kv, float* imp, float* tok_score,
+                            float* chunk_score, int32_t* chunk_off, uint8_t* chunk_keep,
+                            int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off, int32_t* n_kept,
+                            void* ws, size_t ws_bytes, sp_stream_t stream) {
+    sp_shape s2;
+    KvSrc src;
+    Plan pl;
+    int rc = kv_plan(shape, params, kv, &s2, &src, &pl);
+    if (rc != SP_OK) return rc;
+    if (!seq_off || !q || !kept_idx || !kept_pos || !kept_off || !n_kept || !aligned16(q))
+        return SP_ERR_INVALID_ARG;
+    if (params->rule != SP_RULE_EXACT && !post_fused(params)) return SP_ERR_UNSUPPORTED;
+    if ((rc = check_ws(pl, ws, ws_bytes)) != SP_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* imp_p = imp ? imp : ws_ptr<float>(ws, pl.o_imp);
+    if (launch_prep(pl, seq_off, ws, chunk_off, st) != cudaSuccess) return SP_ERR_CUDA;
+    if ((rc = importance_waves(pl, &s2, seq_off, q, nullptr, imp_p, ws, st, false, nullptr, &src)) != SP_OK)
+        return rc;
+    return select_tail(pl, params, seq_off, imp_p, tok_score, chunk_score, chunk_keep, kept_idx,
                        kept_pos, kept_off, n_kept, ws, st);
 }
 

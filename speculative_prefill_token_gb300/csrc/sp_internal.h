@@ -14,6 +14,7 @@ constexpr int kTileTokens = 128;   // tokens per logits tile (tensor-core M)
 constexpr int kMaxRows = 64;       // max query rows per slab (L * G)
 constexpr int kPostBlockTarget = 1024;
 constexpr int kMaxSeqs = 65536;
+constexpr int kMaxKvLayers = 64;    // per-layer key pools (one tensor map each, kernel parameters)
 constexpr int kMaxChunk = 8192;
 constexpr int kMaxPool = 8191;
 constexpr int kMaxPromptChunks = 16384;  // per-prompt chunk count the in-CTA selection handles
@@ -46,6 +47,7 @@ struct Plan {
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
     int head_h;           // per-head pooling: half window (0 = pool the per-token importance)
+    int kv_block_size, kv_table_stride;  // block-paged key source (checked by the prep kernel)
     // workspace offsets (bytes)
     size_t o_tile_base, o_chunk_off, o_pblk_base, o_slice_base, o_scount, o_segcnt, o_logits, o_lmax, o_part, o_lse, o_alog, o_imp, o_tok,
         o_rpart, o_csum,
@@ -66,9 +68,19 @@ cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_
 // (one 128-row slot per tile), plus softmax records per (CTA, segment,
 // warpgroup). Tensor-core (tcgen05 + TMA) kernel on `grid` CTAs.
 int logits_tc_grid(const Plan& pl, int nslab);
+// Keys held per layer by a draft engine: one pool per layer, addressed by
+// the packed token index, or (block_table != nullptr) by blocks of
+// block_size tokens through a per-prompt table of physical block ids.
+struct KvSrc {
+    const uint16_t* layer_k[kMaxKvLayers];
+    const int32_t* block_table;  // [B][table_stride], device
+    int block_size, table_stride;
+    int64_t pool_tokens;         // token rows in each layer's pool
+};
+// With kv != nullptr the keys come from kv (k is unused).
 cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                              const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                             int grid, cudaStream_t st);
+                             int grid, cudaStream_t st, const KvSrc* kv = nullptr);
 
 
 // Softmax, max over heads/layers of the wave; the last wave writes imp.

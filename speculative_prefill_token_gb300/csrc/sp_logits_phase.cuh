@@ -70,6 +70,12 @@ struct TcArgs {
     uint32_t q_block_bytes;  // Nmma * 128
     float scale2;
     int64_t spin;
+    // key source: 0 = one tensor map (token, head, layer); 1 = one map per
+    // layer, packed token index; 2 = one map per layer, block-paged
+    int kv_mode, n_layers;
+    const int32_t* block_table;  // kv_mode 2: [B][table_stride]
+    int block_size, table_stride, box_h, nbox;  // box_h tokens per TMA box, nbox boxes per tile
+    int64_t pool_tokens;
 };
 
 struct SmemLayout {
@@ -224,7 +230,7 @@ __device__ __forceinline__ void logits_setup(LogitsCtx& c, const TcArgs& a, cons
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
-        prefetch_tmap(tmap_k);
+        for (int l = 0; l < (a.kv_mode ? a.n_layers : 1); ++l) prefetch_tmap(tmap_k + l);
         prefetch_tmap(tmap_q);
         prefetch_tmap(tmap_s);
     }
@@ -241,6 +247,117 @@ __device__ __forceinline__ void logits_teardown(const LogitsCtx& c, const TcArgs
     if ((threadIdx.x >> 5) == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(c.tmem_base, static_cast<uint32_t>(kAcc * a.Nacc));
+    }
+}
+
+// Block-paged keys (kv_mode 2): the key-map row of box `lane` (< nbox) of
+// the cursor's tile. Box j covers logical tokens [t, t + box_h) of the
+// prompt, t = 128 i + j box_h, inside one block; boxes past the prompt's end
+// read its last block (those rows are masked later). A block id outside the
+// pool is reported and replaced by row 0.
+__device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur, int lane) {
+    if (lane >= a.nbox) return 0;
+    const int64_t t = static_cast<int64_t>(cur.it.tile - cur.base_b) * kTileTokens +
+                      static_cast<int64_t>(lane) * a.box_h;
+    int64_t lb = t / a.block_size;
+    const int64_t lb_max = (static_cast<int64_t>(cur.n) - 1) / a.block_size;
+    if (lb > lb_max) lb = lb_max;
+    const int64_t page = a.block_table[static_cast<int64_t>(cur.it.b) * a.table_stride + lb];
+    const int64_t row = page * a.block_size + t % a.block_size;
+    if (page < 0 || row + a.box_h > a.pool_tokens) {
+        atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_DEVICE));
+        return 0;
+    }
+    return static_cast<int>(row);
+}
+
+// Producer of the block-paged path, run by the whole producer warp: lane 0
+// waits on the ring and issues the copies (nbox boxes per 16 KB stage);
+// lane j < nbox looks up the block of box j, one item ahead, so that the
+// table's latency overlaps the current item's copies.
+__device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& a,
+                                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
+                                              int64_t T, int64_t w_begin, int64_t w_end, int lane) {
+    constexpr unsigned kFull = 0xffffffffu;
+    const uint64_t pol = policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    int qn = 0;
+    int64_t prev_key = -1;
+    uint32_t issued_phase[kMaxStages];
+    bool issued[kMaxStages];
+    for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
+    bool ok = true;
+    ItemCursor cur, nxt;
+    int row = 0;
+    if (w_begin < w_end) {
+        cur.set(a, w_begin, T);
+        row = paged_row(a, cur, lane);
+    }
+    for (int64_t w = w_begin; w < w_end; ++w) {
+        int row_next = 0;
+        if (w + 1 < w_end) {
+            nxt = cur;
+            nxt.next(a, w + 1, T);
+            row_next = paged_row(a, nxt, lane);
+        }
+        const Item& it = cur.it;
+        const int slab = a.slab0 + it.slab;
+        const int layer = slab / a.Hk, g = slab - layer * a.Hk;
+        const int64_t key = static_cast<int64_t>(it.slab) * a.B + it.b;
+        if (key != prev_key) {
+            const int qb = qn & 1;
+            if (lane == 0 && !mbar_wait_bounded(c.bar_qempty + 8 * qb, ((qn >> 1) & 1) ^ 1, a.spin,
+                                                c.abort_flag)) {
+                record_timeout(a, c.abort_flag);
+                ok = false;
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(c.bar_qfull + 8 * qb, static_cast<uint32_t>(a.R) * 128u * a.d_blocks);
+                for (int kb = 0; kb < a.d_blocks; ++kb)
+                    tma_load_5d(c.q_buf + qb * c.q_stage_bytes + kb * a.q_block_bytes, tmap_q,
+                                c.bar_qfull + 8 * qb, kb * 64, g * a.G, 0, layer, it.b);
+            }
+            ++qn;
+            prev_key = key;
+        }
+        for (int kb = 0; kb < a.d_blocks; ++kb) {
+            if (lane == 0 && !mbar_wait_bounded(c.bar_empty + 8 * stage, phase ^ 1, a.spin, c.abort_flag)) {
+                record_timeout(a, c.abort_flag);
+                ok = false;
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(c.bar_full + 8 * stage, kKBlockBytes);
+            for (int j = 0; j < a.nbox; ++j) {
+                const int rj = __shfl_sync(kFull, row, j);
+                if (lane == 0)
+                    tma_load_4d(c.k_ring + stage * kKBlockBytes + static_cast<uint32_t>(j * a.box_h) * 128u,
+                                tmap_k + layer, c.bar_full + 8 * stage, kb * 64, rj, g, 0, pol);
+            }
+            if (lane == 0) {
+                issued[stage] = true;
+                issued_phase[stage] = phase;
+            }
+            if (++stage == a.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        if (!ok) break;
+        cur = nxt;
+        row = row_next;
+    }
+    if (lane == 0) {
+        // drain: every copy this thread issued must land before exit
+        for (int s = 0; s < a.stages; ++s)
+            if (issued[s]) mbar_wait_spin(c.bar_full + 8 * s, issued_phase[s], kDrainSpin);
+        for (int i = 0; i < 2 && i < qn; ++i) {
+            const int last = (qn - 1 - i);
+            mbar_wait_spin(c.bar_qfull + 8 * (last & 1), (last >> 1) & 1, kDrainSpin);
+        }
     }
 }
 
@@ -265,7 +382,9 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
     const int64_t w_begin = split_start(W, C, cta);
     const int64_t w_end = split_start(W, C, cta + 1);
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && a.kv_mode == 2) {
+        produce_paged(c, a, tmap_k, tmap_q, T, w_begin, w_end, lane);
+    } else if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int stage = 0;
@@ -306,8 +425,8 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                         break;
                     }
                     mbar_arrive_expect_tx(bar_full + 8 * stage, kKBlockBytes);
-                    tma_load_4d(k_ring + stage * kKBlockBytes, tmap_k, bar_full + 8 * stage,
-                                kb * 64, it.tok0, g, layer, pol);
+                    tma_load_4d(k_ring + stage * kKBlockBytes, a.kv_mode ? tmap_k + layer : tmap_k,
+                                bar_full + 8 * stage, kb * 64, it.tok0, g, a.kv_mode ? 0 : layer, pol);
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == a.stages) {

@@ -34,6 +34,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     logits_teardown(c, a);
 }
 
+// Per-layer key maps of a draft engine's cache (kv_mode 1 and 2), passed
+// as one kernel parameter.
+struct KvMaps {
+    CUtensorMap m[kMaxKvLayers];
+};
+
+template <int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    logits_tc_kv_kernel(const __grid_constant__ KvMaps kmaps,
+                        const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    LogitsCtx c = logits_ctx<NH>(smem_raw, a);
+    logits_setup(c, a, kmaps.m, &tmap_q, &tmap_s);
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t T = *a.bad ? 0 : a.tile_base[a.B];
+    logits_phase<NH>(c, a, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    logits_teardown(c, a);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -148,8 +169,49 @@ cudaError_t logits_config(const Plan& pl, const int32_t* seq_off, void* ws, int 
     a.q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
     a.scale2 = pl.scale2;
     a.spin = pl.spin;
+    a.kv_mode = 0;
+    a.n_layers = pl.Ly;
+    a.block_table = nullptr;
+    a.block_size = 0;
+    a.table_stride = 0;
+    a.box_h = kTileTokens;
+    a.nbox = 1;
+    a.pool_tokens = pl.Ntot;
     return logits_smem(pl, &a.stages, smem, nh);
 }
+
+namespace {
+
+// Tokens per K box of a key source: one 128-token box, or one box per block
+// of a block-paged cache whose blocks are shorter than a tile.
+int kv_box_h(const KvSrc* kv) {
+    return (kv && kv->block_table && kv->block_size < kTileTokens) ? kv->block_size : kTileTokens;
+}
+
+cudaError_t make_kv_maps(const Plan& pl, const sp_shape* s, const KvSrc* kv, KvMaps* km) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int d = pl.d;
+    const int64_t sh = pl.Hk > 1 ? s->k_stride_head : d;
+    for (int l = 0; l < pl.Ly; ++l) {
+        // dims (d, pool row, kv head, 1)
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv->pool_tokens),
+                              static_cast<cuuint64_t>(pl.Hk), 1};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(s->k_stride_token) * 2,
+                                 static_cast<cuuint64_t>(sh) * 2,
+                                 static_cast<cuuint64_t>(s->k_stride_token) * 2 *
+                                     static_cast<cuuint64_t>(kv->pool_tokens)};
+        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kv_box_h(kv)), 1, 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&km->m[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(kv->layer_k[l]),
+                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
 
 int logits_tc_grid(const Plan& pl, int nslab) {
     int dev = 0, sms = 0;
@@ -161,18 +223,36 @@ int logits_tc_grid(const Plan& pl, int nslab) {
 
 cudaError_t launch_logits_tc(const Plan& pl, const sp_shape* s, const int32_t* seq_off,
                              const uint16_t* q, const uint16_t* k, void* ws, int slab0, int nslab,
-                             int grid, cudaStream_t st) {
+                             int grid, cudaStream_t st, const KvSrc* kv) {
     LogitsMaps m;
-    cudaError_t err = make_logits_maps(pl, s, q, k, ws, nslab, &m);
+    // without a key source the single K map addresses k; with one, the
+    // single map is not used (it is built over the first layer's pool)
+    cudaError_t err = make_logits_maps(pl, s, q, kv ? kv->layer_k[0] : k, ws, nslab, &m);
     if (err != cudaSuccess) return err;
     TcArgs a;
     uint32_t smem = 0;
     int nh = 1;
     if ((err = logits_config(pl, seq_off, ws, slab0, nslab, &a, &smem, &nh)) != cudaSuccess) return err;
-    auto kern = nh == 2 ? logits_tc_kernel<2> : logits_tc_kernel<1>;
+    if (!kv) {
+        auto kern = nh == 2 ? logits_tc_kernel<2> : logits_tc_kernel<1>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        return launch_k(kern, grid, kThreads, smem, st, m.k, m.q, m.s, a);
+    }
+    KvMaps km;  // the launch copies the maps into the kernel's parameter space
+    if ((err = make_kv_maps(pl, s, kv, &km)) != cudaSuccess) return err;
+    a.kv_mode = kv->block_table ? 2 : 1;
+    a.n_layers = pl.Ly;
+    a.block_table = kv->block_table;
+    a.block_size = kv->block_table ? kv->block_size : 0;
+    a.table_stride = kv->table_stride;
+    a.box_h = kv_box_h(kv);
+    a.nbox = kTileTokens / a.box_h;
+    a.pool_tokens = kv->pool_tokens;
+    auto kern = nh == 2 ? logits_tc_kv_kernel<2> : logits_tc_kv_kernel<1>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    return launch_k(kern, grid, kThreads, smem, st, m.k, m.q, m.s, a);
+    return launch_k(kern, grid, kThreads, smem, st, km, m.q, m.s, a);
 }
 
 }  // namespace sp

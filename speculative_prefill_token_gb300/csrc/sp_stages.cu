@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
                                                             int32_t* chunk_off_out,
                                                             const int32_t* chunk_off_check,
                                                             unsigned* seg_cnt, int64_t n_seg_cnt,
+                                                            int block_size, int table_stride,
                                                             WsHeader* hdr) {
     grid_dep_wait();
     grid_dep_launch();
@@ -52,8 +53,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
         hdr->ticket = 0u;
     }
     __syncthreads();
-    for (int b = tid; b < B; b += kPrepThreads)
-        if (seq_off[b + 1] < seq_off[b]) bad = 1;
+    for (int b = tid; b < B; b += kPrepThreads) {
+        const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
+        if (n < 0) bad = 1;
+        // a block-paged key source must list every block of the prompt
+        if (block_size > 0 && (n + block_size - 1) / block_size > table_stride) bad = 1;
+    }
     for (int64_t i = tid; i < n_seg_cnt; i += kPrepThreads) seg_cnt[i] = 0u;
     __syncthreads();
     const int per = (B + kPrepThreads - 1) / kPrepThreads;
@@ -531,7 +536,7 @@ cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), chunk_off_out,
         nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
-        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B,
+        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B, pl.kv_block_size, pl.kv_table_stride,
         ws_ptr<WsHeader>(ws, 0));
 }
 
@@ -542,7 +547,7 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), nullptr,
         chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
-        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B,
+        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B, pl.kv_block_size, pl.kv_table_stride,
         ws_ptr<WsHeader>(ws, 0));
 }
 

@@ -236,3 +236,31 @@ def test_pool_at_validation(lib):
     assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="head", pool_w=129, chunk=48)) == 8
     assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="head", pool_w=129)) == 6
     assert sp.kernels_per_call(s, sp.SelectionParams(pool_at="token", pool_w=131)) == 8
+
+
+def test_kv_source_validation(lib):
+    """Draft-cache key sources are checked on the host before any launch."""
+    s = _shape(n_tokens_total=4096, n_layers=2)
+    p = sp.SelectionParams()._c()
+    a = ctypes.c_void_p(4096)
+
+    def call(ptrs, table=None, bs=0, stride=0, rows=4096, shape=s):
+        # a 16-byte workspace: every call that passes the checks stops there
+        arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        src = sp._KvSource(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), table, bs, stride, rows)
+        return lib.sp_specprefill_score_kv(ctypes.byref(shape), ctypes.byref(p), a, a, ctypes.byref(src),
+                                           None, None, None, None, None, a, a, a, a, a, 16, None)
+
+    good = [8192, 12288]
+    assert lib.sp_specprefill_score_kv(ctypes.byref(s), ctypes.byref(p), a, a, None, None, None,
+                                       None, None, None, a, a, a, a, a, 1 << 40, None) == 1
+    assert call([8192, None]) == 1                     # a missing layer pool
+    assert call([8192, 12296]) == 1                    # not 16-byte aligned
+    assert call(good, rows=4095) == 1                  # pool shorter than the packed tokens
+    assert call(good, table=4096, bs=12, stride=8) == 1     # unsupported block size
+    assert call(good, table=4096, bs=16, stride=0) == 1     # empty table rows
+    assert call(good, table=4096, bs=16, stride=8, rows=1 << 31) == 1  # rows past int32
+    many = _shape(n_tokens_total=4096, n_layers=65)
+    assert call([8192] * 65, shape=many) == 2          # more layers than tensor maps
+    # the workspace check comes after: a valid source reaches it
+    assert call(good, table=4096, bs=16, stride=256) == 3
