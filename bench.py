@@ -18,7 +18,8 @@ ranks scored divided by the slowest rank's time.
 flight on as many streams, each with its own workspace and outputs;
 `listing_rule` the rate of the same calls under the pages' own selection
 rule (reference-compatibility mode), `head_pool` with the pool applied to
-every attention row before the max; `consumer` the bandwidth of the
+every attention row before the max, `paged_kv` with the keys read in place
+from a block-paged draft cache; `consumer` the bandwidth of the
 sparse-prefill gathers (kept token ids, kept K and V rows).
 """
 
@@ -409,6 +410,48 @@ def run_ours(args, rank, world, local):
                            max_keep=2000)
     head_pool = time_variant("W=13 pool on every attention row before the max", pool_at="head")
 
+    # keys read in place from a block-paged draft cache: one pool of
+    # 16-token blocks per layer, the prompt's blocks shuffled over the pool
+    # (a copy of the same keys per rotation, so inputs stay larger than L2)
+    bs = 16
+    nblk = -(-ntot // bs)
+    perm = torch.from_numpy(np.random.default_rng(0).permutation(nblk)).to(dev)
+    table = perm.to(torch.int32).view(1, nblk)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nblk, device=dev)
+    kv_pools = []
+    for x in ks:
+        kk = x.view(torch.bfloat16).view(shape.n_layers, ntot, shape.n_kv_heads, shape.head_dim)
+        pad = nblk * bs - ntot
+        if pad:
+            kk = torch.cat([kk, kk[:, :pad]], dim=1)
+        blocks = kk.reshape(shape.n_layers, nblk, bs, shape.n_kv_heads, shape.head_dim)
+        kv_pools.append([blocks[l][inv].contiguous() for l in range(shape.n_layers)])
+    kv_shape = sp.shape_of_kv(qs[0], kv_pools[0], ntot, table)
+    kv_ws = sp.make_workspace(kv_shape, params, dev)
+    kv_out = sp.alloc_outputs(qs[0], ks[0], params, intermediates=False)
+
+    def kv_step(i):
+        sp.specprefill_score_kv(qs[i % N_COPIES], kv_pools[i % N_COPIES], off, ntot, params,
+                                block_table=table, out=kv_out, ws=kv_ws, stream=stream)
+
+    for i in range(args.warmup):
+        kv_step(i)
+    torch.cuda.synchronize()
+    k0e, k1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0e.record(stream)
+    for i in range(args.steps):
+        kv_step(i)
+    k1e.record(stream)
+    torch.cuda.synchronize()
+    kv_ms = k0e.elapsed_time(k1e) / args.steps
+    paged = {"what": "keys read in place from per-layer pools of 16-token blocks (shuffled)",
+             "ms_per_step": kv_ms, "value": world * ntot / (kv_ms / 1e3), "unit": UNIT,
+             "kept_tokens": int(kv_out.n_kept.item()), "device_status": sp.device_status(kv_ws),
+             "same_kept_as_dense": bool(torch.equal(kv_out.kept_idx[:n_kept], out.kept_idx[:n_kept]))
+             if int(kv_out.n_kept.item()) == n_kept else False}
+    del kv_pools
+
     # sparse-prefill consumer, reported beside the headline: the kept
     # tokens' ids and their K and V rows (two 201 MB draft-cache tensors)
     # gathered on the device from the scoring call's kept list
@@ -477,6 +520,7 @@ def run_ours(args, rank, world, local):
         "pipelined": pipelined,
         "listing_rule": listing,
         "head_pool": head_pool,
+        "paged_kv": paged,
         "consumer": {"what": "kept token ids + kept K and V rows (gather_tokens, 2x gather_rows)",
                      "ms_per_step": c_ms, "bytes_per_step": c_bytes,
                      "gbs": c_bytes / (c_ms / 1e3) / 1e9, "frac": c_bytes / (c_ms / 1e3) / 1e9 / peak,

@@ -250,20 +250,26 @@ __device__ __forceinline__ void logits_teardown(const LogitsCtx& c, const TcArgs
     }
 }
 
-// Block-paged keys (kv_mode 2): the key-map row of box `lane` (< nbox) of
-// the cursor's tile. Box j covers logical tokens [t, t + box_h) of the
-// prompt, t = 128 i + j box_h, inside one block; boxes past the prompt's end
-// read its last block (those rows are masked later). A block id outside the
-// pool is reported and replaced by row 0.
-__device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur, int lane) {
+// Block-paged keys (kv_mode 2). Box j of a tile covers logical tokens
+// [t, t + box_h) of the prompt, t = 128 i + j box_h, inside one block;
+// boxes past the prompt's end read its last block (those rows are masked
+// later). paged_block requests the block id of box `lane` of the cursor's
+// tile without using it (so the lane does not wait for it); paged_row turns
+// it into a key-map row when the copies are issued, and reports a block
+// outside the pool (replaced by row 0).
+__device__ __forceinline__ int paged_block(const TcArgs& a, const ItemCursor& cur, int lane) {
     if (lane >= a.nbox) return 0;
     const int64_t t = static_cast<int64_t>(cur.it.tile - cur.base_b) * kTileTokens +
                       static_cast<int64_t>(lane) * a.box_h;
-    int64_t lb = t / a.block_size;
-    const int64_t lb_max = (static_cast<int64_t>(cur.n) - 1) / a.block_size;
-    if (lb > lb_max) lb = lb_max;
-    const int64_t page = a.block_table[static_cast<int64_t>(cur.it.b) * a.table_stride + lb];
-    const int64_t row = page * a.block_size + t % a.block_size;
+    const int64_t lb = min64(t / a.block_size, (static_cast<int64_t>(cur.n) - 1) / a.block_size);
+    return a.block_table[static_cast<int64_t>(cur.it.b) * a.table_stride + lb];
+}
+
+__device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur, int lane, int page) {
+    if (lane >= a.nbox) return 0;
+    const int64_t t = static_cast<int64_t>(cur.it.tile - cur.base_b) * kTileTokens +
+                      static_cast<int64_t>(lane) * a.box_h;
+    const int64_t row = static_cast<int64_t>(page) * a.block_size + t % a.block_size;
     if (page < 0 || row + a.box_h > a.pool_tokens) {
         atomicCAS(a.status, 0, static_cast<int32_t>(SP_ERR_DEVICE));
         return 0;
@@ -273,8 +279,9 @@ __device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur,
 
 // Producer of the block-paged path, run by the whole producer warp: lane 0
 // waits on the ring and issues the copies (nbox boxes per 16 KB stage);
-// lane j < nbox looks up the block of box j, one item ahead, so that the
-// table's latency overlaps the current item's copies.
+// lane j < nbox looks up the block of box j three items ahead, so that
+// the table's latency overlaps the copies of the items before it (also at
+// the start, where the ring is still empty).
 __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& a,
                                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                                               int64_t T, int64_t w_begin, int64_t w_end, int lane) {
@@ -288,18 +295,34 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
     bool issued[kMaxStages];
     for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
     bool ok = true;
-    ItemCursor cur, nxt;
-    int row = 0;
+    // block ids of the current item (p0) and of the next three (p1..p3);
+    // `ahead` is the cursor of the last item looked up
+    ItemCursor cur, ahead;
+    int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
     if (w_begin < w_end) {
         cur.set(a, w_begin, T);
-        row = paged_row(a, cur, lane);
+        ahead = cur;
+        p0 = paged_block(a, ahead, lane);
+        if (w_begin + 1 < w_end) {
+            ahead.next(a, w_begin + 1, T);
+            p1 = paged_block(a, ahead, lane);
+        }
+        if (w_begin + 2 < w_end) {
+            ahead.next(a, w_begin + 2, T);
+            p2 = paged_block(a, ahead, lane);
+        }
+        if (w_begin + 3 < w_end) {
+            ahead.next(a, w_begin + 3, T);
+            p3 = paged_block(a, ahead, lane);
+        }
     }
     for (int64_t w = w_begin; w < w_end; ++w) {
-        int row_next = 0;
-        if (w + 1 < w_end) {
-            nxt = cur;
-            nxt.next(a, w + 1, T);
-            row_next = paged_row(a, nxt, lane);
+        if (w > w_begin) cur.next(a, w, T);
+        const int row = paged_row(a, cur, lane, p0);
+        int pn = 0;
+        if (w + 4 < w_end) {
+            ahead.next(a, w + 4, T);
+            pn = paged_block(a, ahead, lane);
         }
         const Item& it = cur.it;
         const int slab = a.slab0 + it.slab;
@@ -347,8 +370,10 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
             }
         }
         if (!ok) break;
-        cur = nxt;
-        row = row_next;
+        p0 = p1;
+        p1 = p2;
+        p2 = p3;
+        p3 = pn;
     }
     if (lane == 0) {
         // drain: every copy this thread issued must land before exit
