@@ -73,14 +73,21 @@ struct TcArgs {
     // key source: 0 = one tensor map (token, head, layer); 1 = one map per
     // layer, packed token index; 2 = one map per layer, block-paged
     int kv_mode, n_layers;
+    int epi_wait;   // the epilogue waits for the prep kernel (the other roles did not)
+    int64_t Ntot;
     const int32_t* block_table;  // kv_mode 2: [B][table_stride]
     int block_size, table_stride, box_h, nbox;  // box_h tokens per TMA box, nbox boxes per tile
     int64_t pool_tokens;
 };
 
 struct SmemLayout {
-    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, seg_flag, stats, total;
+    uint32_t k_ring, q_buf, out_buf, bars, tmem_slot, abort_flag, seg_flag, stats, tile_base, total;
 };
+
+// Batches of at most this many prompts get their tile offsets computed by
+// every CTA of the logits kernel itself (from seq_off, a call input), so
+// that its producer and MMA warps need not wait for the prep kernel.
+constexpr int kLocalPrompts = 256;
 
 __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint32_t q_block_bytes,
                                                   int nh) {
@@ -103,6 +110,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
     off += 8;
     s.stats = off;
     off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
+    s.tile_base = off;          // [kLocalPrompts + 1] int32, then per-warp sums
+    off += 4u * (kLocalPrompts + 1 + kThreads / 32);
     s.total = off;
     return s;
 }
@@ -238,6 +247,39 @@ __device__ __forceinline__ void logits_setup(LogitsCtx& c, const TcArgs& a, cons
     __syncthreads();
     tc_fence_after();
     c.tmem_base = *c.tmem_slot;
+}
+
+// Tile offsets of the batch computed by this CTA (all kThreads threads,
+// B <= kLocalPrompts) from seq_off: tb[b] = sum over earlier prompts of
+// ceil(n / 128), tb[B] the total; returns the tile count, 0 when seq_off is
+// not a valid packing of Ntot tokens (or, for a block-paged key source, a
+// prompt has more blocks than its table row), as the prep kernel decides.
+__device__ __forceinline__ int64_t local_tile_base(const TcArgs& a, int32_t* tb) {
+    int32_t* warp_sum = tb + kLocalPrompts + 1;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    int ok = 1;
+    int32_t tiles = 0;
+    if (t < a.B) {
+        const int64_t n = static_cast<int64_t>(a.seq_off[t + 1]) - a.seq_off[t];
+        if (n < 0) ok = 0;
+        if (a.kv_mode == 2 && (n + a.block_size - 1) / a.block_size > a.table_stride) ok = 0;
+        tiles = n > 0 ? static_cast<int32_t>((n + kTileTokens - 1) / kTileTokens) : 0;
+    }
+    if (t == 0 && (a.seq_off[0] != 0 || static_cast<int64_t>(a.seq_off[a.B]) != a.Ntot)) ok = 0;
+    int32_t incl = tiles;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    ok = __syncthreads_and(ok);
+    int32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += warp_sum[w];
+    if (t < a.B) tb[t] = before + incl - tiles;
+    if (t == a.B - 1) tb[a.B] = before + incl;
+    __syncthreads();
+    const int64_t T = ok ? static_cast<int64_t>(tb[a.B]) : 0;
+    return T < a.tiles_max ? T : a.tiles_max;
 }
 
 // Frees the tensor memory (all kThreads threads).
@@ -536,7 +578,9 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             }
         }
     } else {
-        // epilogue warpgroups
+        // epilogue warpgroups; the per-segment counters they update are
+        // zeroed by the prep kernel
+        if (a.epi_wait) grid_dep_wait();
         const int e = warp >> 2;          // warpgroup: tiles j with j % 2 == e
         const int qw = warp & 3;          // TMEM lane quarter
         const int bar_id = 1 + e;

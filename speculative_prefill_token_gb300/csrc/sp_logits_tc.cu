@@ -17,6 +17,28 @@
 namespace sp {
 namespace {
 
+// Tile count of the call and, for small batches, this CTA's own tile
+// offsets: the call's inputs (seq_off, Q, K) were complete before the prep
+// kernel passed its own wait, so the producer and MMA warps start at once
+// and only the epilogue waits for the prep kernel's counters; larger
+// batches wait for the prep kernel's offsets. The dependent kernel may
+// launch from here on.
+__device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, TcArgs& la) {
+    int64_t T;
+    if (la.B <= kLocalPrompts) {
+        int32_t* tb = reinterpret_cast<int32_t*>(c.smem + c.L.tile_base);
+        T = local_tile_base(la, tb);
+        la.tile_base = tb;
+        la.epi_wait = 1;
+    } else {
+        grid_dep_wait();
+        T = *la.bad ? 0 : la.tile_base[la.B];  // invalid offsets: no work, normal teardown
+        la.epi_wait = 0;
+    }
+    grid_dep_launch();
+    return T;
+}
+
 template <int NH>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -25,12 +47,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
     logits_setup(c, a, &tmap_k, &tmap_q, &tmap_s);
-    // everything above touched only this CTA's shared and tensor memory; the
-    // offsets and counters below come from the preceding kernel
-    grid_dep_wait();
-    grid_dep_launch();
-    const int64_t T = *a.bad ? 0 : a.tile_base[a.B];  // invalid offsets: no work, normal teardown
-    logits_phase<NH>(c, a, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    TcArgs la = a;
+    const int64_t T = logits_start(c, la);
+    logits_phase<NH>(c, la, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
@@ -48,10 +67,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
     logits_setup(c, a, kmaps.m, &tmap_q, &tmap_s);
-    grid_dep_wait();
-    grid_dep_launch();
-    const int64_t T = *a.bad ? 0 : a.tile_base[a.B];
-    logits_phase<NH>(c, a, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    TcArgs la = a;
+    const int64_t T = logits_start(c, la);
+    logits_phase<NH>(c, la, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
@@ -170,6 +188,8 @@ cudaError_t logits_config(const Plan& pl, const int32_t* seq_off, void* ws, int 
     a.scale2 = pl.scale2;
     a.spin = pl.spin;
     a.kv_mode = 0;
+    a.epi_wait = 0;
+    a.Ntot = pl.Ntot;
     a.n_layers = pl.Ly;
     a.block_table = nullptr;
     a.block_size = 0;
