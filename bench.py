@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "2093f60dcee70b3a7bfedd3d0864ea5b3b82a7c8", "bytes_per_launch": 202496256}
+TRAFFIC = {"source_sha1": "b8db307fdfd190248bb76de8ecf1a7cab53855f9", "bytes_per_launch": 202254592}
 
 
 def parse():
