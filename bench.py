@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "b8db307fdfd190248bb76de8ecf1a7cab53855f9", "bytes_per_launch": 202254592}
+TRAFFIC = {"source_sha1": "b23e28d7abe04b5647ad7ab7f0451840c8cc9be3", "bytes_per_launch": 202689152}
 
 
 def parse():

@@ -73,7 +73,6 @@ struct TcArgs {
     // key source: 0 = one tensor map (token, head, layer); 1 = one map per
     // layer, packed token index; 2 = one map per layer, block-paged
     int kv_mode, n_layers;
-    int epi_wait;   // the epilogue waits for the prep kernel (the other roles did not)
     int64_t Ntot;
     const int32_t* block_table;  // kv_mode 2: [B][table_stride]
     int block_size, table_stride, box_h, nbox;  // box_h tokens per TMA box, nbox boxes per tile
@@ -133,12 +132,14 @@ struct ItemCursor {
     int next_b;  // first tile of the next prompt
     int start, n;
 
+    const int32_t* tb;  // the batch's tile offsets (the CTA's own copy or the prep kernel's)
+
     __device__ __forceinline__ void set(const TcArgs& a, int64_t w, int64_t T) {
         it.slab = static_cast<int>(w / T);
         it.tile = static_cast<int>(w - static_cast<int64_t>(it.slab) * T);
-        it.b = search_base(a.tile_base, a.B, it.tile);
-        base_b = a.tile_base[it.b];
-        next_b = a.tile_base[it.b + 1];
+        it.b = search_base(tb, a.B, it.tile);
+        base_b = tb[it.b];
+        next_b = tb[it.b + 1];
         start = a.seq_off[it.b];
         n = a.seq_off[it.b + 1] - start;
         place();
@@ -324,7 +325,7 @@ __device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur,
 // lane j < nbox looks up the block of box j three items ahead, so that
 // the table's latency overlaps the copies of the items before it (also at
 // the start, where the ring is still empty).
-__device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& a,
+__device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& a, const int32_t* tb,
                                               const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                                               int64_t T, int64_t w_begin, int64_t w_end, int lane) {
     constexpr unsigned kFull = 0xffffffffu;
@@ -340,6 +341,7 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
     // block ids of the current item (p0) and of the next three (p1..p3);
     // `ahead` is the cursor of the last item looked up
     ItemCursor cur, ahead;
+    cur.tb = tb;
     int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
     if (w_begin < w_end) {
         cur.set(a, w_begin, T);
@@ -432,7 +434,8 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
 // On return every TMA store of this CTA has completed; the CTA is not
 // synchronised.
 template <int NH>
-__device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a, const CUtensorMap* tmap_k,
+__device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a, const int32_t* tb, int epi_wait,
+                                             const CUtensorMap* tmap_k,
                                              const CUtensorMap* tmap_q, const CUtensorMap* tmap_s,
                                              int64_t T, int64_t C, int64_t cta) {
     uint8_t* const smem = c.smem;
@@ -450,7 +453,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
     const int64_t w_end = split_start(W, C, cta + 1);
 
     if (warp == kProducerWarp && a.kv_mode == 2) {
-        produce_paged(c, a, tmap_k, tmap_q, T, w_begin, w_end, lane);
+        produce_paged(c, a, tb, tmap_k, tmap_q, T, w_begin, w_end, lane);
     } else if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
@@ -463,6 +466,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             for (int s = 0; s < kMaxStages; ++s) issued[s] = false;
             bool ok = true;
             ItemCursor cur;
+            cur.tb = tb;
             for (int64_t w = w_begin; w < w_end && ok; ++w) {
                 if (w == w_begin) cur.set(a, w, T);
                 else cur.next(a, w, T);
@@ -522,6 +526,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             bool ok = true;
             bool any_mma = false;
             ItemCursor cur;
+            cur.tb = tb;
             for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
                 if (w == w_begin) cur.set(a, w, T);
                 else cur.next(a, w, T);
@@ -580,7 +585,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
     } else {
         // epilogue warpgroups; the per-segment counters they update are
         // zeroed by the prep kernel
-        if (a.epi_wait) grid_dep_wait();
+        if (epi_wait) grid_dep_wait();
         const int e = warp >> 2;          // warpgroup: tiles j with j % 2 == e
         const int qw = warp & 3;          // TMEM lane quarter
         const int bar_id = 1 + e;
@@ -600,6 +605,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
         bool ok = true;
         int64_t j = 0;
         ItemCursor cur;
+        cur.tb = tb;
         for (int64_t w = w_begin; w < w_end; ++w, ++j) {
             if (w == w_begin) cur.set(a, w, T);
             else cur.next(a, w, T);
@@ -608,7 +614,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             if (key != cur_key) {
                 if (cur_key >= 0) {
                     flush_rows<NH>(run, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
-                    segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
+                    segment_done(tb, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2,
                                  a.R, a.Rs, st_sm, seg_flag, qw, bar_id);
                 }
                 cur_key = key;
@@ -691,7 +697,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
         }
         if (ok && cur_key >= 0) {
             flush_rows<NH>(run, st_sm, qw, bar_id, a.rec + ((cta + cur_key) * 2 + e) * a.Rs, a.R);
-            segment_done(a.tile_base, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
+            segment_done(tb, a.B, a.nslab, C, cur_key, 1, a.rec, a.seg_cnt, a.lse2, a.R,
                          a.Rs, st_sm, seg_flag, qw, bar_id);
         }
         if (qw == 0 && lane == 0 && stores) bulk_wait0();

@@ -23,17 +23,19 @@ namespace {
 // and only the epilogue waits for the prep kernel's counters; larger
 // batches wait for the prep kernel's offsets. The dependent kernel may
 // launch from here on.
-__device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, TcArgs& la) {
+__device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, const TcArgs& a, const int32_t** tb,
+                                                int* epi_wait) {
     int64_t T;
-    if (la.B <= kLocalPrompts) {
-        int32_t* tb = reinterpret_cast<int32_t*>(c.smem + c.L.tile_base);
-        T = local_tile_base(la, tb);
-        la.tile_base = tb;
-        la.epi_wait = 1;
+    if (a.B <= kLocalPrompts) {
+        int32_t* own = reinterpret_cast<int32_t*>(c.smem + c.L.tile_base);
+        T = local_tile_base(a, own);
+        *tb = own;
+        *epi_wait = 1;
     } else {
         grid_dep_wait();
-        T = *la.bad ? 0 : la.tile_base[la.B];  // invalid offsets: no work, normal teardown
-        la.epi_wait = 0;
+        T = *a.bad ? 0 : a.tile_base[a.B];  // invalid offsets: no work, normal teardown
+        *tb = a.tile_base;
+        *epi_wait = 0;
     }
     grid_dep_launch();
     return T;
@@ -47,9 +49,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
     logits_setup(c, a, &tmap_k, &tmap_q, &tmap_s);
-    TcArgs la = a;
-    const int64_t T = logits_start(c, la);
-    logits_phase<NH>(c, la, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    const int32_t* tb;
+    int epi_wait;
+    const int64_t T = logits_start(c, a, &tb, &epi_wait);
+    logits_phase<NH>(c, a, tb, epi_wait, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
@@ -67,9 +70,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
     logits_setup(c, a, kmaps.m, &tmap_q, &tmap_s);
-    TcArgs la = a;
-    const int64_t T = logits_start(c, la);
-    logits_phase<NH>(c, la, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    const int32_t* tb;
+    int epi_wait;
+    const int64_t T = logits_start(c, a, &tb, &epi_wait);
+    logits_phase<NH>(c, a, tb, epi_wait, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
@@ -188,7 +192,6 @@ cudaError_t logits_config(const Plan& pl, const int32_t* seq_off, void* ws, int 
     a.scale2 = pl.scale2;
     a.spin = pl.spin;
     a.kv_mode = 0;
-    a.epi_wait = 0;
     a.Ntot = pl.Ntot;
     a.n_layers = pl.Ly;
     a.block_table = nullptr;
