@@ -52,7 +52,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kKBlockBytes = kTileTokens * 128;  // 128 tokens x 64 bf16
 constexpr int kStageOutBytes = kTileTokens * 64;   // 128 tokens x 32 quantised 16-bit logits
 constexpr int kMaxStages = 16;
-constexpr int kRingStages = 8;   // stages the host configures (at most kMaxStages)
+constexpr int kRingStages = 6;   // stages the host configures (at most kMaxStages)
 constexpr int kAcc = 4;                          // TMEM accumulators (tiles in flight)
 constexpr int kSmemLimit = 232448;              // per-block opt-in maximum on sm_100-class parts
 constexpr int64_t kDrainSpin = int64_t(1) << 22;

@@ -158,7 +158,7 @@ cudaError_t logits_smem(const Plan& pl, int* stages, uint32_t* smem, int* nh) {
     const uint32_t q_block_bytes = static_cast<uint32_t>(pl.Nmma) * 128u;
     *nh = pl.Rs > 32 ? 2 : 1;
     const uint32_t fixed = smem_layout(0, d_blocks, q_block_bytes, *nh).total + 1024;
-    // A ring of kRingStages 16 KB stages (2 tiles in flight) already keeps the
+    // A ring of kRingStages 16 KB stages (1.5 tiles in flight) already keeps the
     // key stream at its rate; the shared memory it leaves lets the small
     // kernels of other calls (streams) share the SM with a logits CTA.
     int st = static_cast<int>((kSmemLimit - static_cast<int>(fixed)) / kKBlockBytes);
