@@ -256,18 +256,35 @@ __device__ __forceinline__ void logits_setup(LogitsCtx& c, const TcArgs& a, cons
 // ceil(n / 128), tb[B] the total; returns the tile count, 0 when seq_off is
 // not a valid packing of Ntot tokens (or, for a block-paged key source, a
 // prompt has more blocks than its table row), as the prep kernel decides.
-__device__ __forceinline__ int64_t local_tile_base(const TcArgs& a, int32_t* tb) {
+// The prompt bounds of thread t < B, requested (by logits_offsets_request)
+// before the CTA's setup so that their latency overlaps it.
+struct PromptBounds {
+    int32_t lo, hi;
+};
+
+__device__ __forceinline__ PromptBounds logits_offsets_request(const TcArgs& a) {
+    PromptBounds pb{0, 0};
+    const int t = threadIdx.x;
+    if (a.B <= kLocalPrompts && t < a.B) {
+        pb.lo = a.seq_off[t];
+        pb.hi = a.seq_off[t + 1];
+    }
+    return pb;
+}
+
+__device__ __forceinline__ int64_t local_tile_base(const TcArgs& a, PromptBounds pb, int32_t* tb) {
     int32_t* warp_sum = tb + kLocalPrompts + 1;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     int ok = 1;
     int32_t tiles = 0;
     if (t < a.B) {
-        const int64_t n = static_cast<int64_t>(a.seq_off[t + 1]) - a.seq_off[t];
+        const int64_t n = static_cast<int64_t>(pb.hi) - pb.lo;
         if (n < 0) ok = 0;
         if (a.kv_mode == 2 && (n + a.block_size - 1) / a.block_size > a.table_stride) ok = 0;
         tiles = n > 0 ? static_cast<int32_t>((n + kTileTokens - 1) / kTileTokens) : 0;
+        if (t == 0 && pb.lo != 0) ok = 0;
+        if (t == a.B - 1 && static_cast<int64_t>(pb.hi) != a.Ntot) ok = 0;
     }
-    if (t == 0 && (a.seq_off[0] != 0 || static_cast<int64_t>(a.seq_off[a.B]) != a.Ntot)) ok = 0;
     int32_t incl = tiles;
     for (int o = 1; o < 32; o <<= 1) {
         const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);

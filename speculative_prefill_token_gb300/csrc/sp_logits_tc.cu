@@ -23,12 +23,12 @@ namespace {
 // and only the epilogue waits for the prep kernel's counters; larger
 // batches wait for the prep kernel's offsets. The dependent kernel may
 // launch from here on.
-__device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, const TcArgs& a, const int32_t** tb,
-                                                int* epi_wait) {
+__device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, const TcArgs& a, PromptBounds pb,
+                                                const int32_t** tb, int* epi_wait) {
     int64_t T;
     if (a.B <= kLocalPrompts) {
         int32_t* own = reinterpret_cast<int32_t*>(c.smem + c.L.tile_base);
-        T = local_tile_base(a, own);
+        T = local_tile_base(a, pb, own);
         *tb = own;
         *epi_wait = 1;
     } else {
@@ -48,10 +48,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
+    const PromptBounds pb = logits_offsets_request(a);
     logits_setup(c, a, &tmap_k, &tmap_q, &tmap_s);
     const int32_t* tb;
     int epi_wait;
-    const int64_t T = logits_start(c, a, &tb, &epi_wait);
+    const int64_t T = logits_start(c, a, pb, &tb, &epi_wait);
     logits_phase<NH>(c, a, tb, epi_wait, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
@@ -69,10 +70,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_s, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     LogitsCtx c = logits_ctx<NH>(smem_raw, a);
+    const PromptBounds pb = logits_offsets_request(a);
     logits_setup(c, a, kmaps.m, &tmap_q, &tmap_s);
     const int32_t* tb;
     int epi_wait;
-    const int64_t T = logits_start(c, a, &tb, &epi_wait);
+    const int64_t T = logits_start(c, a, pb, &tb, &epi_wait);
     logits_phase<NH>(c, a, tb, epi_wait, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
