@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "b23e28d7abe04b5647ad7ab7f0451840c8cc9be3", "bytes_per_launch": 202689152}
+TRAFFIC = {"source_sha1": "1e84e8f593cd12bdcf564ad4a30b24e9cde43946", "bytes_per_launch": 201999232}
 
 
 def parse():
