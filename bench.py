@@ -16,7 +16,9 @@ ranks scored divided by the slowest rank's time.
 `value` is the single-stream rate (one call after another on one stream).
 `pipelined` reports, beside it, the rate with --pipeline-streams calls in
 flight on as many streams, each with its own workspace and outputs;
-`listing_rule` the rate of the same calls under the pages' own selection
+`importance_paths` the importance phase with the tcgen05 logits kernel and
+with the CUDA-core one; `listing_rule` the rate of the same calls under the
+pages' own selection
 rule (reference-compatibility mode), `head_pool` with the pool applied to
 every attention row before the max, `paged_kv` with the keys read in place
 from a block-paged draft cache; `consumer` the bandwidth of the
@@ -406,6 +408,32 @@ def run_ours(args, rank, world, local):
                 "kernels_per_step": sp.kernels_per_call(shape, v_params),
                 "kept_tokens": int(v_out.n_kept.item()), "device_status": sp.device_status(v_ws)}
 
+    # the tensor-core choice: token importance (logits + importance kernels,
+    # prep included) with the tcgen05 logits kernel against the CUDA-core
+    # (SIMT, fp32 FMA) logits kernel of the same path
+    imp_buf = torch.empty(ntot, dtype=torch.float32, device=dev)
+    imp_ws = sp.make_workspace(shape, params, dev)
+
+    def time_importance(simt):
+        for i in range(args.warmup):
+            sp.attn_importance(qs[i % N_COPIES], ks[i % N_COPIES], off, params, imp=imp_buf, ws=imp_ws,
+                               stream=stream, simt=simt)
+        torch.cuda.synchronize()
+        i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        i0.record(stream)
+        for i in range(args.steps):
+            sp.attn_importance(qs[i % N_COPIES], ks[i % N_COPIES], off, params, imp=imp_buf, ws=imp_ws,
+                               stream=stream, simt=simt)
+        i1.record(stream)
+        torch.cuda.synchronize()
+        return i0.elapsed_time(i1) / args.steps
+
+    imp_tc_ms, imp_simt_ms = time_importance(False), time_importance(True)
+    importance_paths = {"what": "token importance only (prep, logits, importance kernels)",
+                        "tcgen05_ms": imp_tc_ms, "simt_fp32_ms": imp_simt_ms,
+                        "simt_over_tcgen05": imp_simt_ms / imp_tc_ms,
+                        "device_status": sp.device_status(imp_ws)}
+
     listing = time_variant("listing rule, min_tok 128, max_keep 2000", rule="listing", min_tok=128,
                            max_keep=2000)
     head_pool = time_variant("W=13 pool on every attention row before the max", pool_at="head")
@@ -518,6 +546,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "pipelined": pipelined,
+        "importance_paths": importance_paths,
         "listing_rule": listing,
         "head_pool": head_pool,
         "paged_kv": paged,
