@@ -1,6 +1,6 @@
 // The logits phase of the SpecPrefill scoring path on fifth-generation
-// tensor cores (sm_103a), shared by the stand-alone logits kernel and the
-// persistent fused kernel.
+// tensor cores (sm_103a), shared by the logits kernels for dense and for
+// in-situ (per-layer, block-paged) key sources.
 //
 // For one (layer l, KV head g) "slab" and one prompt, the logits are
 //   s[t, r] = <k[l, t, g, :], q[l, step(r), g*G + head(r), :]>   (unscaled)

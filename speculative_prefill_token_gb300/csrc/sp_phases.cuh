@@ -1,8 +1,6 @@
 // Per-item phases of the SpecPrefill scoring path after the token
-// importance, written as device functions for a group of threads so that
-// the stand-alone kernels (one item per CTA) and the persistent fused kernel
-// (items strided over a fixed grid, phases separated by grid barriers) run
-// the same code:
+// importance, written as device functions for a group of threads (the
+// kernels run one item per CTA):
 //
 //   pool_tile     one 128-token tile: W-window mean of the importance
 //                 (llama.cpp PR "Speculative prefill" §Approach item 3), the
@@ -15,9 +13,8 @@
 //   gather_slice  kept token indices and positions of one slice (guide
 //                 §How It Works / Sparse Prefill) and the per-prompt offsets
 //
-// Values written by other CTAs (in the persistent kernel: earlier in the
-// same launch) are read through L2 (ld.global.cg), never from a possibly
-// stale L1 line.
+// Values written by other CTAs or kernels are read through L2
+// (ld.global.cg), never from a possibly stale L1 line.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -39,6 +36,100 @@ struct GroupBar {
     }
 };
 
+// --------------------------------------------------------------- locate
+// Item x (a tile or slice) of a per-prompt base table (base[0] = 0,
+// non-decreasing, base[B] = the item count): its prompt b = the last b < B
+// with base[b] <= x, base[b], base[B], the first prompt f <= b with
+// base[f] = base[b] (prompts f .. b-1 are empty), and aux[k][b],
+// aux[k][b + 1] for NA more tables of B + 1 entries. For B < 32 kLocRegs
+// every lane of the warp loads entries lane + 32 j of each table, so all of
+// it takes one round of loads, and b and f come from ballots; larger
+// batches search. Called by whole warps with x uniform across the warp.
+constexpr int kLocRegs = 2;
+
+template <int NA>
+struct Located {
+    int b, first;
+    int32_t base_b, total;
+    int32_t lo[NA > 0 ? NA : 1], hi[NA > 0 ? NA : 1];
+};
+
+__device__ __forceinline__ int32_t lane_pick(const int32_t (&v)[kLocRegs], int j) {
+    int32_t out = 0;
+#pragma unroll
+    for (int k = 0; k < kLocRegs; ++k) {
+        const int32_t u = __shfl_sync(0xffffffffu, v[k], j & 31);
+        if ((j >> 5) == k) out = u;
+    }
+    return out;
+}
+
+template <int NA>
+__device__ __forceinline__ Located<NA> locate(const int32_t* base, const int32_t* const (&aux)[NA > 0 ? NA : 1],
+                                              int B, int64_t x) {
+    Located<NA> r;
+    if (B < 32 * kLocRegs) {
+        const int lane = threadIdx.x & 31;
+        int32_t v[kLocRegs], w[NA > 0 ? NA : 1][kLocRegs];
+#pragma unroll
+        for (int k = 0; k < kLocRegs; ++k) {
+            const int j = lane + 32 * k;
+            v[k] = j <= B ? base[j] : 0;
+#pragma unroll
+            for (int q = 0; q < NA; ++q) w[q][k] = j <= B ? aux[q][j] : 0;
+        }
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < kLocRegs; ++k)
+            cnt += __popc(__ballot_sync(0xffffffffu, lane + 32 * k < B && v[k] <= x));
+        r.b = cnt > 0 ? cnt - 1 : 0;
+        r.base_b = lane_pick(v, r.b);
+        r.total = lane_pick(v, B);
+        int before = 0;
+#pragma unroll
+        for (int k = 0; k < kLocRegs; ++k)
+            before += __popc(__ballot_sync(0xffffffffu, lane + 32 * k < B && v[k] < r.base_b));
+        r.first = before;
+#pragma unroll
+        for (int q = 0; q < NA; ++q) {
+            r.lo[q] = lane_pick(w[q], r.b);
+            r.hi[q] = lane_pick(w[q], r.b + 1);
+        }
+    } else {
+        r.total = base[B];
+        r.b = search_base(base, B, x);
+        r.base_b = base[r.b];
+        int f = r.b;
+        while (f > 0 && base[f - 1] == r.base_b) --f;
+        r.first = f;
+#pragma unroll
+        for (int q = 0; q < NA; ++q) {
+            r.lo[q] = aux[q][r.b];
+            r.hi[q] = aux[q][r.b + 1];
+        }
+    }
+    return r;
+}
+
+// A single prompt (B = 1) has seq_off = {0, Ntot} once the prep kernel has
+// accepted the input (it raises the bad-input flag otherwise), so every
+// per-prompt table follows from Ntot without loads: `items` is base[1] (the
+// tile or slice count) and aux[q] = {0, hi[q]}.
+template <int NA>
+__device__ __forceinline__ Located<NA> one_prompt(int32_t items, const int64_t (&hi)[NA > 0 ? NA : 1]) {
+    Located<NA> r;
+    r.b = 0;
+    r.first = 0;
+    r.base_b = 0;
+    r.total = items;
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+        r.lo[q] = 0;
+        r.hi[q] = static_cast<int32_t>(hi[q]);
+    }
+    return r;
+}
+
 // ------------------------------------------------------------------ pool
 constexpr int kPoolThreads = 128;
 constexpr int kPoolMaxHalo = 64;
@@ -51,6 +142,7 @@ struct PoolArgs {
     const int32_t* seq_off;
     const int32_t* tile_base;
     const int32_t* chunk_off;
+    int64_t Ntot;
     int B, W, C, bf_n, bl_n;
     float bf_mult, bl_mult;
 };
@@ -61,15 +153,17 @@ struct PoolShared {
     float red_mn[kPoolThreads / 32], red_mx[kPoolThreads / 32];
 };
 
-// One tile by kPoolThreads threads (tid = thread index within the group).
-// Chunks never straddle tiles (C divides 128); the halo is W/2 <= 64 tokens
-// clipped to the prompt. Per-chunk sums run in token order.
+// One tile by kPoolThreads threads (tid = thread index within the group),
+// located by loc (tile_base; aux seq_off, chunk_off). Chunks never straddle
+// tiles (C divides 128); the halo is W/2 <= 64 tokens clipped to the
+// prompt. Per-chunk sums run in token order. With bad1 (single prompt, see
+// one_prompt) the window is requested before the flag is read.
 __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int tid, GroupBar g,
-                                          PoolShared& sh) {
-    const int b = search_base(a.tile_base, a.B, tile);
-    const int64_t i = tile - a.tile_base[b];
-    const int64_t start = a.seq_off[b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
+                                          PoolShared& sh, const Located<2>& loc, const int32_t* bad1) {
+    const int b = loc.b;
+    const int64_t i = tile - loc.base_b;
+    const int64_t start = loc.lo[0];
+    const int64_t n = static_cast<int64_t>(loc.hi[0]) - start;
     const int64_t t0 = i * kTileTokens, t1 = min64(n, t0 + kTileTokens);
     const int h = a.W / 2;
     const int64_t lo = max64(0, t0 - h), hi = min64(n, t1 + h);
@@ -80,6 +174,7 @@ __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int t
         const int64_t u = lo + tid + k * kPoolThreads;
         r[k] = u < hi ? __ldcg(a.imp + start + u) : 0.0f;
     }
+    if (bad1 && *bad1) return;
 #pragma unroll
     for (int k = 0; k < kWin; ++k) {
         const int64_t u = lo + tid + k * kPoolThreads;
@@ -132,7 +227,7 @@ __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int t
             sbx += bx;
             sb += bb;
         }
-        a.csum[a.chunk_off[b] + c] = make_float2(sbx, sb);
+        a.csum[loc.lo[1] + c] = make_float2(sbx, sb);
     }
     g.sync();  // the group's shared memory may be reused for the next tile
 }
@@ -162,6 +257,7 @@ struct PostArgs {
     WsHeader* hdr;
     int B, C, mode, normalize, force_bos, force_last;
     int rule, min_tok, max_keep;
+    int64_t Ntot;
     float keep_p, mass;
 };
 
@@ -174,6 +270,7 @@ struct RankShared {
     int32_t warp_cnt[kRankWarps], warp_spare[kRankWarps];
     int64_t red[kRankWarps];
     int64_t base[kSliceChunks];
+    uint8_t keepf[kSliceChunks];
 };
 
 __device__ __forceinline__ int64_t chunk_tokens(int64_t n, int C, int64_t c) { return min64(C, n - c * C); }
@@ -191,13 +288,17 @@ __device__ __forceinline__ int64_t chunk_tokens(int64_t n, int C, int64_t c) { r
 // The final chunk is forced. Writes the chunk scores, keep flags and the
 // slice's kept-token count (chunk 0 counts its BOS token when it is not
 // selected). The set equals that of the radix selection behind sp_select.
+// The slice is located by loc (slice_base; aux seq_off, chunk_off,
+// tile_base). With bad1 (single prompt, see one_prompt) the chunk sums and
+// tile extrema are requested before the flag is read.
 __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, GroupBar g,
-                                           float* cs_s, RankShared& sh) {
+                                           float* cs_s, RankShared& sh, const Located<3>& loc,
+                                           const int32_t* bad1) {
     const int lane = t & 31, warp = t >> 5;
-    const int b = search_base(a.slice_base, a.B, s);
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - a.seq_off[b];
-    const int64_t coff = a.chunk_off[b];
-    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
+    const int b = loc.b;
+    const int64_t n = static_cast<int64_t>(loc.hi[0]) - loc.lo[0];
+    const int64_t coff = loc.lo[1];
+    const int64_t nc = static_cast<int64_t>(loc.hi[1]) - coff;
     if (nc > kMaxPromptChunks) {
         // reported; the slice keeps nothing so that the gather stays in bounds
         if (t == 0) {
@@ -207,7 +308,7 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         }
         return;
     }
-    const int64_t c_lo = (s - a.slice_base[b]) * kSliceChunks;
+    const int64_t c_lo = (s - loc.base_b) * kSliceChunks;
     const int64_t c_hi = min64(nc, c_lo + kSliceChunks);
 
     // each thread's first chunk sums and its tile min / max are requested
@@ -219,11 +320,15 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         const int64_t c = t + k * kRankThreads;
         v[k] = c < nc ? __ldcg(a.csum + coff + c) : make_float2(0.0f, 0.0f);
     }
+    const int64_t p0 = loc.lo[2], p1 = loc.hi[2];
+    float2 r0 = make_float2(INFINITY, -INFINITY);
+    if (a.normalize && p0 + t < p1) r0 = __ldcg(a.rpart + p0 + t);
+    if (bad1 && *bad1) return;
     float mn = 0.0f, mx = 0.0f;
     if (a.normalize) {
-        mn = INFINITY;
-        mx = -INFINITY;
-        for (int64_t p = a.tile_base[b] + t; p < a.tile_base[b + 1]; p += kRankThreads) {
+        mn = fminf(INFINITY, r0.x);  // as the loop would take it (a NaN is dropped)
+        mx = fmaxf(-INFINITY, r0.y);
+        for (int64_t p = p0 + t + kRankThreads; p < p1; p += kRankThreads) {
             const float2 r = __ldcg(a.rpart + p);
             mn = fminf(mn, r.x);
             mx = fmaxf(mx, r.y);
@@ -376,11 +481,26 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
 // the slice by the kept tokens of all earlier slices and writes its kept
 // token indices and positions; s == S writes the batch total and the
 // offsets of prompts without tokens at the end of the batch.
-__device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int64_t S, int t, GroupBar g,
-                                             RankShared& sh) {
+// The slice is located by loc (slice_base, x = s; aux seq_off, chunk_off);
+// loc.total is the slice count S. With bad1 (single prompt, see one_prompt)
+// the slice's keep flags are requested with the counts, before the flag is
+// read.
+__device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int t, GroupBar g,
+                                             RankShared& sh, const Located<2>& loc, const int32_t* bad1) {
     const int lane = t & 31, warp = t >> 5;
+    const int64_t S = loc.total;
+    const int b = loc.b;
+    const int64_t sb = loc.base_b;
+    const int64_t start = loc.lo[0];
+    const int64_t n = static_cast<int64_t>(loc.hi[0]) - start;
+    const int64_t coff = loc.lo[1];
+    const int64_t nc = static_cast<int64_t>(loc.hi[1]) - coff;
+    uint8_t f1 = 0;
+    if (bad1 && warp == 0 && s < S && (s - sb) * kSliceChunks + lane < nc)
+        f1 = __ldcg(a.keep + coff + (s - sb) * kSliceChunks + lane);
     int64_t part = 0;
     for (int64_t i = t; i < s; i += kRankThreads) part += __ldcg(a.scount + i);
+    if (bad1 && *bad1) return;
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) sh.red[warp] = part;
     g.sync();
@@ -388,32 +508,31 @@ __device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int64
     for (int w = 0; w < kRankWarps; ++w) P += sh.red[w];
     if (s == S) {
         if (t == 0) {
-            for (int b = a.B - 1; b >= 0 && a.slice_base[b] == S; --b) a.kept_off[b] = static_cast<int32_t>(P);
+            // prompts without slices at the end of the batch (loc: the last prompt)
+            if (sb == S)
+                for (int bb = loc.first; bb < a.B; ++bb) a.kept_off[bb] = static_cast<int32_t>(P);
             a.kept_off[a.B] = static_cast<int32_t>(P);
             *a.n_kept = static_cast<int32_t>(P);
         }
         g.sync();
         return;
     }
-    const int b = search_base(a.slice_base, a.B, s);
-    if (t == 0 && s == a.slice_base[b]) {
+    if (t == 0 && s == sb) {
         // first slice of prompt b: its offset, and that of empty prompts before it
-        for (int bb = b; bb >= 0 && a.slice_base[bb] == s; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
+        for (int bb = loc.first; bb <= b; ++bb) a.kept_off[bb] = static_cast<int32_t>(P);
     }
-    const int64_t start = a.seq_off[b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
-    const int64_t coff = a.chunk_off[b];
-    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
     const bool ok = nc <= kMaxPromptChunks;  // else reported by the rank; nothing kept
-    const int64_t c_lo = (s - a.slice_base[b]) * kSliceChunks;
+    const int64_t c_lo = (s - sb) * kSliceChunks;
     // exclusive scan of the slice's per-chunk kept tokens (lane = chunk)
     if (warp == 0) {
         const int64_t c = c_lo + lane;
         int64_t cnt = 0;
+        uint8_t f = 0;
         if (ok && c < nc) {
-            const uint8_t f = __ldcg(a.keep + coff + c);
+            f = bad1 ? f1 : __ldcg(a.keep + coff + c);
             cnt = f ? chunk_tokens(n, a.C, c) : ((c == 0 && a.force_bos && n > 0) ? 1 : 0);
         }
+        sh.keepf[lane] = f;
         int64_t incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -428,7 +547,7 @@ __device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int64
             const int64_t c = c_lo + q;
             if (c >= nc) break;
             const int64_t base = sh.base[q];
-            if (__ldcg(a.keep + coff + c)) {
+            if (sh.keepf[q]) {
                 const int64_t a0 = c * a.C, a1 = min64(n, a0 + a.C);
                 for (int64_t tt = a0 + lane; tt < a1; tt += 32) {
                     a.kept_idx[base + (tt - a0)] = static_cast<int32_t>(start + tt);

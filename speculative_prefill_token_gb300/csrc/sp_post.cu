@@ -5,7 +5,7 @@
 //
 // Both kernels run one CTA per slice of kSliceChunks consecutive chunks of a
 // prompt, so a long prompt is spread over many SMs (the per-slice code is in
-// sp_phases.cuh, shared with the persistent fused kernel):
+// sp_phases.cuh):
 //
 //   rank    rebuilds every chunk score of the prompt in shared memory --
 //           min-max normalisation over the prompt ("SpecPrefill —
@@ -46,24 +46,45 @@ namespace {
 __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
     grid_dep_wait();
     grid_dep_launch();
-    if (a.hdr->bad_input) return;
     const int64_t s = blockIdx.x;
-    if (s >= a.slice_base[a.B]) return;
     extern __shared__ float cs_s[];  // the prompt's chunk scores
     __shared__ RankShared sh;
-    rank_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh);
+    if (a.B == 1) {  // rank_slice reads the flag after requesting its inputs
+        const int64_t nc = (a.Ntot + a.C - 1) / a.C;
+        const int64_t hi[3] = {a.Ntot, nc, (a.Ntot + kTileTokens - 1) / kTileTokens};
+        const Located<3> loc = one_prompt<3>(static_cast<int32_t>((nc + kSliceChunks - 1) / kSliceChunks), hi);
+        if (s >= loc.total) return;
+        rank_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, &a.hdr->bad_input);
+        return;
+    }
+    const int32_t* const aux[3] = {a.seq_off, a.chunk_off, a.tile_base};
+    const int32_t bad_v = a.hdr->bad_input;
+    const Located<3> loc = locate<3>(a.slice_base, aux, a.B, s);
+    if (bad_v) return;
+    if (s >= loc.total) return;
+    rank_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, nullptr);
 }
 
 // One CTA per slice, plus one past the last slice for the totals.
 __global__ void __launch_bounds__(kRankThreads) gather_kernel(const PostArgs a) {
     grid_dep_wait();
     grid_dep_launch();
-    if (a.hdr->bad_input) return;
     __shared__ RankShared sh;
-    const int64_t S = a.slice_base[a.B];
     const int64_t s = blockIdx.x;
-    if (s > S) return;
-    gather_slice(a, s, S, threadIdx.x, GroupBar{1, kRankThreads}, sh);
+    if (a.B == 1) {  // gather_slice reads the flag after requesting its inputs
+        const int64_t nc = (a.Ntot + a.C - 1) / a.C;
+        const int64_t hi[2] = {a.Ntot, nc};
+        const Located<2> loc = one_prompt<2>(static_cast<int32_t>((nc + kSliceChunks - 1) / kSliceChunks), hi);
+        if (s > loc.total) return;
+        gather_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, sh, loc, &a.hdr->bad_input);
+        return;
+    }
+    const int32_t* const aux[2] = {a.seq_off, a.chunk_off};
+    const int32_t bad_v = a.hdr->bad_input;
+    const Located<2> loc = locate<2>(a.slice_base, aux, a.B, s);
+    if (bad_v) return;
+    if (s > loc.total) return;
+    gather_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, sh, loc, nullptr);
 }
 
 // Listing rule: the final kept count of prompt b from its count before the
@@ -233,6 +254,7 @@ PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, f
     a.ucount = ws_ptr<int32_t>(ws, pl.o_ucount);
     a.hdr = ws_ptr<WsHeader>(ws, 0);
     a.B = pl.B;
+    a.Ntot = pl.Ntot;
     a.C = pl.C;
     a.mode = p->mode;
     a.normalize = p->normalize;

@@ -168,26 +168,47 @@ __global__ void __launch_bounds__(kReduceThreads, 4) reduce_kernel(
 #pragma unroll
     for (int u = 0; u < kReduceSlabBatch; ++u)
         if (u < nslab) v[u] = __ldcs(src + u * slab_stride);
-    if (*bad) return;
-    if (tile >= tile_base[B]) return;
     extern __shared__ float sm[];
     const int q0 = sub * TOK / 32, nq = (TOK + 31) / 32;  // warp quarters of the CTA's tokens
     float* off_s = sm;                       // [nq][nslab][Rs]: M - lse2
     float* ms = off_s + nq * nslab * Rs;     // [TOK][Rs + 1]
-    const int b = search_base(tile_base, B, tile);
-    const int64_t i = tile - tile_base[b];
-    const int64_t start = seq_off[b];
-    const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - start;
+    // A single prompt (B = 1) has seq_off = {0, Ntot} once the prep kernel
+    // has accepted the input: its offsets come from Ntot and the table is
+    // requested before the flag is read.
+    const auto fill_table = [&](int b) {
+        for (int idx = threadIdx.x; idx < nq * nslab * Rs; idx += kReduceThreads) {
+            const int qq = idx / (nslab * Rs), rem = idx - qq * nslab * Rs;
+            const int s = rem / Rs, r = rem - s * Rs;
+            off_s[idx] = lmax[((static_cast<int64_t>(s) * tiles_max + tile) * 4 + q0 + qq) * Rs + r] -
+                         lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
+        }
+    };
+    const bool one = B == 1;
+    int b = 0;
+    int64_t i, start, n;
+    if (one) {
+        if (tile >= (Ntot + kTileTokens - 1) / kTileTokens) return;
+        fill_table(0);
+        if (*bad) return;
+        i = tile;
+        start = 0;
+        n = Ntot;
+    } else {
+        const int32_t* const aux[1] = {seq_off};
+        const int32_t bad_v = *bad;
+        const Located<1> loc = locate<1>(tile_base, aux, B, tile);
+        if (bad_v) return;
+        if (tile >= loc.total) return;
+        b = loc.b;
+        i = tile - loc.base_b;
+        start = loc.lo[0];
+        n = static_cast<int64_t>(loc.hi[0]) - start;
+    }
     const int64_t first = i * kTileTokens + static_cast<int64_t>(sub) * TOK;  // within the prompt
     const int nvalid = static_cast<int>(min64(TOK, n - first));
     if (nvalid <= 0) return;
     const bool act = tq < nvalid;
-    for (int idx = threadIdx.x; idx < nq * nslab * Rs; idx += kReduceThreads) {
-        const int qq = idx / (nslab * Rs), rem = idx - qq * nslab * Rs;
-        const int s = rem / Rs, r = rem - s * Rs;
-        off_s[idx] = lmax[((static_cast<int64_t>(s) * tiles_max + tile) * 4 + q0 + qq) * Rs + r] -
-                     lse2[(static_cast<int64_t>(s) * B + b) * Rs + r];
-    }
+    if (!one) fill_table(b);
     __syncthreads();
     const float* ot = off_s + (tq / 32) * nslab * Rs + 8 * c;  // this token's quarter
     float m[8];
@@ -238,11 +259,21 @@ __global__ void __launch_bounds__(kReduceThreads, 4) reduce_kernel(
 __global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(const PoolArgs a, const int32_t* bad) {
     grid_dep_wait();
     grid_dep_launch();
-    if (*bad) return;
     const int64_t tile = blockIdx.x;
-    if (tile >= a.tile_base[a.B]) return;
     __shared__ PoolShared sh;
-    pool_tile(a, tile, threadIdx.x, GroupBar{1, kPoolThreads}, sh);
+    if (a.B == 1) {  // pool_tile reads the flag after requesting the window
+        const int64_t hi[2] = {a.Ntot, (a.Ntot + a.C - 1) / a.C};
+        const Located<2> loc = one_prompt<2>(static_cast<int32_t>((a.Ntot + kTileTokens - 1) / kTileTokens), hi);
+        if (tile >= loc.total) return;
+        pool_tile(a, tile, threadIdx.x, GroupBar{1, kPoolThreads}, sh, loc, bad);
+        return;
+    }
+    const int32_t* const aux[2] = {a.seq_off, a.chunk_off};
+    const int32_t bad_v = *bad;
+    const Located<2> loc = locate<2>(a.tile_base, aux, a.B, tile);
+    if (bad_v) return;
+    if (tile >= loc.total) return;
+    pool_tile(a, tile, threadIdx.x, GroupBar{1, kPoolThreads}, sh, loc, nullptr);
 }
 
 // ----------------------------------------------------------------- pool
@@ -581,6 +612,7 @@ PoolArgs pool_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, c
     a.seq_off = seq_off;
     a.tile_base = ws_ptr<int32_t>(ws, pl.o_tile_base);
     a.chunk_off = ws_ptr<int32_t>(ws, pl.o_chunk_off);
+    a.Ntot = pl.Ntot;
     a.B = pl.B;
     a.W = p->pool_w;
     a.C = pl.C;

@@ -227,6 +227,27 @@ def test_ragged_batch_with_empty_and_tiny_prompts(cuda_lib):
     assert got["kept_off"][4] == got["kept_off"][5]
 
 
+@pytest.mark.parametrize("n_prompts", [40, 63, 64, 150])
+def test_many_prompt_batches_locate_every_prompt(cuda_lib, n_prompts):
+    """The post kernels find each tile's or slice's prompt with a warp ballot
+    over the offset tables for batches of fewer than 64 prompts and with a
+    binary search above; empty prompts at the start, in the middle and at the
+    end must get the offsets of their neighbours and keep nothing."""
+    rng = np.random.default_rng(960 + n_prompts)
+    lengths = rng.integers(1, 400, n_prompts)
+    lengths[[0, n_prompts // 2, n_prompts // 2 + 1, n_prompts - 2, n_prompts - 1]] = 0
+    lengths[3] = 1
+    q, k, off = random_case(970 + n_prompts, lengths.tolist(), 1, 4, 2, 64, 2, q_gain=2.0)
+    kw = dict(BASE, mode="fixed", keep_p=0.3)
+    got, _ = _run(cuda_lib, q, k, off, kw)
+    ref = oracle.run(q, k, off, **kw)
+    _check_scores(got, ref)
+    _check_t1(got, off, kw)
+    _check_t2(got, ref, off, kw)
+    for b in np.flatnonzero(lengths == 0):
+        assert got["kept_off"][b] == got["kept_off"][b + 1], b
+
+
 def test_invalid_offsets_set_device_status(cuda_lib):
     import torch
     sp = cuda_lib
@@ -241,6 +262,30 @@ def test_invalid_offsets_set_device_status(cuda_lib):
     out = sp.specprefill_score(qd, kd, torch.from_numpy(off).cuda(), p, ws=ws)
     assert sp.device_status(ws) == 0
     assert int(out.n_kept.item()) > 0
+
+
+def test_invalid_single_prompt_offsets_set_device_status(cuda_lib):
+    """With one prompt the kernels after the prep take every offset from
+    n_tokens_total and request their data before reading the prep kernel's
+    verdict: offsets that do not span [0, Ntot) must still end in
+    SP_ERR_DEVICE, and the next valid call on the same workspace must equal
+    a call on a fresh one."""
+    import torch
+    sp = cuda_lib
+    q, k, off = random_case(903, [300], 2, 4, 2, 64, 2, q_gain=2.0)
+    qd, kd, _ = gh.to_device(type("I", (), {"q": q, "k": k, "seq_off": off})())
+    p = sp.SelectionParams(**dict(BASE, mode="fixed", keep_p=0.3))
+    shape = sp.shape_of(qd, kd)
+    ws = sp.make_workspace(shape, p, poison=True)
+    for bad in ([0, 290], [5, 300], [0, 100000], [-1, 300]):
+        sp.specprefill_score(qd, kd, torch.tensor(bad, dtype=torch.int32, device="cuda"), p, ws=ws)
+        assert sp.device_status(ws) == 6, bad
+    od = torch.from_numpy(off).cuda()
+    got = gh.out_to_numpy(sp.specprefill_score(qd, kd, od, p, ws=ws))
+    assert sp.device_status(ws) == 0
+    fresh = gh.out_to_numpy(sp.specprefill_score(qd, kd, od, p))
+    for key in fresh:
+        assert np.array_equal(got[key], fresh[key]), key
 
 
 def test_bounded_wait_timeout_is_reported_and_recoverable(cuda_lib):
