@@ -134,18 +134,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 
 // --------------------------------------------------------------- reduce
 // Token importance from the wave's quantised logits. One CTA covers TOK =
-// 2048 / Rs tokens of one tile (Rs / 8 threads per token, 8 rows each):
+// 1024 / Rs tokens of one tile (Rs / 8 threads per token, 8 rows each):
 // every thread loads its eight 16-bit values of every slab (16 bytes,
 // coalesced) and keeps the max over slabs of
 // y - lse2 = (M - lse2) - q / kLogitQuant, the log2 softmax probability,
 // with M - lse2 taken from a per-CTA table [warp quarter][slab][row]. One
 // thread per token then takes the max over the G heads of each lookahead
 // step, combines it with earlier waves, and (last wave) writes
-// imp[t] = (1/L) sum_l exp2(max over layers, heads).
-constexpr int kReduceThreads = 256;
+// imp[t] = (1/L) sum_l exp2(max over layers, heads). Small CTAs (eight per
+// SM) spread a wave over every SM that the logits kernel frees.
+constexpr int kReduceThreads = 128;
 constexpr int kReduceSlabBatch = 4;
 
-__global__ void __launch_bounds__(kReduceThreads, 4) reduce_kernel(
+__global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
     const uint16_t* logits, const float* lmax, const float* lse2, const int32_t* seq_off,
     const int32_t* tile_base, float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab,
     int64_t Ntot, int64_t rows_per_slab, int64_t tiles_max, int first_wave, int last_wave,
