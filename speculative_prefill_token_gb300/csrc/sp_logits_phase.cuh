@@ -110,8 +110,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int d_blocks, uint
     off += 8;
     s.stats = off;
     off += 2u * 4u * 64u * 8u;  // [warpgroup][warp][row] float2
-    s.tile_base = off;          // [kLocalPrompts + 1] int32, then per-warp sums
-    off += 4u * (kLocalPrompts + 1 + kThreads / 32);
+    s.tile_base = off;          // [kLocalPrompts + 1] int32, per-warp sums, then seq_off
+    off += 4u * (2 * (kLocalPrompts + 1) + kThreads / 32);
     s.total = off;
     return s;
 }
@@ -134,6 +134,7 @@ struct ItemCursor {
     int start, n;
 
     const int32_t* tb;  // the batch's tile offsets (the CTA's own copy or the prep kernel's)
+    const int32_t* so;  // the batch's token offsets (the CTA's own copy or seq_off)
 
     __device__ __forceinline__ void set(const TcArgs& a, int64_t w, int64_t T) {
         it.slab = static_cast<int>(w / T);
@@ -141,8 +142,8 @@ struct ItemCursor {
         it.b = search_base(tb, a.B, it.tile);
         base_b = tb[it.b];
         next_b = tb[it.b + 1];
-        start = a.seq_off[it.b];
-        n = a.seq_off[it.b + 1] - start;
+        start = so[it.b];
+        n = so[it.b + 1] - start;
         place();
     }
     __device__ __forceinline__ void place() {
@@ -253,9 +254,11 @@ __device__ __forceinline__ void logits_setup(LogitsCtx& c, const TcArgs& a, cons
 
 // Tile offsets of the batch computed by this CTA (all kThreads threads,
 // B <= kLocalPrompts) from seq_off: tb[b] = sum over earlier prompts of
-// ceil(n / 128), tb[B] the total; returns the tile count, 0 when seq_off is
-// not a valid packing of Ntot tokens (or, for a block-paged key source, a
-// prompt has more blocks than its table row), as the prep kernel decides.
+// ceil(n / 128), tb[B] the total, and a copy of seq_off after the per-warp
+// sums (tb + kLocalPrompts + 1 + kThreads / 32); returns the tile count, 0
+// when seq_off is not a valid packing of Ntot tokens (or, for a block-paged
+// key source, a prompt has more blocks than its table row), as the prep
+// kernel decides.
 // The prompt bounds of thread t < B, requested (by logits_offsets_request)
 // before the CTA's setup so that their latency overlaps it.
 struct PromptBounds {
@@ -265,7 +268,8 @@ struct PromptBounds {
 __device__ __forceinline__ PromptBounds logits_offsets_request(const TcArgs& a) {
     PromptBounds pb{0, 0};
     const int t = threadIdx.x;
-    if (a.B <= kLocalPrompts && t < a.B) {
+    // (a single unpaged prompt takes its bounds from Ntot: see logits_start)
+    if (a.B <= kLocalPrompts && t < a.B && !(a.B == 1 && a.kv_mode != 2)) {
         pb.lo = a.seq_off[t];
         pb.hi = a.seq_off[t + 1];
     }
@@ -294,8 +298,15 @@ __device__ __forceinline__ int64_t local_tile_base(const TcArgs& a, PromptBounds
     ok = __syncthreads_and(ok);
     int32_t before = 0;
     for (int w = 0; w < warp; ++w) before += warp_sum[w];
-    if (t < a.B) tb[t] = before + incl - tiles;
-    if (t == a.B - 1) tb[a.B] = before + incl;
+    int32_t* so = warp_sum + kThreads / 32;  // the CTA's copy of seq_off
+    if (t < a.B) {
+        tb[t] = before + incl - tiles;
+        so[t] = pb.lo;
+    }
+    if (t == a.B - 1) {
+        tb[a.B] = before + incl;
+        so[a.B] = pb.hi;
+    }
     __syncthreads();
     const int64_t T = ok ? static_cast<int64_t>(tb[a.B]) : 0;
     return T < a.tiles_max ? T : a.tiles_max;
@@ -344,7 +355,7 @@ __device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur,
 // the table's latency overlaps the copies of the items before it (also at
 // the start, where the ring is still empty).
 __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& a, const int32_t* tb,
-                                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
+                                              const int32_t* so, const CUtensorMap* tmap_k, const CUtensorMap* tmap_q,
                                               int64_t T, int64_t w_begin, int64_t w_end, int lane) {
     constexpr unsigned kFull = 0xffffffffu;
     const uint64_t pol = policy_evict_first();
@@ -360,6 +371,7 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
     // `ahead` is the cursor of the last item looked up
     ItemCursor cur, ahead;
     cur.tb = tb;
+    cur.so = so;
     int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
     if (w_begin < w_end) {
         cur.set(a, w_begin, T);
@@ -452,7 +464,8 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
 // On return every TMA store of this CTA has completed; the CTA is not
 // synchronised.
 template <int NH>
-__device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a, const int32_t* tb, int epi_wait,
+__device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a, const int32_t* tb,
+                                             const int32_t* so, int epi_wait,
                                              const CUtensorMap* tmap_k,
                                              const CUtensorMap* tmap_q, const CUtensorMap* tmap_s,
                                              int64_t T, int64_t C, int64_t cta) {
@@ -471,7 +484,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
     const int64_t w_end = split_start(W, C, cta + 1);
 
     if (warp == kProducerWarp && a.kv_mode == 2) {
-        produce_paged(c, a, tb, tmap_k, tmap_q, T, w_begin, w_end, lane);
+        produce_paged(c, a, tb, so, tmap_k, tmap_q, T, w_begin, w_end, lane);
     } else if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
@@ -485,6 +498,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             bool ok = true;
             ItemCursor cur;
             cur.tb = tb;
+            cur.so = so;
             for (int64_t w = w_begin; w < w_end && ok; ++w) {
                 if (w == w_begin) cur.set(a, w, T);
                 else cur.next(a, w, T);
@@ -545,6 +559,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             bool any_mma = false;
             ItemCursor cur;
             cur.tb = tb;
+            cur.so = so;
             for (int64_t w = w_begin; w < w_end && ok; ++w, ++j) {
                 if (w == w_begin) cur.set(a, w, T);
                 else cur.next(a, w, T);
@@ -624,6 +639,7 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
         int64_t j = 0;
         ItemCursor cur;
         cur.tb = tb;
+        cur.so = so;
         for (int64_t w = w_begin; w < w_end; ++w, ++j) {
             if (w == w_begin) cur.set(a, w, T);
             else cur.next(a, w, T);

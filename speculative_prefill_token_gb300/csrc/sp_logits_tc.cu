@@ -23,18 +23,37 @@ namespace {
 // and only the epilogue waits for the prep kernel's counters; larger
 // batches wait for the prep kernel's offsets. The dependent kernel may
 // launch from here on.
+// A single prompt with keys that are not block-paged takes its offsets from
+// Ntot ({0, Ntot}; the prep kernel rejects anything else and the scores of
+// such a call are never used), so the producer starts right after the
+// setup; every key read stays inside the key map's Ntot rows.
 __device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, const TcArgs& a, PromptBounds pb,
-                                                const int32_t** tb, int* epi_wait) {
+                                                const int32_t** tb, const int32_t** so, int* epi_wait) {
     int64_t T;
     if (a.B <= kLocalPrompts) {
         int32_t* own = reinterpret_cast<int32_t*>(c.smem + c.L.tile_base);
-        T = local_tile_base(a, pb, own);
+        int32_t* own_so = own + kLocalPrompts + 1 + kThreads / 32;
+        if (a.B == 1 && a.kv_mode != 2) {
+            T = (a.Ntot + kTileTokens - 1) / kTileTokens;
+            if (threadIdx.x == 0) {
+                own[0] = 0;
+                own[1] = static_cast<int32_t>(T);
+                own_so[0] = 0;
+                own_so[1] = static_cast<int32_t>(a.Ntot);
+            }
+            __syncthreads();
+            if (T > a.tiles_max) T = a.tiles_max;
+        } else {
+            T = local_tile_base(a, pb, own);
+        }
         *tb = own;
+        *so = own_so;
         *epi_wait = 1;
     } else {
         grid_dep_wait();
         T = *a.bad ? 0 : a.tile_base[a.B];  // invalid offsets: no work, normal teardown
         *tb = a.tile_base;
+        *so = a.seq_off;
         *epi_wait = 0;
     }
     grid_dep_launch();
@@ -51,9 +70,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PromptBounds pb = logits_offsets_request(a);
     logits_setup(c, a, &tmap_k, &tmap_q, &tmap_s);
     const int32_t* tb;
+    const int32_t* so;
     int epi_wait;
-    const int64_t T = logits_start(c, a, pb, &tb, &epi_wait);
-    logits_phase<NH>(c, a, tb, epi_wait, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    const int64_t T = logits_start(c, a, pb, &tb, &so, &epi_wait);
+    logits_phase<NH>(c, a, tb, so, epi_wait, &tmap_k, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
@@ -73,9 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PromptBounds pb = logits_offsets_request(a);
     logits_setup(c, a, kmaps.m, &tmap_q, &tmap_s);
     const int32_t* tb;
+    const int32_t* so;
     int epi_wait;
-    const int64_t T = logits_start(c, a, pb, &tb, &epi_wait);
-    logits_phase<NH>(c, a, tb, epi_wait, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
+    const int64_t T = logits_start(c, a, pb, &tb, &so, &epi_wait);
+    logits_phase<NH>(c, a, tb, so, epi_wait, kmaps.m, &tmap_q, &tmap_s, T, gridDim.x, blockIdx.x);
     logits_teardown(c, a);
 }
 
