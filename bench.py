@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "b036350a53869fa28f427f4427405225318c61e9", "bytes_per_launch": 201974400}
+TRAFFIC = {"source_sha1": "8e92c2ef92294d5e22e1c3e1be83f0a2179b7c2f", "bytes_per_launch": 202150528}
 
 
 def parse():
