@@ -256,7 +256,7 @@ __device__ __forceinline__ void segment_done(const int32_t* tile_base, int B, in
 
 // Chunk score = mean over the chunk of boost(t) * normalise(x(t)). The
 // min-max normalisation is affine, so with S_bx = sum boost*x and
-// S_b = sum boost (token order) the mean is
+// S_b = sum boost (warp_chunk_sums) the mean is
 // (S_bx - min * S_b) / (max - min) / count; a constant prompt (max == min)
 // normalises to all ones, giving S_b / count. Clamped at zero (rounding of
 // the difference of two nearly equal sums).

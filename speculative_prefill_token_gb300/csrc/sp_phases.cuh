@@ -130,6 +130,41 @@ __device__ __forceinline__ Located<NA> one_prompt(int32_t items, const int64_t (
     return r;
 }
 
+// Sums over the chunk's tokens [a0, a1) (prompt positions; the pooled
+// score of token t at xs[t - x0]) of boost(t) * x(t) and of boost(t), by
+// one warp in a fixed order: lane k adds tokens a0 + k, a0 + k + 32, ...
+// in turn, then lane k + o is added into lane k for o = 1, 2, 4, 8, 16.
+// The sums are in lane 0. boost(t) = bf_mult for t < bf_n, times bl_mult
+// for t >= n - bl_n.
+__device__ __forceinline__ float2 warp_chunk_sums(const float* xs, int64_t x0, int64_t a0, int64_t a1,
+                                                  int64_t n, int bf_n, float bf_mult, int bl_n,
+                                                  float bl_mult, int lane) {
+    float sbx = 0.0f, sb = 0.0f;
+    for (int64_t t = a0 + lane; t < a1; t += 32) {
+        float bx = xs[t - x0], bb = 1.0f;
+        if (t < bf_n) {
+            bx *= bf_mult;
+            bb *= bf_mult;
+        }
+        if (t >= n - bl_n) {
+            bx *= bl_mult;
+            bb *= bl_mult;
+        }
+        sbx += bx;
+        sb += bb;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float ux = __shfl_down_sync(0xffffffffu, sbx, o);
+        const float ub = __shfl_down_sync(0xffffffffu, sb, o);
+        if (lane + o < 32) {
+            sbx += ux;
+            sb += ub;
+        }
+    }
+    return make_float2(sbx, sb);
+}
+
 // ------------------------------------------------------------------ pool
 constexpr int kPoolThreads = 128;
 constexpr int kPoolMaxHalo = 64;
@@ -156,7 +191,7 @@ struct PoolShared {
 // One tile by kPoolThreads threads (tid = thread index within the group),
 // located by loc (tile_base; aux seq_off, chunk_off). Chunks never straddle
 // tiles (C divides 128); the halo is W/2 <= 64 tokens clipped to the
-// prompt. Per-chunk sums run in token order. With bad1 (single prompt, see
+// prompt. Per-chunk sums: warp_chunk_sums. With bad1 (single prompt, see
 // one_prompt) the window is requested before the flag is read.
 __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int tid, GroupBar g,
                                           PoolShared& sh, const Located<2>& loc, const int32_t* bad1) {
@@ -210,24 +245,12 @@ __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int t
         }
         a.rpart[tile] = make_float2(mn, mx);
     }
+    // one warp per chunk (the staged chunk kernel sums in the same order)
     const int64_t c_lo = t0 / a.C, c_hi = (t1 + a.C - 1) / a.C;
-    for (int64_t c = c_lo + tid; c < c_hi; c += kPoolThreads) {
+    for (int64_t c = c_lo + warp; c < c_hi; c += kPoolThreads / 32) {
         const int64_t a0 = c * a.C, a1 = min64(t1, a0 + a.C);
-        float sbx = 0.0f, sb = 0.0f;
-        for (int64_t t = a0; t < a1; ++t) {
-            float bx = sh.xs[t - t0], bb = 1.0f;
-            if (t < a.bf_n) {
-                bx *= a.bf_mult;
-                bb *= a.bf_mult;
-            }
-            if (t >= n - a.bl_n) {
-                bx *= a.bl_mult;
-                bb *= a.bl_mult;
-            }
-            sbx += bx;
-            sb += bb;
-        }
-        a.csum[loc.lo[1] + c] = make_float2(sbx, sb);
+        const float2 r = warp_chunk_sums(sh.xs, t0, a0, a1, n, a.bf_n, a.bf_mult, a.bl_n, a.bl_mult, lane);
+        if (lane == 0) a.csum[loc.lo[1] + c] = r;
     }
     g.sync();  // the group's shared memory may be reused for the next tile
 }
@@ -262,11 +285,8 @@ struct PostArgs {
 };
 
 struct RankShared {
-    float red_mn[kRankWarps], red_mx[kRankWarps];
+    float red_mn[kRankWarps], red_mx[kRankWarps], red_sm[kRankWarps];
     unsigned long long red_u[kRankWarps];
-    float mn, mx;
-    unsigned long long need;
-    int all, S;
     int32_t warp_cnt[kRankWarps], warp_spare[kRankWarps];
     int64_t red[kRankWarps];
     int64_t base[kSliceChunks];
@@ -342,17 +362,13 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
             sh.red_mx[warp] = mx;
         }
         g.sync();
-        if (t == 0) {
-            for (int w = 1; w < kRankWarps; ++w) {
-                mn = fminf(mn, sh.red_mn[w]);
-                mx = fmaxf(mx, sh.red_mx[w]);
-            }
-            sh.mn = mn;
-            sh.mx = mx;
+        // every thread combines the warps' values in the same order
+        mn = sh.red_mn[0];
+        mx = sh.red_mx[0];
+        for (int w = 1; w < kRankWarps; ++w) {
+            mn = fminf(mn, sh.red_mn[w]);
+            mx = fmaxf(mx, sh.red_mx[w]);
         }
-        g.sync();
-        mn = sh.mn;
-        mx = sh.mx;
     }
     float smax = 0.0f;
     for (int64_t c0 = t;; c0 += kRankThreads * kPre) {
@@ -378,40 +394,33 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
     const bool listing = a.rule == SP_RULE_LISTING;
     if (is_mass) {
         for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-        if (lane == 0) sh.red_mx[warp] = smax;
+        if (lane == 0) sh.red_sm[warp] = smax;
     }
     g.sync();  // cs_s complete (and the per-warp maxima)
+    // every thread derives the scale, the threshold and the keep-all flag
+    // itself from the same shared values
+    uint64_t need = 0;
+    bool all = false;
+    int S = 0;
     if (is_mass) {
-        if (t == 0) {
-            float m = 0.0f;
-            for (int w = 0; w < kRankWarps; ++w) m = fmaxf(m, sh.red_mx[w]);
-            sh.S = mass_scale(nc, m);
-        }
-        g.sync();
-        const int S = sh.S;
+        float m = 0.0f;
+        for (int w = 0; w < kRankWarps; ++w) m = fmaxf(m, sh.red_sm[w]);
+        S = mass_scale(nc, m);
         uint64_t part = 0;
         for (int64_t c = t; c < nc; c += kRankThreads) part += fixed_point(cs_s[c], S);
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) sh.red_u[warp] = part;
         g.sync();
-        if (t == 0) {
-            unsigned long long tot = 0;
-            for (int w = 0; w < kRankWarps; ++w) tot += sh.red_u[w];
-            sh.all = tot == 0 ? 1 : 0;
-            sh.need = mass_threshold(tot, a.mass);
-        }
-    } else if (t == 0) {
-        sh.need = listing ? listing_keep_count(nc, a.keep_p) : fixed_keep_count(nc, a.keep_p);
-        sh.all = 0;
+        unsigned long long tot = 0;
+        for (int w = 0; w < kRankWarps; ++w) tot += sh.red_u[w];
+        all = tot == 0;
+        need = mass_threshold(tot, a.mass);
+    } else {
+        need = listing ? listing_keep_count(nc, a.keep_p) : fixed_keep_count(nc, a.keep_p);
     }
     // the listing keeps every token when p >= 1 (fixed mode) or the prompt
     // is no longer than its smallest kept count
-    if (listing && t == 0 && ((!is_mass && a.keep_p >= 1.0f) || n <= listing_eff_min(n, a.min_tok)))
-        sh.all = 1;
-    g.sync();
-    const uint64_t need = sh.need;
-    const bool all = sh.all != 0;
-    const int S = is_mass ? sh.S : 0;
+    if (listing && ((!is_mass && a.keep_p >= 1.0f) || n <= listing_eff_min(n, a.min_tok))) all = true;
 
     // warp w ranks chunks c_lo + w + kRankWarps * q of the slice: the count
     // (fixed) or fixed-point mass (mass mode) of the chunks ordered before

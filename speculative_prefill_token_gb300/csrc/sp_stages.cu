@@ -380,24 +380,13 @@ __global__ void __launch_bounds__(256) chunk_kernel(const float* tok, const floa
     const float mn = normalize ? s_mn : 0.0f, mx = normalize ? s_mx : 0.0f;
     for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) ys[t - t0] = tok[start + t];
     __syncthreads();
+    // one warp per chunk, in the order of the fused path's pool kernel
     const int64_t c0 = t0 / C, c1 = (t1 + C - 1) / C;
-    for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t c = c0 + warp; c < c1; c += blockDim.x >> 5) {
         const int64_t a0 = c * C, a1 = min64(t1, a0 + C);
-        float sbx = 0.0f, sb = 0.0f;
-        for (int64_t t = a0; t < a1; ++t) {
-            float bx = ys[t - t0], bb = 1.0f;
-            if (t < bf_n) {
-                bx *= bf_mult;
-                bb *= bf_mult;
-            }
-            if (t >= n - bl_n) {
-                bx *= bl_mult;
-                bb *= bl_mult;
-            }
-            sbx += bx;
-            sb += bb;
-        }
-        chunk_score[chunk_off[b] + c] = chunk_score_from_sums(sbx, sb, mn, mx, normalize, a1 - a0);
+        const float2 r = warp_chunk_sums(ys, t0, a0, a1, n, bf_n, bf_mult, bl_n, bl_mult, lane);
+        if (lane == 0) chunk_score[chunk_off[b] + c] = chunk_score_from_sums(r.x, r.y, mn, mx, normalize, a1 - a0);
     }
 }
 
