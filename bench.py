@@ -48,13 +48,13 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "8e92c2ef92294d5e22e1c3e1be83f0a2179b7c2f", "bytes_per_launch": 202150528}
+TRAFFIC = {"source_sha1": "27cb8d70f739bfa73e2cd9ae87eb7aa76afcd2b1", "bytes_per_launch": 202046336}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -159,7 +159,7 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(1.0)  # nvidia-smi's start (NVML initialisation) stays out of the timed region
         return self
 
     def __exit__(self, *exc):
