@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "27cb8d70f739bfa73e2cd9ae87eb7aa76afcd2b1", "bytes_per_launch": 202046336}
+TRAFFIC = {"source_sha1": "9da68b7390c426b7197489032a18f1d471ac0e05", "bytes_per_launch": 202160640}
 
 
 def parse():

@@ -30,9 +30,22 @@ constexpr float kLogitQuant = 2048.0f;
 constexpr float kLogitQuantInv = 1.0f / 2048.0f;
 constexpr uint32_t kLogitQuantMax = 65535u;
 
+// Rounds to nearest (ties to even) on the floating-point adder: for
+// 0 <= c <= 65535, c + 1.5 * 2^23 has a unit in the last place of 1, so its
+// low mantissa bits are the rounded integer. Negative differences give 0,
+// NaN and differences from kLogitQuantMax up give kLogitQuantMax.
 __device__ __forceinline__ uint32_t quant_logit(float M, float y) {
     const float d = (M - y) * kLogitQuant;  // >= 0 for the tokens that are read back
-    return d < static_cast<float>(kLogitQuantMax) ? __float2uint_rn(d) : kLogitQuantMax;
+    const float c = d < static_cast<float>(kLogitQuantMax) ? fmaxf(d, 0.0f) : static_cast<float>(kLogitQuantMax);
+    return __float_as_uint(c + 12582912.0f) - 0x4B400000u;
+}
+
+// 2^x by the PTX approximation instruction, results below 2^-126 flushed
+// to zero (the softmax partial sums it feeds are at least 1).
+__device__ __forceinline__ float exp2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Butterfly reduction of 32 rows held by every lane (v[r] = row r of this

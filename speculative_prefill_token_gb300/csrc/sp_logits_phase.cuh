@@ -698,17 +698,27 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             // the quarter's softmax partial
             if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
             asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+            // the warp's row maxima (lane r: row hh * 32 + r) to every lane
+            // through the warp's part of the statistics scratch
+            float* msm = reinterpret_cast<float*>(st_sm + qw * 64);
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) msm[hh * 32 + lane] = m_own[hh];
+            __syncwarp();
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh) {
                 uint32_t pk[16];
+                const float4* m4 = reinterpret_cast<const float4*>(msm + hh * 32);
 #pragma unroll
-                for (int r = 0; r < 32; r += 2) {
-                    const float M0 = __shfl_sync(0xffffffffu, m_own[hh], r);
-                    const float M1 = __shfl_sync(0xffffffffu, m_own[hh], r + 1);
-                    const float y0 = v[hh][r] * a.scale2, y1 = v[hh][r + 1] * a.scale2;
-                    pk[r / 2] = quant_logit(M0, y0) | (quant_logit(M1, y1) << 16);
-                    v[hh][r] = valid ? exp2f(y0 - M0) : 0.0f;
-                    v[hh][r + 1] = valid ? exp2f(y1 - M1) : 0.0f;
+                for (int r = 0; r < 32; r += 4) {
+                    const float4 M = m4[r / 4];
+                    const float Mr[4] = {M.x, M.y, M.z, M.w};
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2) {
+                        const float y0 = v[hh][r + u] * a.scale2, y1 = v[hh][r + u + 1] * a.scale2;
+                        pk[(r + u) / 2] = quant_logit(Mr[u], y0) | (quant_logit(Mr[u + 1], y1) << 16);
+                        v[hh][r + u] = valid ? exp2_ftz(y0 - Mr[u]) : 0.0f;
+                        v[hh][r + u + 1] = valid ? exp2_ftz(y1 - Mr[u + 1]) : 0.0f;
+                    }
                 }
                 uint4* row = reinterpret_cast<uint4*>(out_buf + hh * kStageOutBytes + tl * 64);
 #pragma unroll
