@@ -40,6 +40,14 @@ __device__ __forceinline__ uint32_t quant_logit(float M, float y) {
     return __float_as_uint(c + 12582912.0f) - 0x4B400000u;
 }
 
+// The 16-bit code of a non-negative distance d = 2^11 (M - y) computed by
+// the caller: round to nearest on the adder, NaN and d >= kLogitQuantMax
+// give kLogitQuantMax (a negative d gives unspecified low bits).
+__device__ __forceinline__ uint32_t quant_distance(float d) {
+    const float c = fminf(d, static_cast<float>(kLogitQuantMax));
+    return __float_as_uint(c + 12582912.0f) - 0x4B400000u;
+}
+
 // 2^x by the PTX approximation instruction, results below 2^-126 flushed
 // to zero (the softmax partial sums it feeds are at least 1).
 __device__ __forceinline__ float exp2_ftz(float x) {

@@ -676,13 +676,15 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                 for (int r = 0; r < 32; ++r)  // columns past the MMA width hold no result
                     if (hh * 32 + r >= a.Nmma) v[hh][r] = 0.0f;
             const bool valid = tl < it.nvalid;
-            // row maxima M of the scaled logits over the warp quarter's valid tokens
+            // row maxima M of the scaled logits over the warp quarter's valid
+            // tokens (rounding is monotonic, so scaling the maximum of the
+            // raw dot products gives the maximum of the scaled ones)
             float m_own[NH];
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh) {
 #pragma unroll
-                for (int r = 0; r < 32; ++r) v[hh][r] = valid ? v[hh][r] * a.scale2 : -INFINITY;
-                m_own[hh] = warp_rows_reduce<true>(v[hh]);
+                for (int r = 0; r < 32; ++r) v[hh][r] = valid ? v[hh][r] : -INFINITY;
+                m_own[hh] = warp_rows_reduce<true>(v[hh]) * a.scale2;
                 if (hh * 32 + lane < a.Rs)
                     a.lmax[((static_cast<int64_t>(it.slab) * a.tiles_max + it.tile) * 4 + qw) * a.Rs + hh * 32 +
                            lane] = m_own[hh];
@@ -698,12 +700,16 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
             // the quarter's softmax partial
             if (qw == 0 && lane == 0 && stores) bulk_wait_read0();
             asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
-            // the warp's row maxima (lane r: row hh * 32 + r) to every lane
-            // through the warp's part of the statistics scratch
+            // the warp's row maxima in quantiser units, 2^11 M (lane r: row
+            // hh * 32 + r), to every lane through the warp's part of the
+            // statistics scratch. With y' = 2^11 y, d = 2^11 M - y' is the
+            // quantised distance before rounding (>= 0 for valid tokens;
+            // the scale by 2^11 is exact) and exp2(y - M) = exp2(-d 2^-11).
             float* msm = reinterpret_cast<float*>(st_sm + qw * 64);
 #pragma unroll
-            for (int hh = 0; hh < NH; ++hh) msm[hh * 32 + lane] = m_own[hh];
+            for (int hh = 0; hh < NH; ++hh) msm[hh * 32 + lane] = m_own[hh] * kLogitQuant;
             __syncwarp();
+            const float s2k = a.scale2 * kLogitQuant;
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh) {
                 uint32_t pk[16];
@@ -714,10 +720,12 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                     const float Mr[4] = {M.x, M.y, M.z, M.w};
 #pragma unroll
                     for (int u = 0; u < 4; u += 2) {
-                        const float y0 = v[hh][r + u] * a.scale2, y1 = v[hh][r + u + 1] * a.scale2;
-                        pk[(r + u) / 2] = quant_logit(Mr[u], y0) | (quant_logit(Mr[u + 1], y1) << 16);
-                        v[hh][r + u] = valid ? exp2_ftz(y0 - Mr[u]) : 0.0f;
-                        v[hh][r + u + 1] = valid ? exp2_ftz(y1 - Mr[u + 1]) : 0.0f;
+                        const float d0 = __fsub_rn(Mr[u], __fmul_rn(v[hh][r + u], s2k));
+                        const float d1 = __fsub_rn(Mr[u + 1], __fmul_rn(v[hh][r + u + 1], s2k));
+                        // invalid tokens (never read back) may give any bits
+                        pk[(r + u) / 2] = __byte_perm(quant_distance(d0), quant_distance(d1), 0x5410);
+                        v[hh][r + u] = valid ? exp2_ftz(__fmul_rn(d0, -kLogitQuantInv)) : 0.0f;
+                        v[hh][r + u + 1] = valid ? exp2_ftz(__fmul_rn(d1, -kLogitQuantInv)) : 0.0f;
                     }
                 }
                 uint4* row = reinterpret_cast<uint4*>(out_buf + hh * kStageOutBytes + tl * 64);
