@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "9da68b7390c426b7197489032a18f1d471ac0e05", "bytes_per_launch": 202160640}
+TRAFFIC = {"source_sha1": "e85a79102c4dbdebe7a6f86580e7c514977b62b8", "bytes_per_launch": 202262272}
 
 
 def parse():
