@@ -264,6 +264,21 @@ def test_invalid_offsets_set_device_status(cuda_lib):
     assert int(out.n_kept.item()) > 0
 
 
+@pytest.mark.parametrize("n", [1, 5, 33, 127, 128, 129, 4095])
+def test_single_prompt_edge_lengths(cuda_lib, n):
+    """One prompt: every kernel after the prep takes its offsets from the
+    token count; lengths around the tile (128), chunk (32) and slice (1,024
+    tokens) edges must match the oracle like a batch does."""
+    q, k, off = random_case(1100 + n, [n], 2, 4, 2, 64, 2, q_gain=2.0)
+    kw = dict(BASE, mode="fixed", keep_p=0.3)
+    got, _ = _run(cuda_lib, q, k, off, kw)
+    ref = oracle.run(q, k, off, **kw)
+    _check_scores(got, ref)
+    _check_t1(got, off, kw)
+    _check_t2(got, ref, off, kw)
+    assert got["kept_off"][0] == 0 and got["kept_off"][1] == len(got["kept_idx"])
+
+
 def test_invalid_single_prompt_offsets_set_device_status(cuda_lib):
     """With one prompt the kernels after the prep take every offset from
     n_tokens_total and request their data before reading the prep kernel's
