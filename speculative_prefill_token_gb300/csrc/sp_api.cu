@@ -13,10 +13,12 @@
 namespace sp {
 namespace {
 
-// Scratch budget of one wave of slabs (quantised logits): about half the L2
-// of a GB300, so the logits written by one wave are still resident when the
-// importance kernel of the same wave reads them.
-constexpr int64_t kWaveScratchBytes = int64_t(60) << 20;
+// Scratch budget of one wave of slabs (quantised logits): most of the 129 MB
+// L2 of a GB300 (the key stream is loaded evict-first), so the logits written
+// by one wave are still resident when the importance kernel of the same wave
+// reads them, with as few waves (logits kernel tails and importance kernels
+// between them) as that allows.
+constexpr int64_t kWaveScratchBytes = int64_t(112) << 20;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -121,6 +123,10 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     int64_t spw = kWaveScratchBytes / per_slab;
     if (spw < 1) spw = 1;
     if (spw > P.slabs) spw = P.slabs;
+    {   // the fewest waves the budget allows, of equal size
+        const int64_t nw = (P.slabs + spw - 1) / spw;
+        spw = (P.slabs + nw - 1) / nw;
+    }
     if (spw > 64) spw = 64;
     P.slabs_per_wave = static_cast<int>(spw);
     P.waves = (P.slabs + P.slabs_per_wave - 1) / P.slabs_per_wave;

@@ -36,11 +36,11 @@ def test_head_pooling_matches_oracle(cuda_lib, case):
 
 
 def test_head_pooling_two_waves_and_64_rows(cuda_lib):
-    """64 query rows per slab (L = 16, G = 4) and 16 slabs of 32K tokens:
+    """64 query rows per slab (L = 16, G = 4) and 16 slabs of 65K tokens:
     the scratch takes two waves, so the per-token maxima of the first wave
     are carried to the second."""
     sp = cuda_lib
-    lengths = [20000, 12768]
+    lengths = [40000, 25536]
     q, k, off = random_case(643, lengths, 4, 16, 4, 64, 16, q_gain=2.0)
     kw = dict(BASE, pool_at="head", mode="fixed", keep_p=0.25)
     got, (qd, kd, _) = _run(cuda_lib, q, k, off, kw)

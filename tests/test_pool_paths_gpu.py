@@ -56,10 +56,10 @@ def test_fused_post_pooling_equals_the_staged_kernels(cuda_lib, case):
 
 
 def test_token_pooling_after_a_first_wave(cuda_lib):
-    """16 slabs of 64 rows over 32K tokens take two waves: the second
+    """16 slabs of 64 rows over 65K tokens take two waves: the second
     wave's importance kernel combines the first wave's per-token maxima."""
     sp = cuda_lib
-    lengths = [20000, 12768]
+    lengths = [40000, 25536]
     q, k, off = random_case(643, lengths, 4, 16, 4, 64, 16, q_gain=2.0)
     kw = dict(BASE, mode="fixed", keep_p=0.25, pool_w=129)
     got, (qd, kd, od) = _run(cuda_lib, q, k, off, kw)
