@@ -195,7 +195,6 @@ struct PoolShared {
 // one_prompt) the window is requested before the flag is read.
 __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int tid, GroupBar g,
                                           PoolShared& sh, const Located<2>& loc, const int32_t* bad1) {
-    const int b = loc.b;
     const int64_t i = tile - loc.base_b;
     const int64_t start = loc.lo[0];
     const int64_t n = static_cast<int64_t>(loc.hi[0]) - start;
