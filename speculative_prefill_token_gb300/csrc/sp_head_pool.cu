@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(kHpThreads, 4) reduce_head_pool_kernel(const H
                     const uint32_t w[4] = {vq[j].x, vq[j].y, vq[j].z, vq[j].w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        dst[(2 * k) * S] = exp2f(fmaf(-static_cast<float>(w[k] & 0xffffu), kLogitQuantInv, off[2 * k]));
-                        dst[(2 * k + 1) * S] = exp2f(fmaf(-static_cast<float>(w[k] >> 16), kLogitQuantInv, off[2 * k + 1]));
+                        dst[(2 * k) * S] = exp2_ftz(fmaf(-static_cast<float>(w[k] & 0xffffu), kLogitQuantInv, off[2 * k]));
+                        dst[(2 * k + 1) * S] = exp2_ftz(fmaf(-static_cast<float>(w[k] >> 16), kLogitQuantInv, off[2 * k + 1]));
                     }
                 } else {
 #pragma unroll
