@@ -28,6 +28,7 @@
 
 #include "sp_device.cuh"
 #include "sp_internal.h"
+#include "sp_phases.cuh"
 
 namespace sp {
 namespace {
@@ -75,12 +76,23 @@ __global__ void __launch_bounds__(kHpThreads, 4) reduce_head_pool_kernel(const H
     const int subs = kTileTokens / TOK;
     const int64_t tile = blockIdx.x / subs;
     const int sub = static_cast<int>(blockIdx.x - tile * subs);
+    // the tile's prompt: from Ntot for a single prompt (the prep kernel
+    // rejects offsets other than {0, Ntot}), else one round of loads
+    Located<1> loc;
+    if (a.B == 1) {
+        const int64_t hi[1] = {a.Ntot};
+        loc = one_prompt<1>(static_cast<int32_t>((a.Ntot + kTileTokens - 1) / kTileTokens), hi);
+    } else {
+        const int32_t* const aux[1] = {a.seq_off};
+        loc = locate<1>(a.tile_base, aux, a.B, tile);
+    }
     if (*a.bad) return;
-    if (tile >= a.tile_base[a.B]) return;
-    const int b = search_base(a.tile_base, a.B, tile);
-    const int64_t start = a.seq_off[b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
-    const int64_t first = (tile - a.tile_base[b]) * kTileTokens + static_cast<int64_t>(sub) * TOK;
+    if (tile >= loc.total) return;
+    const int b = loc.b;
+    const int64_t base_b = loc.base_b;
+    const int64_t start = loc.lo[0];
+    const int64_t n = static_cast<int64_t>(loc.hi[0]) - start;
+    const int64_t first = (tile - base_b) * kTileTokens + static_cast<int64_t>(sub) * TOK;
     const int nvalid = static_cast<int>(min64(TOK, n - first));
     if (nvalid <= 0) return;
     const int H = a.H, E = TOK + 2 * H, S = hp_stride(RS, H);
@@ -92,7 +104,7 @@ __global__ void __launch_bounds__(kHpThreads, 4) reduce_head_pool_kernel(const H
     extern __shared__ float sm[];
     float* tab = sm;                                           // [nqe][RS]: M - lse2
     float* P = tab + hp_quarters(RS, H) * RS;                  // [RS][S]: p of row r, halo token e
-    const int64_t row0 = static_cast<int64_t>(a.tile_base[b]) * kTileTokens;  // scratch row of token 0
+    const int64_t row0 = base_b * kTileTokens;  // scratch row of token 0
     const int t = threadIdx.x;
     const int n_tab = nqe * RS;
 
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(kHpThreads, 4) reduce_head_pool_kernel(const H
             if (idx < n_tab) {
                 const int qq = idx / RS, r = idx - qq * RS;
                 const int64_t pq = pq_lo + qq;
-                const int64_t gt = a.tile_base[b] + pq / 4;
+                const int64_t gt = base_b + pq / 4;
                 tl[j] = __ldcg(a.lmax + ((static_cast<int64_t>(s) * a.tiles_max + gt) * 4 + pq % 4) * RS + r);
                 ts[j] = __ldcg(a.lse2 + (static_cast<int64_t>(s) * a.B + b) * RS + r);
             }
