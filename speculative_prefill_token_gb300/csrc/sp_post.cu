@@ -116,22 +116,49 @@ __device__ __forceinline__ int64_t listing_final_count(const PostArgs& a, int b)
 __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const PostArgs a) {
     grid_dep_wait();
     grid_dep_launch();
-    if (a.hdr->bad_input) return;
     __shared__ int64_t red[3][kRankWarps];
     __shared__ int64_t base_k[kSliceChunks], base_u[kSliceChunks];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int64_t S = a.slice_base[a.B];
     const int64_t s = blockIdx.x;
-    if (s > S) return;
-    const int b = s == S ? a.B : search_base(a.slice_base, a.B, s);
-    const int64_t sb = s == S ? S : a.slice_base[b];
+    // A single prompt (B = 1) has seq_off = {0, Ntot} once the prep kernel
+    // has accepted the input: its slice count follows from Ntot, and the
+    // slice's counts, the prompt's count before the fill and the slice's
+    // keep flags are requested before the flag is read.
+    const bool one = a.B == 1;
+    int64_t S;
+    int64_t k0_one = 0;
+    uint8_t f_one = 0;
+    int64_t part[3] = {0, 0, 0};
+    if (one) {
+        const int64_t nc1 = (a.Ntot + a.C - 1) / a.C;
+        S = (nc1 + kSliceChunks - 1) / kSliceChunks;
+        if (s > S) return;
+        if (s < S) {
+            k0_one = __ldcg(a.lcount);
+            if (warp == 0 && s * kSliceChunks + lane < nc1) f_one = __ldcg(a.keep + s * kSliceChunks + lane);
+        }
+        for (int64_t i = t; i < s; i += kRankThreads) {
+            part[1] += __ldcg(a.scount + i);
+            part[2] += __ldcg(a.ucount + i);
+        }
+        if (a.hdr->bad_input) return;
+    } else {
+        if (a.hdr->bad_input) return;
+        S = a.slice_base[a.B];
+        if (s > S) return;
+    }
+    const int b = one ? 0 : (s == S ? a.B : search_base(a.slice_base, a.B, s));
+    const int64_t sb = one ? 0 : (s == S ? S : a.slice_base[b]);
     // output offset of prompt b (final counts of all earlier prompts) and
     // the kept0 / spare tokens of the prompt's slices before this one
-    int64_t part[3] = {0, 0, 0};
-    for (int bb = t; bb < b; bb += kRankThreads) part[0] += listing_final_count(a, bb);
-    for (int64_t i = sb + t; i < s; i += kRankThreads) {
-        part[1] += __ldcg(a.scount + i);
-        part[2] += __ldcg(a.ucount + i);
+    if (!one) {
+        for (int bb = t; bb < b; bb += kRankThreads) part[0] += listing_final_count(a, bb);
+        for (int64_t i = sb + t; i < s; i += kRankThreads) {
+            part[1] += __ldcg(a.scount + i);
+            part[2] += __ldcg(a.ucount + i);
+        }
+    } else if (s == S && t == 0) {
+        part[0] = listing_final_count(a, 0);  // the totals CTA: the prompt's final count
     }
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
@@ -147,7 +174,8 @@ __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const Post
     }
     if (s == S) {
         if (t == 0) {
-            for (int bb = a.B - 1; bb >= 0 && a.slice_base[bb] == S; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
+            for (int bb = a.B - 1; !one && bb >= 0 && a.slice_base[bb] == S; --bb)
+                a.kept_off[bb] = static_cast<int32_t>(P);
             a.kept_off[a.B] = static_cast<int32_t>(P);
             *a.n_kept = static_cast<int32_t>(P);
         }
@@ -155,14 +183,15 @@ __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const Post
     }
     if (t == 0 && s == sb) {
         // first slice of prompt b: its offset, and that of empty prompts before it
-        for (int bb = b; bb >= 0 && a.slice_base[bb] == s; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
+        a.kept_off[b] = static_cast<int32_t>(P);
+        for (int bb = b - 1; bb >= 0 && a.slice_base[bb] == s; --bb) a.kept_off[bb] = static_cast<int32_t>(P);
     }
-    const int64_t start = a.seq_off[b];
-    const int64_t n = static_cast<int64_t>(a.seq_off[b + 1]) - start;
-    const int64_t coff = a.chunk_off[b];
-    const int64_t nc = static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
+    const int64_t start = one ? 0 : a.seq_off[b];
+    const int64_t n = one ? a.Ntot : static_cast<int64_t>(a.seq_off[b + 1]) - start;
+    const int64_t coff = one ? 0 : a.chunk_off[b];
+    const int64_t nc = one ? (a.Ntot + a.C - 1) / a.C : static_cast<int64_t>(a.chunk_off[b + 1]) - coff;
     if (nc > kMaxPromptChunks) return;  // reported by the rank kernel; nothing kept
-    const int64_t k0 = __ldcg(a.lcount + b);
+    const int64_t k0 = one ? k0_one : __ldcg(a.lcount + b);
     const int64_t fill = min64(max64(0, listing_eff_min(n, a.min_tok) - k0), n - k0);
     const int64_t k = k0 + fill;
     const int64_t M = (a.max_keep > 0 && k > a.max_keep) ? a.max_keep : 0;
@@ -174,7 +203,7 @@ __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const Post
         int64_t ck = 0, cu = 0;
         if (c < nc) {
             const int64_t a0 = c * a.C, a1 = a0 + chunk_tokens(n, a.C, c);
-            if (__ldcg(a.keep + coff + c) & 1) {
+            if ((one ? f_one : __ldcg(a.keep + coff + c)) & 1) {
                 ck = a1 - a0;
             } else {
                 ck = listing_forced_in(a0, a1, n);
