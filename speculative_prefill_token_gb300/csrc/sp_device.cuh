@@ -201,12 +201,19 @@ __device__ __forceinline__ void flush_rows(float2 (&run)[NH], float2* sm, int qw
 }
 
 // Work split of the logits kernels: CTA c of C owns flattened items
-// [floor(W*c/C), floor(W*(c+1)/C)). owner(w) = the CTA owning item w.
-__device__ __forceinline__ int64_t split_start(int64_t W, int64_t C, int64_t c) { return (W * c) / C; }
+// [start(c), start(c + 1)), q = W / C items each and one more for the first
+// r = W mod C CTAs (start(c) = c q + min(c, r)). The last CTA index is the
+// one most often placed late (on the SM that still runs the previous
+// kernel), so it never carries an extra item. owner(w) = the CTA owning
+// item w.
+__device__ __forceinline__ int64_t split_start(int64_t W, int64_t C, int64_t c) {
+    const int64_t q = W / C, r = W - q * C;
+    return c * q + (c < r ? c : r);
+}
 
-// largest c with floor(W*c/C) <= w  <=>  W*c < (w+1)*C
 __device__ __forceinline__ int64_t split_owner(int64_t W, int64_t C, int64_t w) {
-    return ((w + 1) * C - 1) / W;
+    const int64_t q = W / C, r = W - q * C, big = r * (q + 1);
+    return w < big ? w / (q + 1) : r + (w - big) / q;
 }
 
 // Called by all 128 threads of a warpgroup right after it wrote (and
