@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) of one logits-kernel launch on this workload, from
 # an ncu application-replay capture (profiles/logits_tc_draft2b.md); reported
 # only while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "7135f4a60b7287a1dfd92d4e864c172e980727b0", "bytes_per_launch": 202267264}
+TRAFFIC = {"source_sha1": "a9ae8b8b5b7868ffbac52202f1eb1c3d87ec713e", "bytes_per_launch": 202212608}
 
 
 def parse():

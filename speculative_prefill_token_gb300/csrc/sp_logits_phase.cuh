@@ -350,7 +350,7 @@ __device__ __forceinline__ int paged_row(const TcArgs& a, const ItemCursor& cur,
 }
 
 // Producer of the block-paged path, run by the whole producer warp: lane 0
-// waits on the ring and issues the copies (nbox boxes per 16 KB stage);
+// waits on the ring, lane j issues box j of each 16 KB stage (nbox boxes);
 // lane j < nbox looks up the block of box j three items ahead, so that
 // the table's latency overlaps the copies of the items before it (also at
 // the start, where the ring is still empty).
@@ -428,12 +428,12 @@ __device__ __forceinline__ void produce_paged(const LogitsCtx& c, const TcArgs& 
             ok = __shfl_sync(kFull, ok, 0);
             if (!ok) break;
             if (lane == 0) mbar_arrive_expect_tx(c.bar_full + 8 * stage, kKBlockBytes);
-            for (int j = 0; j < a.nbox; ++j) {
-                const int rj = __shfl_sync(kFull, row, j);
-                if (lane == 0)
-                    tma_load_4d(c.k_ring + stage * kKBlockBytes + static_cast<uint32_t>(j * a.box_h) * 128u,
-                                tmap_k + layer, c.bar_full + 8 * stage, kb * 64, rj, g, 0, pol);
-            }
+            __syncwarp();
+            // lane j issues box j of the stage (its own block's row): one
+            // thread issuing all of a stage's boxes set the rate of small blocks
+            if (lane < a.nbox)
+                tma_load_4d(c.k_ring + stage * kKBlockBytes + static_cast<uint32_t>(lane * a.box_h) * 128u,
+                            tmap_k + layer, c.bar_full + 8 * stage, kb * 64, row, g, 0, pol);
             if (lane == 0) {
                 issued[stage] = true;
                 issued_phase[stage] = phase;
