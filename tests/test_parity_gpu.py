@@ -282,7 +282,7 @@ def test_single_prompt_edge_lengths(cuda_lib, n):
 def test_invalid_single_prompt_offsets_set_device_status(cuda_lib):
     """With one prompt the kernels after the prep take every offset from
     n_tokens_total and request their data before reading the prep kernel's
-    verdict: offsets that do not span [0, Ntot) must still end in
+    decision: offsets that do not span [0, Ntot) must still end in
     SP_ERR_DEVICE, and the next valid call on the same workspace must equal
     a call on a fresh one."""
     import torch
