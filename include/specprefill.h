@@ -118,7 +118,10 @@ typedef struct sp_shape {
     int32_t head_dim;        /* d in {64, 128, 256} */
     int32_t n_lookahead;     /* L >= 1 query vectors per layer and head; L*G <= 64 */
     int32_t n_tokens_total;  /* Ntot = seq_off[B] >= 1 */
-    int32_t reserved;        /* must be 0 */
+    int32_t max_seq_len;     /* 0 (no bound), or the longest prompt the caller
+                                allows: a prompt with more tokens makes the
+                                call's device status SP_ERR_DEVICE (checked on
+                                the device with seq_off); < 0 is invalid */
     int64_t k_stride_layer, k_stride_token, k_stride_head;
     int64_t q_stride_seq, q_stride_layer, q_stride_step, q_stride_head;
 } sp_shape;
@@ -170,6 +173,12 @@ int sp_workspace_init(void* ws, size_t ws_bytes, sp_stream_t stream);
 
 /* Token importance (logits, softmax, max over heads and layers, mean over
  * steps): imp[t] for every global token t (device, Ntot floats).
+ * Defined by "SpecPrefill — Implementation Guide", §How It Works / Attention
+ * Capture (one post-softmax attention row per head and lookahead step over
+ * the prompt's keys) and §How It Works / Token Importance (max over heads,
+ * then max over layers, then the mean over the lookahead steps); the draft's
+ * L lookahead queries and full-attention layers are those of llama.cpp PR
+ * "Speculative prefill", §Approach items 1-2.
  * seq_off (device, B+1 int32, non-decreasing from 0 to Ntot), q and k
  * (device, bf16 bits) as described at sp_shape. */
 int sp_attn_importance(const sp_shape* shape, const sp_params* params,
@@ -184,6 +193,11 @@ int sp_attn_importance_simt(const sp_shape* shape, const sp_params* params,
                             float* imp, void* ws, size_t ws_bytes, sp_stream_t stream);
 
 /* Smoothing and chunk scores from imp (device, Ntot floats).
+ * Defined by llama.cpp PR "Speculative prefill", §Approach item 3 (the
+ * W-wide average pool), "SpecPrefill — Implementation Guide" v3.1, §v3.1
+ * Optimizations item 5 (min-max normalisation), v3 §v3 Improvements item 2
+ * (structural boost of the first and last tokens) and §Chunk Selection (a
+ * chunk's score is the mean of its tokens' scores).
  * tok_score (device, Ntot floats, nullable): pooled score before
  * normalisation and boost. chunk_score (device, sp_max_chunks floats): the
  * final chunk scores. chunk_off (device, B+1 int32): written. */
@@ -204,11 +218,19 @@ int sp_pool_chunk(const sp_shape* shape, const sp_params* params, const int32_t*
  *   required device outputs.
  * - status_out (device, one int32, nullable) receives this call's device
  *   status in stream order: SP_OK, or SP_ERR_DEVICE when seq_off is invalid.
- * - Batches whose scratch does not fit return SP_ERR_UNSUPPORTED. The
- *   scratch is about 12*(B+1) bytes of offsets plus 8 bytes per 1024-token
- *   block (chunk 32), i.e. up to roughly 4096 prompts of 16M tokens total.
- * - The first call on each GPU looks up the array's device address once;
- *   make that first call before any stream capture.
+ * - Batches whose scratch does not fit return SP_ERR_UNSUPPORTED before
+ *   anything is enqueued. The scratch is a 256-byte header, four offset
+ *   tables of 4*(B+1) bytes each (each rounded up to 256 bytes) and 8 bytes
+ *   per pooling block of floor(1024 / chunk) * chunk tokens (one block per
+ *   1024 tokens at chunk 32, plus one per prompt); it depends on B, Ntot and
+ *   chunk only. At chunk 32 that admits, for example, 16,000 prompts of 1K
+ *   tokens or one prompt of 100M tokens.
+ * - Each call looks up the array's device address in the calling thread's
+ *   current CUDA context (a new context after cudaDeviceReset, or another
+ *   context on the same GPU, has its own copy of the array) unless the
+ *   stream is being captured; a call made during stream capture reuses the
+ *   address the last uncaptured call on that context found, so make one
+ *   uncaptured call per context first.
  * - All calls on one GPU share the array and each leaves its contents
  *   behind: calls that overlap on the GPU (unordered streams or threads)
  *   race, so order them on one stream. */
@@ -217,7 +239,12 @@ int sp_pool_chunk_noalloc(const sp_shape* shape, const sp_params* params,
                           float* chunk_score, int32_t* chunk_off, int32_t* status_out,
                           sp_stream_t stream);
 
-/* Chunk selection per prompt. chunk_keep (device, one byte per chunk):
+/* Chunk selection per prompt, defined by "SpecPrefill — Implementation
+ * Guide", §Chunk Selection (the top k = max(1, ceil(nc * p)) chunks by
+ * score), v3 §v3 Improvements item 1 (cumulative attention mass: the
+ * shortest ranked prefix holding `mass` of the total) and llama.cpp PR
+ * "Speculative prefill", §Approach item 4 (BOS and the final chunk are always
+ * kept). chunk_keep (device, one byte per chunk):
  * bit 0 = chosen by the ranking, bit 1 = forced final chunk.
  * SP_RULE_LISTING is not a chunk-level rule: SP_ERR_UNSUPPORTED (likewise
  * for sp_gather_kept). */
@@ -225,7 +252,10 @@ int sp_select(const sp_shape* shape, const sp_params* params, const int32_t* seq
               const int32_t* chunk_off, const float* chunk_score, uint8_t* chunk_keep,
               void* ws, size_t ws_bytes, sp_stream_t stream);
 
-/* Stream compaction of kept tokens. For prompt b, its kept tokens (those
+/* Stream compaction of kept tokens, defined by "SpecPrefill —
+ * Implementation Guide", §How It Works / Sparse Prefill (the target
+ * prefills only the kept tokens, each at its original position ID). For
+ * prompt b, its kept tokens (those
  * in a chunk with chunk_keep != 0, plus token 0 when force_bos) in
  * increasing order occupy [kept_off[b], kept_off[b+1]) of kept_idx (global
  * token index) and kept_pos (position within the prompt, i.e. the original
@@ -353,7 +383,12 @@ int sp_select_from_importance(const sp_shape* shape, const sp_params* params,
                               int32_t* kept_idx, int32_t* kept_pos, int32_t* kept_off,
                               int32_t* n_kept, void* ws, size_t ws_bytes, sp_stream_t stream);
 
-/* The whole path in one call. imp, tok_score, chunk_score, chunk_off and
+/* The whole path in one call: sp_attn_importance, sp_pool_chunk, sp_select
+ * and sp_gather_kept in sequence, defined by the passages cited at each of
+ * them ("SpecPrefill — Implementation Guide", §How It Works / Attention
+ * Capture, Token Importance, Sparse Prefill, §Chunk Selection, v3 §v3
+ * Improvements items 1-2, v3.1 §v3.1 Optimizations item 5; llama.cpp PR
+ * "Speculative prefill", §Approach items 1-4). imp, tok_score, chunk_score, chunk_off and
  * chunk_keep are optional outputs (nullable; kept in the workspace when
  * null); kept_idx, kept_pos, kept_off and n_kept are required. `prof` is
  * optional (nullable). */

@@ -65,7 +65,7 @@ class _Shape(ctypes.Structure):
     _fields_ = [("n_seqs", ctypes.c_int32), ("n_layers", ctypes.c_int32),
                 ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_lookahead", ctypes.c_int32),
-                ("n_tokens_total", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_tokens_total", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("k_stride_layer", ctypes.c_int64), ("k_stride_token", ctypes.c_int64),
                 ("k_stride_head", ctypes.c_int64), ("q_stride_seq", ctypes.c_int64),
                 ("q_stride_layer", ctypes.c_int64), ("q_stride_step", ctypes.c_int64),
@@ -206,8 +206,10 @@ def _stream(stream) -> int:
     return s.cuda_stream
 
 
-def shape_of(q, k, seq_off=None, n_seqs: Optional[int] = None) -> _Shape:
-    """C shape struct from the q [B, Ly, L, Hq, d] and k [Ly, Ntot, Hk, d] tensors."""
+def shape_of(q, k, seq_off=None, n_seqs: Optional[int] = None, max_seq_len: int = 0) -> _Shape:
+    """C shape struct from the q [B, Ly, L, Hq, d] and k [Ly, Ntot, Hk, d]
+    tensors; max_seq_len > 0 states the longest prompt allowed (a longer one
+    makes the call's device status SP_ERR_DEVICE)."""
     if q.dim() != 5 or k.dim() != 4:
         raise ValueError("q must be [B, Ly, L, Hq, d] and k [Ly, Ntot, Hk, d]")
     if q.element_size() != 2 or k.element_size() != 2:
@@ -218,7 +220,7 @@ def shape_of(q, k, seq_off=None, n_seqs: Optional[int] = None) -> _Shape:
         raise ValueError("q and k disagree on layers or head_dim")
     if q.stride(-1) != 1 or k.stride(-1) != 1:
         raise ValueError("head_dim must be contiguous")
-    return _Shape(int(b), int(ly), int(hq), int(hk), int(d), int(steps), int(ntot), 0,
+    return _Shape(int(b), int(ly), int(hq), int(hk), int(d), int(steps), int(ntot), int(max_seq_len),
                   k.stride(0), k.stride(1), k.stride(2),
                   q.stride(0), q.stride(1), q.stride(2), q.stride(3))
 
@@ -430,13 +432,13 @@ def alloc_outputs(q, k, params: SelectionParams, intermediates: bool = True) -> 
 
 
 def specprefill_score(q, k, seq_off, params: SelectionParams, out: Optional[ScoreOutputs] = None,
-                      ws=None, stream=None, profile_events=None) -> ScoreOutputs:
+                      ws=None, stream=None, profile_events=None, max_seq_len: int = 0) -> ScoreOutputs:
     """The whole path: kept token indices and positions per prompt.
 
     ``profile_events`` = (start, stop) torch.cuda.Event pair recorded around
-    the logits kernel(s).
+    the logits kernel(s). ``max_seq_len`` > 0: the longest prompt allowed.
     """
-    shape = shape_of(q, k)
+    shape = shape_of(q, k, max_seq_len=max_seq_len)
     if out is None:
         out = alloc_outputs(q, k, params)
     if ws is None:

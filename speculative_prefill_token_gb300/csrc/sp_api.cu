@@ -29,7 +29,7 @@ bool finite_pos(float x) { return std::isfinite(x) && x > 0.0f; }
 int check_shape(const sp_shape* s) {
     if (!s) return SP_ERR_INVALID_ARG;
     if (s->n_seqs < 1 || s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1 ||
-        s->head_dim < 1 || s->n_lookahead < 1 || s->n_tokens_total < 1 || s->reserved != 0)
+        s->head_dim < 1 || s->n_lookahead < 1 || s->n_tokens_total < 1 || s->max_seq_len < 0)
         return SP_ERR_INVALID_ARG;
     if (s->n_q_heads % s->n_kv_heads != 0) return SP_ERR_INVALID_ARG;
     if (s->n_seqs > kMaxSeqs) return SP_ERR_UNSUPPORTED;
@@ -106,6 +106,7 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.Nmma = P.R <= 16 ? 16 : ((P.R + 15) & ~15);
     P.Nacc = P.Nmma <= 32 ? 32 : 64;
     P.Ntot = s->n_tokens_total;
+    P.max_len = s->max_seq_len;
     P.slabs = P.Ly * P.Hk;
     P.C = p->chunk;
     P.W = p->pool_w;

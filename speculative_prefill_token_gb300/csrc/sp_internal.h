@@ -46,6 +46,7 @@ struct Plan {
     int slabs_per_wave, waves;
     float scale2;         // logit scale * log2(e)
     int64_t spin;         // bounded-wait poll limit
+    int max_len;          // longest prompt the caller allows (0 = no bound)
     int head_h;           // per-head pooling: half window (0 = pool the per-token importance)
     int kv_block_size, kv_table_stride;  // block-paged key source (checked by the prep kernel)
     // workspace offsets (bytes)
@@ -60,9 +61,10 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* plan);
 // Each returns cudaSuccess or the launch error.
 
 // Per-call offsets and checks; also zeroes the per-segment record counters
-// and the per-prompt kept counts of the listing rule (one range).
+// and the per-prompt kept counts of the listing rule (one range of
+// n_counters words; < 0 selects the plan's own count).
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
-                        cudaStream_t st);
+                        cudaStream_t st, int64_t n_counters = -1);
 
 // Logits of the slabs [slab0, slab0 + nslab) into the workspace scratch
 // (one 128-row slot per tile), plus softmax records per (CTA, segment,

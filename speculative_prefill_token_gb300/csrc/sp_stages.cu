@@ -29,7 +29,8 @@ namespace {
 __device__ __forceinline__ void set_status(WsHeader* h, int code) { atomicCAS(&h->status, 0, code); }
 
 // ------------------------------------------------------------------ prep
-// One CTA: validates seq_off (0 = first, non-decreasing, last = Ntot) and
+// One CTA: validates seq_off (0 = first, non-decreasing, last = Ntot, no
+// prompt longer than the shape's max_seq_len when that is set) and
 // writes the per-prompt bases of logits tiles, chunks and post blocks.
 // A user-provided chunk_off (standalone select/gather) must match.
 constexpr int kPrepThreads = 256;  // small enough to share an SM with the logits kernel
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
                                                             const int32_t* chunk_off_check,
                                                             unsigned* seg_cnt, int64_t n_seg_cnt,
                                                             int block_size, int table_stride,
-                                                            WsHeader* hdr) {
+                                                            int max_len, WsHeader* hdr) {
     grid_dep_wait();
     grid_dep_launch();
     __shared__ int bad;
@@ -56,6 +57,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
     for (int b = tid; b < B; b += kPrepThreads) {
         const int64_t n = static_cast<int64_t>(seq_off[b + 1]) - seq_off[b];
         if (n < 0) bad = 1;
+        // a prompt longer than the caller's stated bound
+        if (max_len > 0 && n > max_len) bad = 1;
         // a block-paged key source must list every block of the prompt
         if (block_size > 0 && (n + block_size - 1) / block_size > table_stride) bad = 1;
     }
@@ -551,14 +554,14 @@ __global__ void __launch_bounds__(256) gather_write_kernel(
 // ================================================================ launchers
 
 cudaError_t launch_prep(const Plan& pl, const int32_t* seq_off, void* ws, int32_t* chunk_off_out,
-                        cudaStream_t st) {
+                        cudaStream_t st, int64_t n_counters) {
+    if (n_counters < 0) n_counters = (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B;
     return launch_k(prep_kernel, 1, kPrepThreads, 0, st, seq_off, pl.B, pl.Ntot, pl.C, pl.Tb,
         ws_ptr<int32_t>(ws, pl.o_tile_base),
         ws_ptr<int32_t>(ws, pl.o_chunk_off),
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), chunk_off_out,
-        nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt),
-        (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B, pl.kv_block_size, pl.kv_table_stride,
-        ws_ptr<WsHeader>(ws, 0));
+        nullptr, ws_ptr<unsigned>(ws, pl.o_segcnt), n_counters, pl.kv_block_size,
+        pl.kv_table_stride, pl.max_len, ws_ptr<WsHeader>(ws, 0));
 }
 
 cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
@@ -569,7 +572,7 @@ cudaError_t launch_prep_check(const Plan& pl, const int32_t* seq_off, void* ws,
         ws_ptr<int32_t>(ws, pl.o_pblk_base), ws_ptr<int32_t>(ws, pl.o_slice_base), nullptr,
         chunk_off_check, ws_ptr<unsigned>(ws, pl.o_segcnt),
         (static_cast<int64_t>(pl.slabs_per_wave) + 1) * pl.B, pl.kv_block_size, pl.kv_table_stride,
-        ws_ptr<WsHeader>(ws, 0));
+        pl.max_len, ws_ptr<WsHeader>(ws, 0));
 }
 
 cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int nslab, int wave,

@@ -38,6 +38,39 @@ def test_header_declares_the_entry_points():
         assert required in names
 
 
+def _comment_before(text, name):
+    """The block comment directly above the declaration of `name`."""
+    m = re.search(r"/\*((?:(?!\*/).)*?)\*/\s*(?:int|const char\*)\s+" + name + r"\s*\(", text, flags=re.S)
+    assert m, f"no comment above {name}"
+    return " ".join(m.group(1).replace("*", " ").split())
+
+
+def test_each_method_entry_point_cites_its_passage():
+    text = open(os.path.join(ROOT, "include", "specprefill.h")).read()
+    cites = {
+        "sp_attn_importance": ("Token Importance", "Attention Capture"),
+        "sp_pool_chunk": ("§Approach item 3", "§Chunk Selection"),
+        "sp_select": ("§Chunk Selection", "§v3 Improvements item 1", "§Approach item 4"),
+        "sp_gather_kept": ("Sparse Prefill",),
+        "sp_specprefill_score": ("Token Importance", "Sparse Prefill", "§Approach items 1-4"),
+    }
+    for name, needles in cites.items():
+        comment = _comment_before(text, name)
+        for needle in needles:
+            assert needle in comment, f"{name}: no '{needle}' in its comment"
+
+
+def test_max_seq_len_field_is_the_shape_bound(lib):
+    assert [f for f, _ in sp._Shape._fields_][7] == "max_seq_len"
+    s = _shape()
+    s.max_seq_len = -1
+    rc, _ = _ws(s, sp.SelectionParams())
+    assert rc == 1
+    s.max_seq_len = 4096
+    rc, _ = _ws(s, sp.SelectionParams())
+    assert rc == 0
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} is declared but not exported"
@@ -264,3 +297,23 @@ def test_kv_source_validation(lib):
     assert call([8192] * 65, shape=many) == 2          # more layers than tensor maps
     # the workspace check comes after: a valid source reaches it
     assert call(good, table=4096, bs=16, stride=256) == 3
+
+
+def test_noalloc_rejects_an_oversized_batch_before_any_launch(lib):
+    """The fixed scratch of sp_pool_chunk_noalloc holds the offset tables and
+    one (min, max) pair per pooling block; a batch that does not fit is
+    refused on the host (the pointers are never dereferenced)."""
+    a = ctypes.c_void_p(4096)
+    p = sp.SelectionParams(mode="mass")._c()
+    # 65536 prompts: four tables of 256 KB each do not fit 1 MiB
+    big_b = sp.token_shape(65536, 1 << 20)
+    assert lib.sp_pool_chunk_noalloc(ctypes.byref(big_b), ctypes.byref(p), a, a, a, a, a, None,
+                                     None) == 2
+    # 2^30 tokens at chunk 32: 2^20 pooling blocks of 8 bytes
+    big_n = sp.token_shape(1, 1 << 30)
+    assert lib.sp_pool_chunk_noalloc(ctypes.byref(big_n), ctypes.byref(p), a, a, a, a, a, None,
+                                     None) == 2
+    # null outputs are refused first
+    ok = sp.token_shape(4, 4096)
+    assert lib.sp_pool_chunk_noalloc(ctypes.byref(ok), ctypes.byref(p), a, a, None, a, a, None,
+                                     None) == 1

@@ -264,6 +264,34 @@ def test_invalid_offsets_set_device_status(cuda_lib):
     assert int(out.n_kept.item()) > 0
 
 
+def test_max_seq_len_bound_is_checked_on_the_device(cuda_lib):
+    """sp_shape.max_seq_len > 0 bounds every prompt's length: a batch with a
+    longer prompt ends in SP_ERR_DEVICE, the same batch with the bound at its
+    longest prompt (or no bound) is scored exactly as without it."""
+    import torch
+    sp = cuda_lib
+    q, k, off = random_case(904, [300, 700, 64], 1, 4, 2, 64, 2, q_gain=2.0)
+    qd, kd, od = gh.to_device(type("I", (), {"q": q, "k": k, "seq_off": off})())
+    p = sp.SelectionParams(**dict(BASE, mode="fixed", keep_p=0.3))
+    ws = sp.make_workspace(sp.shape_of(qd, kd), p)
+    sp.specprefill_score(qd, kd, od, p, ws=ws, max_seq_len=699)
+    assert sp.device_status(ws) == 6
+    got = gh.out_to_numpy(sp.specprefill_score(qd, kd, od, p, ws=ws, max_seq_len=700))
+    assert sp.device_status(ws) == 0
+    free = gh.out_to_numpy(sp.specprefill_score(qd, kd, od, p, ws=ws))
+    assert sp.device_status(ws) == 0
+    for key in free:
+        assert np.array_equal(got[key], free[key]), key
+    # one prompt: the post kernels take its offsets from the token count
+    q1, k1, off1 = random_case(905, [900], 1, 4, 2, 64, 2, q_gain=2.0)
+    qd, kd, od = gh.to_device(type("I", (), {"q": q1, "k": k1, "seq_off": off1})())
+    ws = sp.make_workspace(sp.shape_of(qd, kd), p)
+    sp.specprefill_score(qd, kd, od, p, ws=ws, max_seq_len=512)
+    assert sp.device_status(ws) == 6
+    sp.specprefill_score(qd, kd, od, p, ws=ws, max_seq_len=900)
+    assert sp.device_status(ws) == 0
+
+
 @pytest.mark.parametrize("n", [1, 5, 33, 127, 128, 129, 4095])
 def test_single_prompt_edge_lengths(cuda_lib, n):
     """One prompt: every kernel after the prep takes its offsets from the
