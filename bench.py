@@ -31,9 +31,12 @@ the importance phase with the tcgen05 logits kernel and with the CUDA-core
 one; `listing_rule`, the same calls under the pages' own selection rule
 (reference-compatibility mode); `head_pool`, the pool applied to every
 attention row before the max; `paged_kv`, the keys read in place from
-block-paged per-layer pools (one entry per --paged-block size); `consumer`,
-the bandwidth of the sparse-prefill gathers (kept token ids, kept K and V
-rows).
+block-paged per-layer pools (one entry per --paged-block size); `draft_kv`,
+the same scoring of a random-weight draft model's own cache (projected,
+QK-normed, rotated keys of the prompt in 16-token blocks and the queries of
+its lookahead tokens, synth/draft.py) at the workload's attention shape;
+`consumer`, the bandwidth of the sparse-prefill gathers (kept token ids,
+kept K and V rows).
 """
 
 import argparse
@@ -54,7 +57,7 @@ if ROOT not in sys.path:
 METRIC = "prompt tokens scored+selected/sec at N=32K; HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-ALL_LEGS = ("e2e", "pipelined", "importance", "listing", "head_pool", "paged", "consumer")
+ALL_LEGS = ("e2e", "pipelined", "importance", "listing", "head_pool", "paged", "draft", "consumer")
 # DRAM bytes (read + write) of one logits-kernel launch per workload, from an
 # ncu application-replay capture of this bench's own calls; reported only
 # while the kernel sources are the ones that were measured.
@@ -418,6 +421,8 @@ def run_ours(args, rank, world, local):
             legs_out["paged_kv"] = [leg_paged(sp, torch, args, timer, shape, params, qs, ks, off,
                                               out, n_kept, world, ntot, dev, int(bs))
                                     for bs in args.paged_block.split(",") if bs]
+        if "draft" in legs:
+            legs_out["draft_kv"] = leg_draft(sp, torch, args, timer, w, params, world, dev)
         if "consumer" in legs:
             legs_out["consumer"] = leg_consumer(sp, torch, args, timer, shape, ks, out, n_kept,
                                                 ntot, dev)
@@ -614,6 +619,57 @@ def leg_paged(sp, torch, args, timer, shape, params, qs, ks, off, out, n_kept, w
            "same_kept_as_dense": bool(nk == n_kept and torch.equal(kv_out.kept_idx[:nk],
                                                                    out.kept_idx[:nk]))}
     del pools
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_draft(sp, torch, args, timer, w, params, world, dev):
+    """Keys and lookahead queries of a random-weight draft model with the
+    workload's attention shape and prompt lengths (hidden 2048 for 32K-token
+    prompts, else 1024), its cache in 16-token blocks shuffled over one pool
+    per layer, scored in place; the kept lists are compared with the dense
+    call on the same keys."""
+    from synth import DraftShape, draft_attention_inputs, page_keys
+    from synth.inputs import prompt_lengths
+    lengths = prompt_lengths(w)
+    t0 = time.perf_counter()
+    shape_d = DraftShape(hidden=2048 if int(lengths.sum()) >= 32768 else 1024, n_layers=w.n_layers,
+                         n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+                         n_lookahead=w.n_lookahead, rotary_dim=w.head_dim // 4, seed=2002)
+    q_np, k_np, off_np = draft_attention_inputs(shape_d, lengths)
+    pools_np, table_np = page_keys(k_np, off_np, 16, seed=2)
+    build_s = time.perf_counter() - t0
+    ntot = int(off_np[-1])
+    qd = torch.from_numpy(np.ascontiguousarray(q_np).view(np.int16)).to(dev)
+    od = torch.from_numpy(off_np).to(dev)
+    td = torch.from_numpy(table_np).to(dev)
+    copies = max(2, min(4, -(-(768 << 20) // max(k_np.nbytes, 1))))
+    pools = [[torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in pools_np]
+             for _ in range(copies)]
+    kv_shape = sp.shape_of_kv(qd, pools[0], ntot, td)
+    kv_ws = sp.make_workspace(kv_shape, params, dev)
+    nb = len(lengths)
+    kv_out = sp.ScoreOutputs(kept_idx=torch.empty(ntot, dtype=torch.int32, device=dev),
+                             kept_pos=torch.empty(ntot, dtype=torch.int32, device=dev),
+                             kept_off=torch.empty(nb + 1, dtype=torch.int32, device=dev),
+                             n_kept=torch.empty(1, dtype=torch.int32, device=dev))
+
+    def d_step(i):
+        sp.specprefill_score_kv(qd, pools[i % copies], od, ntot, params, block_table=td, out=kv_out,
+                                ws=kv_ws, stream=timer.stream)
+
+    d_ms, _ = timer.run(d_step, args.steps, args.warmup)
+    d_ms /= args.steps
+    nk = int(kv_out.n_kept.item())
+    kd = torch.from_numpy(np.ascontiguousarray(k_np).view(np.int16)).to(dev)
+    flat = sp.specprefill_score(qd, kd, od, params)
+    same = bool(int(flat.n_kept.item()) == nk and torch.equal(flat.kept_idx[:nk], kv_out.kept_idx[:nk]))
+    res = {"what": f"random-weight draft (hidden {shape_d.hidden}, QK-norm, RoPE on {shape_d.rotary_dim} of "
+                   f"{shape_d.head_dim} dims), cache in 16-token blocks scored in place",
+           "ms_per_step": d_ms, "value": world * ntot / (d_ms / 1e3), "unit": UNIT, "kept_tokens": nk,
+           "device_status": sp.device_status(kv_ws), "same_kept_as_dense": same,
+           "fixture_build_s": build_s}
+    del pools, kd
     torch.cuda.empty_cache()
     return res
 
