@@ -61,8 +61,8 @@ ALL_LEGS = ("e2e", "pipelined", "importance", "listing", "head_pool", "paged", "
 # DRAM bytes (read + write) of one logits-kernel launch per workload, from an
 # ncu application-replay capture of this bench's own calls; reported only
 # while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "a9ae8b8b5b7868ffbac52202f1eb1c3d87ec713e",
-           "bytes_per_launch": {"draft2b": 202212608}}
+TRAFFIC = {"source_sha1": "d43cc97e7f72ea0eba637d40ec86af769eebe21c",
+           "bytes_per_launch": {"draft2b": 203495552}}
 
 
 def parse(argv=None):
@@ -83,6 +83,9 @@ def parse(argv=None):
                     help="comma-separated legs to run beside the headline (or 'none')")
     ap.add_argument("--copies", type=int, default=0,
                     help="rotating copies of the inputs (0: enough to exceed the L2)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prompt length of a single-prompt workload (a smaller case of the same "
+                         "kernels, e.g. for a profiler capture); 0 keeps the workload's")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -232,9 +235,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def make_inputs(name):
+def make_inputs(name, tokens=0):
     from tests.gpu_helpers import workload_inputs
-    return workload_inputs(name)
+    if not tokens:
+        return workload_inputs(name)
+    from synth import get_workload, make_inputs as draw
+    w = get_workload(name)
+    if w.n_prompts != 1:
+        raise SystemExit("--tokens applies to single-prompt workloads")
+    w = w.with_(lengths=(int(tokens),))
+    return w, draw(w)
 
 
 def oracle_rate(w, inp, budget_s, max_runs=3):
@@ -362,7 +372,7 @@ def run_ours(args, rank, world, local):
     _build.build()
     sp.load()
     legs = set() if args.legs == "none" else set(args.legs.split(","))
-    w, inp = make_inputs(args.workload)
+    w, inp = make_inputs(args.workload, args.tokens)
     params = sp.SelectionParams(**w.selection_kwargs())
     ntot = inp.n_tokens_total
     q_np = np.ascontiguousarray(inp.q).view(np.int16)

@@ -145,6 +145,12 @@ typedef struct sp_params {
     int32_t min_tok;           /* SP_RULE_LISTING: >= 0 (128), bound of eff_min */
     int32_t max_keep;          /* SP_RULE_LISTING: >= 0 (2000 in the pages' tool); 0 = no cap */
     int32_t pool_at;           /* SP_POOL_TOKEN (0) or SP_POOL_HEAD */
+    int32_t wave_mib;          /* >= 0; 0 selects the default (2048). The logits
+                                  of all slabs are kept in the workspace between
+                                  the two passes of the softmax; when they need
+                                  more than this many MiB the slabs are scored in
+                                  waves that each fit it (smaller workspace, one
+                                  more pair of kernels per wave) */
 } sp_params;
 
 /* Optional profiling hook: when non-null, `logits_start`/`logits_stop` are

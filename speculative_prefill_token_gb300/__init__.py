@@ -81,7 +81,7 @@ class _Params(ctypes.Structure):
                 ("force_last_chunk", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("spin_limit", ctypes.c_int32), ("rule", ctypes.c_int32),
                 ("min_tok", ctypes.c_int32), ("max_keep", ctypes.c_int32),
-                ("pool_at", ctypes.c_int32)]
+                ("pool_at", ctypes.c_int32), ("wave_mib", ctypes.c_int32)]
 
 
 class _KvSource(ctypes.Structure):
@@ -102,7 +102,9 @@ class SelectionParams:
     tokens {0,1,2,3,n-2,n-1}, fill to min(min_tok, max(4, n/10)), cap to
     max_keep tokens when max_keep > 0). pool_at "head" pools every attention
     row before the max over heads and layers instead of the per-token
-    importance."""
+    importance. wave_mib (0: the library's default) bounds the logits
+    scratch of one wave in MiB; larger batches are scored in several
+    waves."""
     pool_w: int = 13
     chunk: int = 32
     mode: str = "mass"
@@ -121,6 +123,7 @@ class SelectionParams:
     min_tok: int = 128
     max_keep: int = 0
     pool_at: str = "token"
+    wave_mib: int = 0
 
     def _c(self) -> _Params:
         return _Params(int(self.pool_w), int(self.chunk), MODES[self.mode], float(self.keep_p),
@@ -128,7 +131,7 @@ class SelectionParams:
                        int(self.boost_first_n), float(self.boost_last_mult), int(self.boost_last_n),
                        int(bool(self.force_bos)), int(bool(self.force_last_chunk)),
                        float(self.scale), int(self.spin_limit), RULES[self.rule],
-                       int(self.min_tok), int(self.max_keep), POOL_AT[self.pool_at])
+                       int(self.min_tok), int(self.max_keep), POOL_AT[self.pool_at], int(self.wave_mib))
 
 
 _lib = None

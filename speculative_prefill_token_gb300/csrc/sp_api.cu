@@ -13,12 +13,14 @@
 namespace sp {
 namespace {
 
-// Scratch budget of one wave of slabs (quantised logits): most of the 129 MB
-// L2 of a GB300 (the key stream is loaded evict-first), so the logits written
-// by one wave are still resident when the importance kernel of the same wave
-// reads them, with as few waves (logits kernel tails and importance kernels
-// between them) as that allows.
-constexpr int64_t kWaveScratchBytes = int64_t(112) << 20;
+// Default scratch budget of one wave of slabs (quantised logits), unless
+// sp_params.wave_mib sets one. Every wave adds a logits-kernel tail and an
+// importance kernel between the key streams; measured on GB300, one wave
+// whose scratch spills from L2 to HBM (written once, read once) beats two
+// L2-sized waves: 258 instead of 295 us per call on the 131K-token d = 128
+// workload, 252 instead of 270 on the 16-prompt serving batch; 25 MB for
+// the 32K-token 2B workload stays in L2.
+constexpr int64_t kWaveScratchBytes = int64_t(2048) << 20;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -67,6 +69,7 @@ int check_params(const sp_params* p) {
         return SP_ERR_INVALID_ARG;
     if (p->pool_at != SP_POOL_TOKEN && p->pool_at != SP_POOL_HEAD) return SP_ERR_INVALID_ARG;
     if (p->pool_at == SP_POOL_HEAD && p->pool_w / 2 > 64) return SP_ERR_UNSUPPORTED;
+    if (p->wave_mib < 0) return SP_ERR_INVALID_ARG;
     return SP_OK;
 }
 
@@ -121,7 +124,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     while (P.sort_cap < maxnc) P.sort_cap <<= 1;
     // quantised logits (2 bytes) plus one fp32 maximum per warp quarter and row
     const int64_t per_slab = (P.tiles_max * kTileTokens) * P.Rs * 2 + P.tiles_max * 4 * P.Rs * 4;
-    int64_t spw = kWaveScratchBytes / per_slab;
+    const int64_t budget = p->wave_mib > 0 ? static_cast<int64_t>(p->wave_mib) << 20 : kWaveScratchBytes;
+    int64_t spw = budget / per_slab;
     if (spw < 1) spw = 1;
     if (spw > P.slabs) spw = P.slabs;
     {   // the fewest waves the budget allows, of equal size

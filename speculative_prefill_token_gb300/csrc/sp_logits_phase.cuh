@@ -728,10 +728,14 @@ __device__ __forceinline__ void logits_phase(const LogitsCtx& c, const TcArgs& a
                         v[hh][r + u + 1] = valid ? exp2_ftz(__fmul_rn(d1, -kLogitQuantInv)) : 0.0f;
                     }
                 }
+                // the staging buffer has the TMA 64-byte swizzle: 16-byte chunk c
+                // of row tl sits at chunk c ^ ((tl >> 1) & 3), so the eight
+                // lanes of each store phase hit distinct banks
                 uint4* row = reinterpret_cast<uint4*>(out_buf + hh * kStageOutBytes + tl * 64);
+                const int sw = (tl >> 1) & 3;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
-                    row[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                    row[c4 ^ sw] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
                 // lane r: this tile's (M, sum) of row hh * 32 + r, merged into the running pair
                 const float z = warp_rows_reduce<false>(v[hh]);
                 run[hh] = merge_partial(run[hh], make_float2(m_own[hh], z));

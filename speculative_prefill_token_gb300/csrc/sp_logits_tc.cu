@@ -161,7 +161,8 @@ cudaError_t make_logits_maps(const Plan& pl, const sp_shape* s, const uint16_t* 
     }
     {
         // quantised logits scratch: dims (row value, tile slot row, slab); box = 32
-        // values x 128 rows, staged densely (64-byte rows)
+        // values x 128 rows, staged as 64-byte rows with the 64-byte swizzle
+        // (conflict-free staging stores; the global layout is dense)
         const uint64_t rows = static_cast<uint64_t>(pl.tiles_max) * kTileTokens;
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(pl.Rs), rows, static_cast<cuuint64_t>(nslab)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(pl.Rs) * 2,
@@ -169,7 +170,7 @@ cudaError_t make_logits_maps(const Plan& pl, const sp_shape* s, const uint16_t* 
         cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTileTokens), 1};
         cuuint32_t es[3] = {1, 1, 1};
         if (enc(&m->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, ws_ptr<uint16_t>(ws, pl.o_logits), dims,
-                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }

@@ -317,3 +317,18 @@ def test_noalloc_rejects_an_oversized_batch_before_any_launch(lib):
     ok = sp.token_shape(4, 4096)
     assert lib.sp_pool_chunk_noalloc(ctypes.byref(ok), ctypes.byref(p), a, a, None, a, a, None,
                                      None) == 1
+
+
+def test_wave_budget_parameter(lib):
+    """sp_params.wave_mib bounds one wave's logits scratch: the default keeps
+    a 65K-token, 16-slab batch in one wave, 80 MiB splits it in two (one
+    more logits and importance kernel), a negative budget is invalid."""
+    s = _shape(n_seqs=1, n_layers=4, n_q_heads=16, n_kv_heads=4, head_dim=64, n_lookahead=16,
+               n_tokens_total=65536)
+    assert sp.kernels_per_call(s, sp.SelectionParams()) == 6
+    assert sp.kernels_per_call(s, sp.SelectionParams(wave_mib=80)) == 8
+    rc, small = _ws(s, sp.SelectionParams(wave_mib=80))
+    rc0, big = _ws(s, sp.SelectionParams())
+    assert rc == rc0 == 0 and small < big
+    rc, _ = _ws(s, sp.SelectionParams(wave_mib=-1))
+    assert rc == 1

@@ -36,15 +36,15 @@ def test_head_pooling_matches_oracle(cuda_lib, case):
 
 
 def test_head_pooling_two_waves_and_64_rows(cuda_lib):
-    """64 query rows per slab (L = 16, G = 4) and 16 slabs of 65K tokens:
-    the scratch takes two waves, so the per-token maxima of the first wave
-    are carried to the second."""
+    """64 query rows per slab (L = 16, G = 4) and 16 slabs of 65K tokens
+    with an 80 MiB wave budget: the scratch takes two waves, so the
+    per-token maxima of the first wave are carried to the second."""
     sp = cuda_lib
     lengths = [40000, 25536]
     q, k, off = random_case(643, lengths, 4, 16, 4, 64, 16, q_gain=2.0)
     kw = dict(BASE, pool_at="head", mode="fixed", keep_p=0.25)
-    got, (qd, kd, _) = _run(cuda_lib, q, k, off, kw)
-    assert sp.kernels_per_call(sp.shape_of(qd, kd), sp.SelectionParams(**kw)) > 6   # > 1 wave
+    got, (qd, kd, _) = _run(cuda_lib, q, k, off, dict(kw, wave_mib=80))
+    assert sp.kernels_per_call(sp.shape_of(qd, kd), sp.SelectionParams(**kw, wave_mib=80)) == 8   # 2 waves
     ref = oracle.run(q, k, off, **kw)
     _check_scores(got, ref)
     _check_t1(got, off, kw)

@@ -56,14 +56,15 @@ def test_fused_post_pooling_equals_the_staged_kernels(cuda_lib, case):
 
 
 def test_token_pooling_after_a_first_wave(cuda_lib):
-    """16 slabs of 64 rows over 65K tokens take two waves: the second
-    wave's importance kernel combines the first wave's per-token maxima."""
+    """16 slabs of 64 rows over 65K tokens take two waves with an 80 MiB
+    wave budget: the second wave's importance kernel combines the first
+    wave's per-token maxima."""
     sp = cuda_lib
     lengths = [40000, 25536]
     q, k, off = random_case(643, lengths, 4, 16, 4, 64, 16, q_gain=2.0)
     kw = dict(BASE, mode="fixed", keep_p=0.25, pool_w=129)
-    got, (qd, kd, od) = _run(cuda_lib, q, k, off, kw)
-    p = sp.SelectionParams(**kw)
+    got, (qd, kd, od) = _run(cuda_lib, q, k, off, dict(kw, wave_mib=80))
+    p = sp.SelectionParams(**kw, wave_mib=80)
     assert sp.kernels_per_call(sp.shape_of(qd, kd), p) == 8   # prep, 2 x (logits, importance), pool sums, rank, gather
     imp, tok = _staged(sp, qd, kd, od, p, int(off[-1]))
     assert np.array_equal(got["imp"], imp)
