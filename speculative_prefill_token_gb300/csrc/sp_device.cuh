@@ -12,8 +12,11 @@ namespace sp {
 // earlier in the stream is complete too); without the launch attribute it
 // returns at once. grid_dep_launch() lets the next kernel of the stream be
 // scheduled: its CTAs may become resident early and then block in their own
-// grid_dep_wait(). Every kernel of this library calls both before its first
-// global-memory access.
+// grid_dep_wait(). Every kernel of this library calls grid_dep_wait() before
+// its first global-memory access; the prep and the last kernels of a call
+// release their successor at once, the logits, importance, pool and rank
+// kernels do not (measured faster: an early-released successor parks its
+// CTAs on the SMs that free up first).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

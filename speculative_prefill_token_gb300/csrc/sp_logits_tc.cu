@@ -21,8 +21,11 @@ namespace {
 // offsets: the call's inputs (seq_off, Q, K) were complete before the prep
 // kernel passed its own wait, so the producer and MMA warps start at once
 // and only the epilogue waits for the prep kernel's counters; larger
-// batches wait for the prep kernel's offsets. The dependent kernel may
-// launch from here on.
+// batches wait for the prep kernel's offsets. The kernel does not release
+// its dependent early: the importance kernel then launches once this one
+// has completed and spreads over every SM, instead of piling its CTAs onto
+// the SMs this kernel frees first (2B workload 66.7 -> 65.8 us per call,
+// 0.8B workload 39.4 -> 36.1 us).
 // A single prompt with keys that are not block-paged takes its offsets from
 // Ntot ({0, Ntot}; the prep kernel rejects anything else and the scores of
 // such a call are never used), so the producer starts right after the
@@ -56,7 +59,6 @@ __device__ __forceinline__ int64_t logits_start(const LogitsCtx& c, const TcArgs
         *so = a.seq_off;
         *epi_wait = 0;
     }
-    grid_dep_launch();
     return T;
 }
 

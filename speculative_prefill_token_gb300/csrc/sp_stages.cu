@@ -154,8 +154,7 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
     const int32_t* tile_base, float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab,
     int64_t Ntot, int64_t rows_per_slab, int64_t tiles_max, int first_wave, int last_wave,
     const int32_t* bad) {
-    grid_dep_wait();
-    grid_dep_launch();
+    grid_dep_wait();   // no early release: the pool kernel spreads over every SM once this one ends
     const int Q8 = Rs / 8;
     const int TOK = kReduceThreads / Q8;
     const int subs = kTileTokens / TOK;
@@ -261,8 +260,7 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
 // --------------------------------------------------------- pool + chunk sums
 // Fused-path pooling: one CTA per 128-token tile of a prompt (pool_tile).
 __global__ void __launch_bounds__(kPoolThreads) pool_sums_kernel(const PoolArgs a, const int32_t* bad) {
-    grid_dep_wait();
-    grid_dep_launch();
+    grid_dep_wait();   // no early release (see the rank kernel)
     const int64_t tile = blockIdx.x;
     __shared__ PoolShared sh;
     if (a.B == 1) {  // pool_tile reads the flag after requesting the window
