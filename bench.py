@@ -61,7 +61,7 @@ ALL_LEGS = ("e2e", "pipelined", "importance", "listing", "head_pool", "paged", "
 # DRAM bytes (read + write) of one logits-kernel launch per workload, from an
 # ncu application-replay capture of this bench's own calls; reported only
 # while the kernel sources are the ones that were measured.
-TRAFFIC = {"source_sha1": "d9dcd9a4c039069f131ef87363e4c30ea1487060",
+TRAFFIC = {"source_sha1": "8bf309972040bef76a132f716bd97e9ee950c555",
            "bytes_per_launch": {"draft2b": 204010496}}
 
 

@@ -13,10 +13,11 @@ namespace sp {
 // returns at once. grid_dep_launch() lets the next kernel of the stream be
 // scheduled: its CTAs may become resident early and then block in their own
 // grid_dep_wait(). Every kernel of this library calls grid_dep_wait() before
-// its first global-memory access; the prep and the last kernels of a call
-// release their successor at once, the logits, importance, pool and rank
-// kernels do not (measured faster: an early-released successor parks its
-// CTAs on the SMs that free up first).
+// its first global-memory access. In the fused call only the prep kernel
+// releases its successor at once (the logits kernel then sets up its TMEM,
+// barriers and tensor maps under the prep kernel's tail); the logits,
+// importance, pool, rank and gather kernels do not (measured faster: an
+// early-released successor parks its CTAs on the SMs that free up first).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -71,8 +71,9 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
 
 // One CTA per slice, plus one past the last slice for the totals.
 __global__ void __launch_bounds__(kRankThreads) gather_kernel(const PostArgs a) {
+    // no early release either: its successor is the next call's prep kernel
+    // (2B workload 64.1 -> 63.5 us per call, 0.8B 35.3 -> 35.2)
     grid_dep_wait();
-    grid_dep_launch();
     __shared__ RankShared sh;
     const int64_t s = blockIdx.x;
     if (a.B == 1) {  // gather_slice reads the flag after requesting its inputs
