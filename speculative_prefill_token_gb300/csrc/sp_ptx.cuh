@@ -118,11 +118,12 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, uint
 }
 
 // Shared -> global tensor store (bulk-group completion).
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2,
+                                             uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
-        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
 }
 
