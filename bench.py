@@ -266,7 +266,7 @@ def oracle_sample_main(args):
     """Child process of cpu_baseline: the oracle with the thread count the
     parent set in the environment; prints one JSON line."""
     w, inp = make_inputs(args.workload)
-    rate, runs, el = oracle_rate(w, inp, budget_s=15.0, max_runs=1)
+    rate, runs, el = oracle_rate(w, inp, budget_s=10.0, max_runs=100)
     print(json.dumps({"value": rate, "runs": runs, "seconds": el}), flush=True)
 
 
@@ -289,11 +289,12 @@ def cpu_baseline(w, inp):
     """The float64 oracle as it stands on the host cores: all cores (BLAS
     threads = host cores, in this process) and one thread (a child process
     with the BLAS thread count set to 1), each on the full workload."""
-    rate, runs, el = oracle_rate(w, inp, budget_s=15.0)
+    rate, runs, el = oracle_rate(w, inp, budget_s=10.0, max_runs=100)
     one = single_thread_rate(w.name)
     return {"value": rate, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"full {w.name} workload (N={inp.n_tokens_total}) x{runs}, numpy float64, "
-                      f"BLAS threads = host cores, {el:.1f} s; single-thread: one full call",
+                      f"BLAS threads = host cores, {el:.1f} s; single-thread: "
+                      f"x{one.get('runs')}, {one.get('seconds') or 0:.1f} s",
             "single_thread": {"value": one.get("value"), "unit": UNIT, "cores": 1,
                               "seconds": one.get("seconds"), "error": one.get("error")}}
 
