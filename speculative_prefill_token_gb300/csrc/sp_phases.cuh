@@ -452,7 +452,26 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         acc[q] = 0;
     }
     if (!all) {
-        for (int j = lane; j < static_cast<int>(nc); j += 32) {
+        // four scores are read before they are compared, so that the shared-
+        // memory latency of one overlaps the comparisons of the others (the
+        // scan is latency-bound: long workload 7.5 us per CTA with one read in
+        // flight)
+        const int nci = static_cast<int>(nc);
+        int j = lane;
+        for (; j + 96 < nci; j += 128) {
+            float sj[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sj[u] = cs_s[j + 32 * u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint64_t kj =
+                    ((static_cast<uint64_t>(score_desc_key(sj[u])) << 32) | static_cast<uint32_t>(j + 32 * u)) & kmask;
+                const uint64_t wj = is_mass ? fixed_point(sj[u], S) : 1u;
+#pragma unroll
+                for (int q = 0; q < kWarpChunks; ++q) acc[q] += kj < ki[q] ? wj : 0u;
+            }
+        }
+        for (; j < nci; j += 32) {
             const float sj = cs_s[j];
             const uint64_t kj = ((static_cast<uint64_t>(score_desc_key(sj)) << 32) | static_cast<uint32_t>(j)) & kmask;
             const uint64_t wj = is_mass ? fixed_point(sj, S) : 1u;
