@@ -360,6 +360,22 @@ class Timer:
         return t0.elapsed_time(t1), host
 
 
+def max_over_ranks(values, world, device):
+    """The element-wise maximum over the ranks of per-rank timings (ms):
+    every rank gets it (one all-reduce; a single rank keeps its own)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(world, ntot, steps, elapsed_ms):
+    """Tokens per second of the whole job: every replica scores ntot tokens
+    per step, and the slowest rank's timed region sets the time."""
+    return world * ntot * steps / (elapsed_ms / 1e3)
+
+
 def run_ours(args, rank, world, local):
     import torch
     import speculative_prefill_token_gb300 as sp
@@ -444,16 +460,13 @@ def run_ours(args, rank, world, local):
         e2e_ms, h2d, d2h = float("nan"), 0, 0
 
     # max over ranks of the timed regions
-    times = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = float(times[0]), float(times[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
-    value = world * ntot * args.steps / (elapsed_ms / 1e3)
+    value = whole_job_rate(world, ntot, args.steps, elapsed_ms)
     peak, peak_kind = measured_peaks()
     avg_logits_s = statistics.mean(logits_ms) / 1e3
     achieved = k_bytes / avg_logits_s / 1e9
