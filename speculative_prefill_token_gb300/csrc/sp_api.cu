@@ -154,8 +154,8 @@ int make_plan(const sp_shape* s, const sp_params* p, Plan* pl) {
     P.o_chunk_off = take(B1 * 4);
     P.o_pblk_base = take(B1 * 4);
     P.o_slice_base = take(B1 * 4);
-    P.o_scount = take(static_cast<size_t>(P.slices_max) * 4);
-    P.o_ucount = take(static_cast<size_t>(P.slices_max) * 4);
+    P.o_scount = take(static_cast<size_t>(P.slices_max) * kRankSplitMax * 4);
+    P.o_ucount = take(static_cast<size_t>(P.slices_max) * kRankSplitMax * 4);
     // per-segment record counters, then the listing rule's per-prompt
     // kept counts: one range, zeroed by the prep kernel on every call
     P.o_segcnt = take((static_cast<size_t>(P.slabs_per_wave) + 1) * P.B * 4);

@@ -18,7 +18,8 @@ constexpr int kMaxKvLayers = 64;    // per-layer key pools (one tensor map each,
 constexpr int kMaxChunk = 8192;
 constexpr int kMaxPool = 8191;
 constexpr int kMaxPromptChunks = 16384;  // per-prompt chunk count the in-CTA selection handles
-constexpr int kSliceChunks = 32;         // chunks per CTA of the fused rank / gather kernels
+constexpr int kSliceChunks = 32;         // chunks per CTA of the fused gather kernels
+constexpr int kRankSplitMax = 4;        // rank CTAs per slice at most (each ranks kSliceChunks / split chunks)
 constexpr int64_t kDefaultSpin = int64_t(1) << 22;  // ~4 s of polls with a 1 us suspend hint
 
 // Workspace header (first 256 bytes of every workspace).

@@ -257,7 +257,6 @@ __device__ __forceinline__ void pool_tile(const PoolArgs& a, int64_t tile, int t
 // ------------------------------------------------------ rank and gather
 constexpr int kRankThreads = 256;
 constexpr int kRankWarps = kRankThreads / 32;
-constexpr int kWarpChunks = kSliceChunks / kRankWarps;  // chunks ranked by each warp
 static_assert(kSliceChunks == 32, "the gather scan uses one lane per chunk of a slice");
 
 struct PostArgs {
@@ -279,13 +278,14 @@ struct PostArgs {
     WsHeader* hdr;
     int B, C, mode, normalize, force_bos, force_last;
     int rule, min_tok, max_keep;
+    int rank_split;             // rank CTAs per slice (1 or kRankSplitMax); scount / ucount per part
     int64_t Ntot;
     float keep_p, mass;
 };
 
 struct RankShared {
     float red_mn[kRankWarps], red_mx[kRankWarps], red_sm[kRankWarps];
-    unsigned long long red_u[kRankWarps];
+    unsigned long long red_u[kRankWarps], red_acc[kRankWarps];
     int32_t warp_cnt[kRankWarps], warp_spare[kRankWarps];
     int64_t red[kRankWarps];
     int64_t base[kSliceChunks];
@@ -294,23 +294,27 @@ struct RankShared {
 
 __device__ __forceinline__ int64_t chunk_tokens(int64_t n, int C, int64_t c) { return min64(C, n - c * C); }
 
-// Slice s (< number of slices) by kRankThreads threads; cs_s holds room for
+// Part `piece` (< SPLIT) of slice s (< number of slices) by kRankThreads
+// threads: the part's kSliceChunks / SPLIT chunks, each warp ranking one or
+// more of them over all or part of the prompt's chunks; cs_s holds room for
 // the prompt's chunk scores (kMaxPromptChunks floats at most).
 //
 // Rebuilds every chunk score of the prompt (the min-max normalisation is
 // affine, so the chunk mean comes from the pool kernel's sums) and decides
-// the slice's chunks by their position in the order (score descending,
+// the part's chunks by their position in the order (score descending,
 // chunk index ascending): fixed mode keeps a chunk when fewer than
 // k = max(1, ceil(nc p)) chunks precede it, mass mode when the exact
 // fixed-point sum of the scores preceding it is below ceil(mass * total)
 // (the shortest prefix that reaches the mass, crossing chunk included).
 // The final chunk is forced. Writes the chunk scores, keep flags and the
-// slice's kept-token count (chunk 0 counts its BOS token when it is not
-// selected). The set equals that of the radix selection behind sp_select.
+// part's kept-token count (chunk 0 counts its BOS token when it is not
+// selected) at scount[s * SPLIT + piece]. The set equals that of the
+// radix selection behind sp_select.
 // The slice is located by loc (slice_base; aux seq_off, chunk_off,
 // tile_base). With bad1 (single prompt, see one_prompt) the chunk sums and
 // tile extrema are requested before the flag is read.
-__device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, GroupBar g,
+template <int SPLIT>
+__device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int piece, int t, GroupBar g,
                                            float* cs_s, RankShared& sh, const Located<3>& loc,
                                            const int32_t* bad1) {
     const int lane = t & 31, warp = t >> 5;
@@ -322,13 +326,26 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         // reported; the slice keeps nothing so that the gather stays in bounds
         if (t == 0) {
             atomicCAS(&a.hdr->status, 0, static_cast<int>(SP_ERR_DEVICE));
-            a.scount[s] = 0;
-            a.ucount[s] = 0;
+            a.scount[s * SPLIT + piece] = 0;
+            a.ucount[s * SPLIT + piece] = 0;
         }
         return;
     }
-    const int64_t c_lo = (s - loc.base_b) * kSliceChunks;
-    const int64_t c_hi = min64(nc, c_lo + kSliceChunks);
+    constexpr int kPart = kSliceChunks / SPLIT;                             // chunks of the part
+    constexpr int kWarpQ = kPart > kRankWarps ? kPart / kRankWarps : 1;     // chunks per warp
+    constexpr int kChunkW = kPart < kRankWarps ? kRankWarps / kPart : 1;    // warps per chunk
+    constexpr int kLanesQ = kPart / kWarpQ;                                 // warps before a warp's next chunk
+    static_assert(kPart * SPLIT == kSliceChunks && kLanesQ * kChunkW == kRankWarps,
+                  "a rank CTA's warps split its chunks evenly");
+    const int64_t c_lo = (s - loc.base_b) * kSliceChunks + piece * kPart;
+    const int64_t c_hi = min64(nc, c_lo + kPart);
+    if (c_lo >= c_hi) {  // past the prompt's last chunk: no chunks, no tokens
+        if (t == 0) {
+            a.scount[s * SPLIT + piece] = 0;
+            a.ucount[s * SPLIT + piece] = 0;
+        }
+        return;
+    }
 
     // each thread's first chunk sums and up to four tile min / max pairs are
     // requested together (one round trip); larger prompts loop (four pairs:
@@ -432,20 +449,22 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
     // is no longer than its smallest kept count
     if (listing && ((!is_mass && a.keep_p >= 1.0f) || n <= listing_eff_min(n, a.min_tok))) all = true;
 
-    // warp w ranks chunks c_lo + w + kRankWarps * q of the slice: the count
-    // (fixed) or fixed-point mass (mass mode) of the chunks ordered before
-    // it. The order key (descending score, ascending index) is one 64-bit
-    // integer so that the comparison is branch-free. The listing rule's
-    // fixed mode counts only chunks with a strictly larger score (the index
-    // half of the key is masked off), so every chunk tied with the k-th
-    // score is kept.
+    // warp w ranks chunks c_lo + w % kLanesQ + kLanesQ * q (q < kWarpQ) of
+    // the part over every kChunkW-th group of 32 chunks of the prompt: the
+    // count (fixed) or fixed-point mass (mass mode) of the chunks ordered
+    // before it; the kChunkW warps of one chunk add their sums. The order
+    // key (descending score, ascending index) is one 64-bit integer so that
+    // the comparison is branch-free. The listing rule's fixed mode counts
+    // only chunks with a strictly larger score (the index half of the key is
+    // masked off), so every chunk tied with the k-th score is kept.
     const uint64_t kmask = (listing && !is_mass) ? 0xffffffff00000000ull : ~0ull;
-    int64_t ci[kWarpChunks];
-    uint64_t ki[kWarpChunks];
-    uint64_t acc[kWarpChunks];
+    const int wq = warp % kLanesQ, wp = warp / kLanesQ;
+    int64_t ci[kWarpQ];
+    uint64_t ki[kWarpQ];
+    uint64_t acc[kWarpQ];
 #pragma unroll
-    for (int q = 0; q < kWarpChunks; ++q) {
-        ci[q] = c_lo + warp + kRankWarps * q;
+    for (int q = 0; q < kWarpQ; ++q) {
+        ci[q] = c_lo + wq + kLanesQ * q;
         ki[q] = ci[q] < c_hi ? ((static_cast<uint64_t>(score_desc_key(cs_s[ci[q]])) << 32) |
                                 static_cast<uint32_t>(ci[q])) & kmask
                              : 0u;
@@ -456,38 +475,45 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
         // memory latency of one overlaps the comparisons of the others (the
         // scan is latency-bound: long workload 7.5 us per CTA with one read in
         // flight)
+        constexpr int kStep = 32 * kChunkW;
         const int nci = static_cast<int>(nc);
-        int j = lane;
-        for (; j + 96 < nci; j += 128) {
+        int j = lane + 32 * wp;
+        for (; j + 3 * kStep < nci; j += 4 * kStep) {
             float sj[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) sj[u] = cs_s[j + 32 * u];
+            for (int u = 0; u < 4; ++u) sj[u] = cs_s[j + kStep * u];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint64_t kj =
-                    ((static_cast<uint64_t>(score_desc_key(sj[u])) << 32) | static_cast<uint32_t>(j + 32 * u)) & kmask;
+                    ((static_cast<uint64_t>(score_desc_key(sj[u])) << 32) | static_cast<uint32_t>(j + kStep * u)) & kmask;
                 const uint64_t wj = is_mass ? fixed_point(sj[u], S) : 1u;
 #pragma unroll
-                for (int q = 0; q < kWarpChunks; ++q) acc[q] += kj < ki[q] ? wj : 0u;
+                for (int q = 0; q < kWarpQ; ++q) acc[q] += kj < ki[q] ? wj : 0u;
             }
         }
-        for (; j < nci; j += 32) {
+        for (; j < nci; j += kStep) {
             const float sj = cs_s[j];
             const uint64_t kj = ((static_cast<uint64_t>(score_desc_key(sj)) << 32) | static_cast<uint32_t>(j)) & kmask;
             const uint64_t wj = is_mass ? fixed_point(sj, S) : 1u;
 #pragma unroll
-            for (int q = 0; q < kWarpChunks; ++q) acc[q] += kj < ki[q] ? wj : 0u;
+            for (int q = 0; q < kWarpQ; ++q) acc[q] += kj < ki[q] ? wj : 0u;
         }
 #pragma unroll
-        for (int q = 0; q < kWarpChunks; ++q)
+        for (int q = 0; q < kWarpQ; ++q)
             for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+    }
+    if (kChunkW > 1) {  // then kWarpQ = 1
+        if (lane == 0) sh.red_acc[warp] = acc[0];
+        g.sync();
+        acc[0] = 0;
+        for (int p = 0; p < kChunkW; ++p) acc[0] += sh.red_acc[wq + p * kLanesQ];
     }
     if (lane == 0) {
         int32_t my_cnt = 0, my_spare = 0;
 #pragma unroll
-        for (int q = 0; q < kWarpChunks; ++q) {
+        for (int q = 0; q < kWarpQ; ++q) {
             const int64_t c = ci[q];
-            if (c >= c_hi) continue;
+            if (wp != 0 || c >= c_hi) continue;
             // fixed: fewer than k chunks before it; mass: mass before it below the threshold
             uint8_t f = (all || acc[q] < need) ? 1 : 0;
             if (!listing && a.force_last && c == nc - 1) f |= 2;
@@ -504,11 +530,11 @@ __device__ __forceinline__ void rank_slice(const PostArgs& a, int64_t s, int t, 
     if (t == 0) {
         int32_t tot = 0;
         for (int w = 0; w < kRankWarps; ++w) tot += sh.warp_cnt[w];
-        a.scount[s] = tot;
+        a.scount[s * SPLIT + piece] = tot;
         if (listing) {
             int32_t spare = 0;
             for (int w = 0; w < kRankWarps; ++w) spare += sh.warp_spare[w];
-            a.ucount[s] = spare;
+            a.ucount[s * SPLIT + piece] = spare;
             atomicAdd(a.lcount + b, tot);
         }
     }
@@ -537,7 +563,7 @@ __device__ __forceinline__ void gather_slice(const PostArgs& a, int64_t s, int t
     if (bad1 && warp == 0 && s < S && (s - sb) * kSliceChunks + lane < nc)
         f1 = __ldcg(a.keep + coff + (s - sb) * kSliceChunks + lane);
     int64_t part = 0;
-    for (int64_t i = t; i < s; i += kRankThreads) part += __ldcg(a.scount + i);
+    for (int64_t i = t; i < s * a.rank_split; i += kRankThreads) part += __ldcg(a.scount + i);
     if (bad1 && *bad1) return;
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) sh.red[warp] = part;

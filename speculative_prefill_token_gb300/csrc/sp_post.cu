@@ -3,9 +3,10 @@
 // "Speculative prefill" §Approach item 3), their per-tile min / max and the
 // per-chunk sums of boost * x and boost.
 //
-// Both kernels run one CTA per slice of kSliceChunks consecutive chunks of a
-// prompt, so a long prompt is spread over many SMs (the per-slice code is in
-// sp_phases.cuh):
+// The gather kernel runs one CTA per slice of kSliceChunks consecutive
+// chunks of a prompt, the rank kernel one or kRankSplitMax CTAs per slice
+// (each ranks its share of the slice's chunks), so a long prompt is spread
+// over many SMs (the per-slice code is in sp_phases.cuh):
 //
 //   rank    rebuilds every chunk score of the prompt in shared memory --
 //           min-max normalisation over the prompt ("SpecPrefill —
@@ -20,8 +21,8 @@
 //           ceil(mass * total) (guide v3, item 1: the shortest prefix that
 //           reaches the mass, crossing chunk included). The final chunk is
 //           forced (PR §Approach item 4). Writes the chunk scores, the keep
-//           flags and the slice's kept-token count (chunk 0 counts its BOS
-//           token when it is not selected).
+//           flags and the kept-token count of its part of the slice (chunk
+//           0 counts its BOS token when it is not selected).
 //   gather  offsets every slice by the kept tokens of all earlier slices and
 //           writes the kept token indices and original positions (guide
 //           §How It Works / Sparse Prefill) plus the per-prompt offsets.
@@ -43,6 +44,7 @@
 namespace sp {
 namespace {
 
+template <int SPLIT>
 __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
     // no early release: a dependent released early parks its CTAs on the
     // SMs its predecessor frees first; launched at this kernel's end it
@@ -50,7 +52,8 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
     // and pool kernels: 2B workload 66.7 -> 64.1 us per call, 0.8B 39.4 ->
     // 35.2, long 257.8 -> 249.2)
     grid_dep_wait();
-    const int64_t s = blockIdx.x;
+    const int64_t s = blockIdx.x / SPLIT;
+    const int sub = static_cast<int>(blockIdx.x - s * SPLIT);
     extern __shared__ float cs_s[];  // the prompt's chunk scores
     __shared__ RankShared sh;
     if (a.B == 1) {  // rank_slice reads the flag after requesting its inputs
@@ -58,7 +61,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
         const int64_t hi[3] = {a.Ntot, nc, (a.Ntot + kTileTokens - 1) / kTileTokens};
         const Located<3> loc = one_prompt<3>(static_cast<int32_t>((nc + kSliceChunks - 1) / kSliceChunks), hi);
         if (s >= loc.total) return;
-        rank_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, &a.hdr->bad_input);
+        rank_slice<SPLIT>(a, s, sub, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, &a.hdr->bad_input);
         return;
     }
     const int32_t* const aux[3] = {a.seq_off, a.chunk_off, a.tile_base};
@@ -66,7 +69,7 @@ __global__ void __launch_bounds__(kRankThreads) rank_kernel(const PostArgs a) {
     const Located<3> loc = locate<3>(a.slice_base, aux, a.B, s);
     if (bad_v) return;
     if (s >= loc.total) return;
-    rank_slice(a, s, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, nullptr);
+    rank_slice<SPLIT>(a, s, sub, threadIdx.x, GroupBar{1, kRankThreads}, cs_s, sh, loc, nullptr);
 }
 
 // One CTA per slice, plus one past the last slice for the totals.
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const Post
             k0_one = __ldcg(a.lcount);
             if (warp == 0 && s * kSliceChunks + lane < nc1) f_one = __ldcg(a.keep + s * kSliceChunks + lane);
         }
-        for (int64_t i = t; i < s; i += kRankThreads) {
+        for (int64_t i = t; i < s * a.rank_split; i += kRankThreads) {
             part[1] += __ldcg(a.scount + i);
             part[2] += __ldcg(a.ucount + i);
         }
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kRankThreads) listing_gather_kernel(const Post
     // the kept0 / spare tokens of the prompt's slices before this one
     if (!one) {
         for (int bb = t; bb < b; bb += kRankThreads) part[0] += listing_final_count(a, bb);
-        for (int64_t i = sb + t; i < s; i += kRankThreads) {
+        for (int64_t i = sb * a.rank_split + t; i < s * a.rank_split; i += kRankThreads) {
             part[1] += __ldcg(a.scount + i);
             part[2] += __ldcg(a.ucount + i);
         }
@@ -299,22 +302,34 @@ PostArgs post_args(const Plan& pl, const sp_params* p, const int32_t* seq_off, f
     a.rule = p->rule;
     a.min_tok = p->min_tok;
     a.max_keep = p->max_keep;
+    a.rank_split = 1;
     return a;
 }
 
 cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_off,
                         float* chunk_score, uint8_t* keep, int32_t* kept_idx, int32_t* kept_pos,
                         int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st) {
-    const PostArgs a = post_args(pl, p, seq_off, chunk_score, keep, kept_idx, kept_pos, kept_off, n_kept, ws);
+    PostArgs a = post_args(pl, p, seq_off, chunk_score, keep, kept_idx, kept_pos, kept_off, n_kept, ws);
+    // Few slices: kRankSplitMax CTAs per slice, one warp per chunk, so that
+    // the ranking scans run on more SMs (2B workload 63.5 -> 62.9 us per
+    // call, 0.8B 35.3 -> 34.6); with more slices than that fills, every CTA
+    // rebuilding all chunk scores costs more than it saves (long workload
+    // 243.7 -> 251.0), so one CTA ranks the whole slice.
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    a.rank_split = pl.slices_max * kRankSplitMax <= sms ? kRankSplitMax : 1;
+    auto kern = a.rank_split == 1 ? rank_kernel<1> : rank_kernel<kRankSplitMax>;
     // shared memory for the largest prompt's chunk scores
     const int64_t maxnc = pl.chunks_max < kMaxPromptChunks ? pl.chunks_max : kMaxPromptChunks;
     const size_t smem = static_cast<size_t>(maxnc) * sizeof(float);
     if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    const cudaError_t e = launch_k(rank_kernel, static_cast<unsigned>(pl.slices_max), kRankThreads, smem, st, a);
+    const cudaError_t e =
+        launch_k(kern, static_cast<unsigned>(pl.slices_max * a.rank_split), kRankThreads, smem, st, a);
     if (e != cudaSuccess) return e;
     if (p->rule == SP_RULE_LISTING)
         return launch_k(listing_gather_kernel, static_cast<unsigned>(pl.slices_max + 1), kRankThreads, 0, st, a);
