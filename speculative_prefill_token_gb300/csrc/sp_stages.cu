@@ -141,11 +141,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 // every thread loads its eight 16-bit values of every slab (16 bytes,
 // coalesced) and keeps the max over slabs of
 // y - lse2 = (M - lse2) - q / kLogitQuant, the log2 softmax probability,
-// with M - lse2 taken from a per-CTA table [warp quarter][slab][row]. One
-// thread per token then takes the max over the G heads of each lookahead
-// step, combines it with earlier waves, and (last wave) writes
-// imp[t] = (1/L) sum_l exp2(max over layers, heads). Small CTAs (eight per
-// SM) spread a wave over every SM that the logits kernel frees.
+// with M - lse2 taken from a per-CTA table [warp quarter][slab][row]. The
+// max over the G heads of each lookahead step is then combined with earlier
+// waves and (last wave) imp[t] = (1/L) sum_l exp2(max over layers, heads)
+// written: when G divides 8, by the token's own threads from registers
+// (their partial sums added by shuffles; 2B workload 62.6 -> 62.1 us per
+// call, 0.8B 34.7 -> 33.9, serving batch 240.8 -> 238.5), else by one
+// thread per token through shared memory. Small CTAs (eight per SM) spread
+// a wave over every SM that the logits kernel frees.
 constexpr int kReduceThreads = 128;
 constexpr int kReduceSlabBatch = 4;
 
@@ -234,6 +237,47 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
 #pragma unroll
         for (int u = 0; u < kReduceSlabBatch; ++u)
             if (act && s1 + u < nslab) v[u] = __ldcs(src + (s1 + u) * slab_stride);
+    }
+    if (8 % G == 0) {
+        // each thread's eight rows are 8 / G whole lookahead steps (row =
+        // step * G + head): their head maxima stay in registers, and the
+        // Q8 threads of a token (adjacent lanes) add their terms by shuffles
+        float gm[8];
+        int ng = 0;
+        if (G == 1) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) gm[k] = m[k];
+            ng = 8;
+        } else if (G == 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gm[k] = fmaxf(m[2 * k], m[2 * k + 1]);
+            ng = 4;
+        } else if (G == 4) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) gm[k] = fmaxf(fmaxf(m[4 * k], m[4 * k + 1]), fmaxf(m[4 * k + 2], m[4 * k + 3]));
+            ng = 2;
+        } else {
+            gm[0] = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+            ng = 1;
+        }
+        float part = 0.0f;
+        const int64_t tok = start + first + tq;
+        const int l0 = 8 * c / G;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < ng && act && l0 + k < L) {
+                const int l = l0 + k;
+                float a = gm[k];
+                if (!first_wave) a = fmaxf(a, alog[l * Ntot + tok]);
+                if (last_wave) part += exp2f(a);
+                else alog[l * Ntot + tok] = a;
+            }
+        }
+        if (last_wave) {
+            for (int o = 1; o < Q8; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (act && c == 0) imp[tok] = part / static_cast<float>(L);
+        }
+        return;
     }
     if (act) {
         float* mrow = ms + tq * (Rs + 1) + 8 * c;
