@@ -147,11 +147,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const int32_t* seq_o
 // written: when G divides 8, by the token's own threads from registers
 // (their partial sums added by shuffles; 2B workload 62.6 -> 62.1 us per
 // call, 0.8B 34.7 -> 33.9, serving batch 240.8 -> 238.5), else by one
-// thread per token through shared memory. Small CTAs (eight per SM) spread
-// a wave over every SM that the logits kernel frees.
+// thread per token through shared memory (kFast: the former, a separate
+// instance without the latter's registers, which lets six slabs per thread
+// be in flight without spills: long workload 243.2 -> 241.1, serving 238.3
+// -> 237.3, 2B unchanged). Small CTAs (eight per SM) spread a wave over
+// every SM that the logits kernel frees.
 constexpr int kReduceThreads = 128;
-constexpr int kReduceSlabBatch = 4;
+constexpr int kReduceSlabBatch = 6;
 
+template <bool kFast>
 __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
     const uint16_t* logits, const float* lmax, const float* lse2, const int32_t* seq_off,
     const int32_t* tile_base, float* alog, float* imp, int B, int G, int L, int R, int Rs, int nslab,
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kReduceThreads, 8) reduce_kernel(
         for (int u = 0; u < kReduceSlabBatch; ++u)
             if (act && s1 + u < nslab) v[u] = __ldcs(src + (s1 + u) * slab_stride);
     }
-    if (8 % G == 0) {
+    if (kFast) {  // G divides 8
         // each thread's eight rows are 8 / G whole lookahead steps (row =
         // step * G + head): their head maxima stay in registers, and the
         // Q8 threads of a token (adjacent lanes) add their terms by shuffles
@@ -624,13 +628,14 @@ cudaError_t launch_reduce(const Plan& pl, const int32_t* seq_off, void* ws, int 
     const int nq = (tok + 31) / 32;
     const size_t smem = sizeof(float) * (static_cast<size_t>(nq) * nslab * pl.Rs +
                                          static_cast<size_t>(tok) * (pl.Rs + 1));
+    auto kern = 8 % pl.G == 0 ? reduce_kernel<true> : reduce_kernel<false>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
     const unsigned grid = static_cast<unsigned>(pl.tiles_max * (kTileTokens / tok));
-    return launch_k(reduce_kernel, grid, kReduceThreads, smem, st, ws_ptr<uint16_t>(ws, pl.o_logits),
+    return launch_k(kern, grid, kReduceThreads, smem, st, ws_ptr<uint16_t>(ws, pl.o_logits),
                     ws_ptr<float>(ws, pl.o_lmax), ws_ptr<float>(ws, pl.o_lse), seq_off,
                     ws_ptr<int32_t>(ws, pl.o_tile_base), ws_ptr<float>(ws, pl.o_alog), imp, pl.B, pl.G, pl.L,
                     pl.R, pl.Rs, nslab, pl.Ntot, pl.tiles_max * kTileTokens, pl.tiles_max,
