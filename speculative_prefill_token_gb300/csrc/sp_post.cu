@@ -311,10 +311,11 @@ cudaError_t launch_post(const Plan& pl, const sp_params* p, const int32_t* seq_o
                         int32_t* kept_off, int32_t* n_kept, void* ws, cudaStream_t st) {
     PostArgs a = post_args(pl, p, seq_off, chunk_score, keep, kept_idx, kept_pos, kept_off, n_kept, ws);
     // Few slices: kRankSplitMax CTAs per slice, one warp per chunk, so that
-    // the ranking scans run on more SMs (2B workload 63.5 -> 62.9 us per
-    // call, 0.8B 35.3 -> 34.6); with more slices than that fills, every CTA
-    // rebuilding all chunk scores costs more than it saves (long workload
-    // 243.7 -> 251.0), so one CTA ranks the whole slice.
+    // the ranking scans run on more SMs (2B workload 63.3 -> 62.5 us per
+    // call, 0.8B 34.8 -> 34.4); with more slices than the SMs hold that way,
+    // every CTA rebuilding all chunk scores costs more than it saves (long
+    // workload 243.7 -> 251.0 with four CTAs per slice, 239.0 -> 240.4 with
+    // two), so one CTA ranks the whole slice.
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
